@@ -1,0 +1,195 @@
+/*
+ * convrot.h -- C ABI of the GB300 (sm_103a) INT8 ConvRot W8A8 linear layer.
+ *
+ * The layer (stable-diffusion.cpp docs "INT8 Convrot Safetensors",
+ * sections "How INT8 convrot works", "Weight quantization",
+ * "Runtime activation quantization"):
+ *
+ *   X_rot   = X R            R = block-diagonal, one normalized Kronecker power
+ *                            of H4 per contiguous group of G input features
+ *   s_x[r]  = max_i |X_rot[r,i]| / 127
+ *   Q_x     = clamp(round(X_rot / s_x), -127, 127)            (int8)
+ *   A[r,o]  = sum_i Q_x[r,i] * Q_w[o,i]                       (int32, exact)
+ *   Y[r,o]  = A[r,o] * s_x[r] * s_w[o] + b[o]                 (bf16 out)
+ *
+ * with Q_w, s_w produced the same way from W_rot = W R, one scale per output
+ * row. The block randomized Hadamard variant (gemma.cpp issue "Add
+ * experimental W8A8 MatMul with optional QuaRot-style rotation", section
+ * "Rotation method": +-1 signs, Walsh-Hadamard, 1/sqrt(B)) and the naive
+ * variant without rotation share the same quantizer and GEMM.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are caller-allocated device memory; the library
+ *    allocates nothing and keeps no state between calls except the device
+ *    error word read by convrot_get_device_status().
+ *  - Work is enqueued on the given stream and runs asynchronously. Argument
+ *    errors are detected on the host and returned BEFORE anything is
+ *    launched; CONVROT_ERR_CUDA reports a failed launch.
+ *  - Row-major layouts; K (the input-feature dimension) is contiguous.
+ *  - Rounding is round-half-to-even. A row whose absmax is 0 gets scale 0 and
+ *    all-zero codes. NaN/Inf inputs are outside the contract.
+ *  - There is no CPU fallback and no silent fallback to an unquantized path:
+ *    an unsupported configuration is an error.
+ */
+#ifndef CONVROT_H_
+#define CONVROT_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CONVROT_OK = 0,
+  CONVROT_ERR_INVALID_ARG = 1,       /* null pointer, bad size, mismatched operands */
+  CONVROT_ERR_UNSUPPORTED_GROUP = 2, /* G not a power of 4 (or 2 for RHT), G does not divide K, or G too large */
+  CONVROT_ERR_ALIGNMENT = 3,         /* pointer or leading dimension not aligned as documented */
+  CONVROT_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed */
+  CONVROT_ERR_TIMEOUT = 5            /* a bounded device-side wait gave up (see convrot_get_device_status) */
+} convrot_status;
+
+typedef enum {
+  /* Regular Hadamard: normalized Kronecker power of H4, G = 4^n
+   * ("INT8 Convrot Safetensors", "How INT8 convrot works"). */
+  CONVROT_T_REGULAR_H4 = 0,
+  /* Block randomized Hadamard: v -> H_B (D v) / sqrt(B), B = group = 2^m,
+   * D = diag(signs), H_B the Walsh-Hadamard matrix in natural order
+   * (gemma.cpp issue, "Rotation method"). */
+  CONVROT_T_RHT = 1,
+  /* No rotation: naive W8A8 (gemma.cpp issue, "Executive summary"). */
+  CONVROT_T_NONE = 2
+} convrot_transform;
+
+enum { CONVROT_DTYPE_F32 = 0, CONVROT_DTYPE_BF16 = 1 };
+
+/* Largest supported K (int32 accumulators cannot overflow: 127*127*K < 2^31
+ * for K <= 133143; the kernels further bound it by on-chip storage). */
+#define CONVROT_MAX_K 32768
+/* Largest supported group size. */
+#define CONVROT_MAX_GROUP 4096
+
+/* Packed activation ("Runtime activation quantization": the I8 rows and
+ * their floating-point row scales, reused by every linear with the same
+ * input and group size). All pointers are device pointers.
+ *   q      int8  [M, K], row stride K; 16-byte aligned.
+ *   scale  fp32  [M].
+ *   q_f16  fp16  [M, K] copy of q (integer-valued, exact) used as the
+ *          tensor-core operand; may be NULL, in which case the linear runs
+ *          the int8 warp-MMA path. 16-byte aligned. */
+typedef struct {
+  const int8_t* q;
+  const float* scale;
+  const uint16_t* q_f16;
+  int64_t M;
+  int64_t K;
+  int32_t group;
+  int32_t transform;
+} convrot_packed_act;
+
+/* Packed weight ("Weight quantization"): the same layout for the rotated,
+ * per-output-row-quantized weight. All pointers are device pointers.
+ *   q      int8  [N, K]; scale fp32 [N]; q_f16 fp16 [N, K] or NULL. */
+typedef struct {
+  const int8_t* q;
+  const float* scale;
+  const uint16_t* q_f16;
+  int64_t N;
+  int64_t K;
+  int32_t group;
+  int32_t transform;
+} convrot_packed_weight;
+
+/* Offline weight preparation ("How INT8 convrot works": W_rot = W R;
+ * "Weight quantization": s_w[o] = max|W_rot[o,:]|/127,
+ * Q_w = clamp(round(W_rot / s_w), -127, 127)).
+ *   W       device, [N, K] row-major, dtype CONVROT_DTYPE_F32 or _BF16.
+ *   signs   device int8 [group] of +-1 for CONVROT_T_RHT, else ignored (may be NULL).
+ *   Qw      device int8 [N, K] (out).   sw  device fp32 [N] (out).
+ *   Qw_f16  device fp16 [N, K] (out) or NULL.
+ * Errors: INVALID_ARG (null/sizes), UNSUPPORTED_GROUP, ALIGNMENT (any pointer
+ * not 16-byte aligned), CUDA. */
+convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N, int64_t K,
+                                       int32_t group, int32_t transform, const int8_t* signs,
+                                       int8_t* Qw, float* sw, uint16_t* Qw_f16,
+                                       cudaStream_t stream);
+
+/* Runtime activation rotation + per-row dynamic quantization
+ * ("Runtime activation quantization"), fused in one kernel.
+ *   X       device bf16 [M, K], row stride ldx elements (ldx >= K).
+ *   signs   device int8 [group] for CONVROT_T_RHT, else ignored.
+ *   Qx      device int8 [M, K] (out), sx device fp32 [M] (out),
+ *   Qx_f16  device fp16 [M, K] (out) or NULL.
+ * X must be 16-byte aligned with ldx a multiple of 8; the fastest path is
+ * taken when X is 32-byte aligned and ldx is a multiple of 16.
+ * M == 0 is a no-op. */
+convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                    int32_t group, int32_t transform, const int8_t* signs,
+                                    int8_t* Qx, float* sx, uint16_t* Qx_f16,
+                                    cudaStream_t stream);
+
+/* The H-as-a-matrix variant of convrot_quantize_act: each group is multiplied
+ * by the dense G x G rotation on the tensor cores ("feat: load ConvRot int4
+ * and per-channel int8 safetensors", section "The rotation": the rotation
+ * applied as one matmul against a shared constant), then quantized as above.
+ * Same arguments and results (up to fp32 rounding) as convrot_quantize_act;
+ * CONVROT_T_REGULAR_H4 with G in {16, 64, 256} only. Kept for comparison. */
+convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                            int32_t group, int8_t* Qx, float* sx,
+                                            uint16_t* Qx_f16, cudaStream_t stream);
+
+/* One linear: Y = A * s_x * s_w + b in bf16 ("Runtime activation
+ * quantization", reconstruction).
+ *   a, w    host pointers to descriptors of device data; a->K == w->K and
+ *           the group/transform of both must match.
+ *   bias    device fp32 [N] or NULL.
+ *   Y       device bf16 [M, N], row stride ldy >= N (multiple of 8, 16-byte aligned).
+ * The tensor-core path is used when both a->q_f16 and w->q_f16 are given and
+ * K is a multiple of 64; otherwise the int8 warp-MMA path. */
+convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_weight* w,
+                              const float* bias, uint16_t* Y, int64_t ldy, cudaStream_t stream);
+
+/* Several linears sharing one packed activation (qkv, gated-FFN pair:
+ * "Runtime activation quantization" on packed-tensor reuse; gemma.cpp
+ * "Implementation" on the fused gated-FFN pair), in one launch.
+ *   n       number of linears, 1..8.
+ *   w       host array [n] of weight descriptors.
+ *   bias    host array [n] of device fp32 pointers (entries may be NULL), or NULL.
+ *   Y       host array [n] of device bf16 outputs; ldy host array [n]. */
+convrot_status convrot_linear_multi(const convrot_packed_act* a, int32_t n,
+                                    const convrot_packed_weight* w, const float* const* bias,
+                                    uint16_t* const* Y, const int64_t* ldy,
+                                    cudaStream_t stream);
+
+/* Raw int32 accumulators A = Q_x Q_w^T through the same GEMM main loop the
+ * linear uses (no scaling). A device int32 [M, N], row stride lda >= N.
+ * Test and diagnostic entry point. */
+convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w,
+                                int32_t* A, int64_t lda, cudaStream_t stream);
+
+/* Reads and clears the device error word of the current device (synchronizes
+ * the device first). CONVROT_OK if no kernel reported a problem, else the
+ * first status a kernel recorded (e.g. CONVROT_ERR_TIMEOUT). */
+convrot_status convrot_get_device_status(void);
+
+/* Test hook for the bounded waits: launches one block that waits on an
+ * mbarrier nothing ever arrives on, with the given spin limit, on `stream`.
+ * The wait gives up, records CONVROT_ERR_TIMEOUT in the device error word
+ * and the kernel returns normally. */
+convrot_status convrot_selftest_wait_timeout(int64_t spin_limit, cudaStream_t stream);
+
+/* Static description of a status code. Never NULL. */
+const char* convrot_status_str(convrot_status s);
+
+/* Human-readable detail of the last error returned on this host thread. */
+const char* convrot_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t convrot_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVROT_H_ */

@@ -1,0 +1,281 @@
+"""GB300-native INT8 ConvRot W8A8 linear layer.
+
+A thin Python binding over ``libconvrot.so`` (C ABI declared in
+``include/convrot.h``). This module only marshals arguments: it allocates
+output tensors with PyTorch, passes raw device pointers and the current CUDA
+stream to the library, and turns status codes into exceptions. Every step of
+the layer (rotation, quantization, GEMM, reconstruction) runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback.
+
+The layer ("INT8 Convrot Safetensors", stable-diffusion.cpp docs, sections
+"How INT8 convrot works", "Weight quantization", "Runtime activation
+quantization"):
+
+    X_rot = X R, s_x = max|X_rot|/127 per row, Q_x = round(X_rot/s_x)
+    A = Q_x Q_w^T (int32),  Y = A * s_x * s_w + b   (bf16)
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+__all__ = [
+    "ConvRotError", "PackedAct", "PackedWeight", "ConvRotLinear", "TRANSFORMS",
+    "convrot_prepare_weights", "convrot_quantize_act", "convrot_quantize_act_hmatmul",
+    "convrot_linear", "convrot_linear_multi", "convrot_gemm_s32",
+    "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libconvrot.so")
+
+TRANSFORMS = {"h4": 0, "rht": 1, "none": 2}
+_DTYPE_F32, _DTYPE_BF16 = 0, 1
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_GROUP", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT"}
+
+
+class ConvRotError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"convrot {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(lib_path):
+        raise ImportError(
+            f"{lib_path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(nvcc, sm_103a). There is no fallback implementation.")
+    return ctypes.CDLL(lib_path)
+
+
+lib = _load()
+
+
+class _Act(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("q_f16", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("group", ctypes.c_int32),
+                ("transform", ctypes.c_int32)]
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("q_f16", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("group", ctypes.c_int32),
+                ("transform", ctypes.c_int32)]
+
+
+_P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+_SIGS = {
+    "convrot_prepare_weights": [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
+    "convrot_quantize_act": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
+    "convrot_quantize_act_hmatmul": [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P],
+    "convrot_linear": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _P, _I64, _P],
+    "convrot_linear_multi": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
+                             ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
+    "convrot_gemm_s32": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P],
+    "convrot_get_device_status": [],
+    "convrot_selftest_wait_timeout": [_I64, _P],
+    "convrot_status_str": [_I32],
+    "convrot_last_error": [],
+    "convrot_version": [],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_char_p if _name in ("convrot_status_str", "convrot_last_error") else ctypes.c_int32
+
+EXPORTED = tuple(_SIGS)
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = lib.convrot_last_error().decode(errors="replace")
+        raise ConvRotError(status, msg or lib.convrot_status_str(status).decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _transform_id(transform) -> int:
+    if isinstance(transform, int):
+        return transform
+    return TRANSFORMS[transform]
+
+
+@dataclasses.dataclass
+class PackedAct:
+    """{int8 rows, fp32 row scales} (+ fp16 operand copy), reusable by every
+    linear that shares the input and the group size."""
+    q: torch.Tensor
+    scale: torch.Tensor
+    q_f16: Optional[torch.Tensor]
+    group: int
+    transform: int
+
+    @property
+    def M(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.q.shape[1]
+
+    def _c(self) -> _Act:
+        return _Act(_ptr(self.q), _ptr(self.scale), _ptr(self.q_f16), self.M, self.K, self.group, self.transform)
+
+
+@dataclasses.dataclass
+class PackedWeight:
+    q: torch.Tensor
+    scale: torch.Tensor
+    q_f16: Optional[torch.Tensor]
+    group: int
+    transform: int
+
+    @property
+    def N(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.q.shape[1]
+
+    def _c(self) -> _Weight:
+        return _Weight(_ptr(self.q), _ptr(self.scale), _ptr(self.q_f16), self.N, self.K, self.group,
+                       self.transform)
+
+
+def convrot_prepare_weights(W: torch.Tensor, group: int, transform="h4", signs: Optional[torch.Tensor] = None,
+                            with_f16: bool = True, stream=None) -> PackedWeight:
+    """Offline path: W_rot = W R, per-output-row int8 (Q_w, s_w)."""
+    if W.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("W must be fp32 or bf16")
+    W = W.contiguous()
+    N, K = W.shape
+    t = _transform_id(transform)
+    q = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    s = torch.empty((N,), dtype=torch.float32, device=W.device)
+    q16 = torch.empty((N, K), dtype=torch.float16, device=W.device) if with_f16 else None
+    _check(lib.convrot_prepare_weights(W.data_ptr(), _DTYPE_F32 if W.dtype == torch.float32 else _DTYPE_BF16,
+                                       N, K, group, t, _ptr(signs), q.data_ptr(), s.data_ptr(), _ptr(q16),
+                                       _stream(stream)))
+    return PackedWeight(q, s, q16, group, t)
+
+
+def convrot_quantize_act(X: torch.Tensor, group: int, transform="h4", signs: Optional[torch.Tensor] = None,
+                         with_f16: bool = True, out: Optional[PackedAct] = None, stream=None) -> PackedAct:
+    """Runtime path: fused X_rot = X R, per-row absmax scale, int8 codes."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2:
+        raise TypeError("X must be a 2-D bf16 tensor")
+    if X.stride(1) != 1:
+        X = X.contiguous()
+    M, K = X.shape
+    t = _transform_id(transform)
+    if out is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        s = torch.empty((M,), dtype=torch.float32, device=X.device)
+        q16 = torch.empty((M, K), dtype=torch.float16, device=X.device) if with_f16 else None
+        out = PackedAct(q, s, q16, group, t)
+    _check(lib.convrot_quantize_act(X.data_ptr(), M, K, X.stride(0), group, t, _ptr(signs), out.q.data_ptr(),
+                                    out.scale.data_ptr(), _ptr(out.q_f16), _stream(stream)))
+    return out
+
+
+def convrot_quantize_act_hmatmul(X: torch.Tensor, group: int, with_f16: bool = True, stream=None) -> PackedAct:
+    """Same result as convrot_quantize_act (regular Hadamard), with the
+    rotation applied as a dense G x G matmul on the tensor cores."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2:
+        raise TypeError("X must be a 2-D bf16 tensor")
+    if X.stride(1) != 1:
+        X = X.contiguous()
+    M, K = X.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    s = torch.empty((M,), dtype=torch.float32, device=X.device)
+    q16 = torch.empty((M, K), dtype=torch.float16, device=X.device) if with_f16 else None
+    _check(lib.convrot_quantize_act_hmatmul(X.data_ptr(), M, K, X.stride(0), group, q.data_ptr(), s.data_ptr(),
+                                            _ptr(q16), _stream(stream)))
+    return PackedAct(q, s, q16, group, TRANSFORMS["h4"])
+
+
+def convrot_linear(a: PackedAct, w: PackedWeight, bias: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y = A * s_x * s_w + b (bf16) for one linear."""
+    if out is None:
+        out = torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q.device)
+    ca, cw = a._c(), w._c()
+    _check(lib.convrot_linear(ctypes.byref(ca), ctypes.byref(cw), _ptr(bias), out.data_ptr(), out.stride(0),
+                              _stream(stream)))
+    return out
+
+
+def convrot_linear_multi(a: PackedAct, ws: Sequence[PackedWeight], biases: Optional[Sequence] = None,
+                         outs: Optional[List[torch.Tensor]] = None, stream=None) -> List[torch.Tensor]:
+    """Several linears sharing one packed activation, in one launch."""
+    n = len(ws)
+    if outs is None:
+        outs = [torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q.device) for w in ws]
+    warr = (_Weight * n)(*[w._c() for w in ws])
+    barr = (ctypes.c_void_p * n)(*[(_ptr(b) if b is not None else None) for b in (biases or [None] * n)])
+    yarr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    larr = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
+    ca = a._c()
+    _check(lib.convrot_linear_multi(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
+    return outs
+
+
+def convrot_gemm_s32(a: PackedAct, w: PackedWeight, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Raw int32 accumulators A = Q_x Q_w^T through the linear's GEMM main loop."""
+    if out is None:
+        out = torch.empty((a.M, w.N), dtype=torch.int32, device=a.q.device)
+    ca, cw = a._c(), w._c()
+    _check(lib.convrot_gemm_s32(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
+                                _stream(stream)))
+    return out
+
+
+def convrot_get_device_status() -> int:
+    """Synchronizes, then reads and clears the library's device error word."""
+    return int(lib.convrot_get_device_status())
+
+
+def convrot_selftest_wait_timeout(spin_limit: int, stream=None) -> None:
+    _check(lib.convrot_selftest_wait_timeout(spin_limit, _stream(stream)))
+
+
+class ConvRotLinear:
+    """A linear layer holding prepared ConvRot weights.
+
+    ``forward`` flattens leading dimensions, quantizes the activation once and
+    runs the int8 GEMM with the fused epilogue, then restores the shape.
+    """
+
+    def __init__(self, packed: PackedWeight, bias: Optional[torch.Tensor], signs: Optional[torch.Tensor] = None):
+        self.weight = packed
+        self.bias = None if bias is None else bias.to(device=packed.q.device, dtype=torch.float32).contiguous()
+        self.signs = signs
+
+    @classmethod
+    def from_float(cls, W: torch.Tensor, bias: Optional[torch.Tensor], group: int, transform="h4",
+                   signs: Optional[torch.Tensor] = None, with_f16: bool = True) -> "ConvRotLinear":
+        if W.dtype == torch.int8:
+            raise TypeError("weight is already quantized; build ConvRotLinear from a PackedWeight instead")
+        return cls(convrot_prepare_weights(W, group, transform, signs, with_f16), bias, signs)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        shape = x.shape
+        x2 = x.reshape(-1, shape[-1])
+        a = convrot_quantize_act(x2, self.weight.group, self.weight.transform, self.signs,
+                                 with_f16=self.weight.q_f16 is not None)
+        y = convrot_linear(a, self.weight, self.bias)
+        return y.reshape(*shape[:-1], y.shape[-1])
+
+    __call__ = forward

@@ -1,0 +1,281 @@
+// extern "C" entry points of libconvrot: argument validation, path choice and
+// launches. Every check happens on the host before anything is enqueued.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "gemm_common.cuh"
+
+namespace convrot {
+
+cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, long long ldx, int G, int transform,
+                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic,
+                            cudaStream_t st, int* path);
+cudaError_t hmatmul_launch(const void* X, long long M, int K, long long ldx, int G, int8_t* Q, float* S,
+                           uint16_t* Q16, cudaStream_t st);
+cudaError_t gemm_mma_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
+                            bool raw, cudaStream_t st);
+cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
+                           bool raw, cudaStream_t st);
+bool gemm_tc_supported(long long M, int K);
+cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st);
+
+CONVROT_DEFINE_STATUS_WORD(status_word_api)
+
+}  // namespace convrot
+
+using namespace convrot;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+convrot_status fail(convrot_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+convrot_status ok() {
+  g_last_error[0] = '\0';
+  return CONVROT_OK;
+}
+
+convrot_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(CONVROT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
+bool is_pow4(long long v) { return is_pow2(v) && (__builtin_ctzll(static_cast<unsigned long long>(v)) % 2) == 0; }
+
+// Group rules: "INT8 Convrot Safetensors", "Checkpoint format" (power of
+// four dividing the input features); gemma.cpp issue, "Rotation method"
+// (block transform only when K is divisible by the block).
+convrot_status check_shape(long long K, int group, int transform) {
+  if (K <= 0 || K > CONVROT_MAX_K) return fail(CONVROT_ERR_INVALID_ARG, "K=%lld outside [1, %d]", K, CONVROT_MAX_K);
+  if (K % 16) return fail(CONVROT_ERR_ALIGNMENT, "K=%lld must be a multiple of 16", K);
+  switch (transform) {
+    case CONVROT_T_REGULAR_H4:
+      if (group < 4 || group > CONVROT_MAX_GROUP || !is_pow4(group))
+        return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "group %d is not a power of four in [4, %d]", group,
+                    CONVROT_MAX_GROUP);
+      if (K % group) return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "group %d does not divide K=%lld", group, K);
+      return CONVROT_OK;
+    case CONVROT_T_RHT:
+      if (group < 2 || group > CONVROT_MAX_GROUP || !is_pow2(group))
+        return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "block %d is not a power of two in [2, %d]", group,
+                    CONVROT_MAX_GROUP);
+      if (K % group) return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "block %d does not divide K=%lld", group, K);
+      return CONVROT_OK;
+    case CONVROT_T_NONE:
+      return CONVROT_OK;
+    default:
+      return fail(CONVROT_ERR_INVALID_ARG, "unknown transform %d", transform);
+  }
+}
+
+convrot_status check_pair(const convrot_packed_act* a, const convrot_packed_weight* w) {
+  if (!a || !w) return fail(CONVROT_ERR_INVALID_ARG, "null descriptor");
+  if (!a->q || !a->scale) return fail(CONVROT_ERR_INVALID_ARG, "activation q/scale is null");
+  if (!w->q || !w->scale) return fail(CONVROT_ERR_INVALID_ARG, "weight q/scale is null");
+  if (a->M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(a->M));
+  if (w->N <= 0) return fail(CONVROT_ERR_INVALID_ARG, "N=%lld must be >= 1", static_cast<long long>(w->N));
+  if (a->K != w->K)
+    return fail(CONVROT_ERR_INVALID_ARG, "K mismatch: activation %lld, weight %lld", static_cast<long long>(a->K),
+                static_cast<long long>(w->K));
+  if (a->transform != w->transform || (a->transform != CONVROT_T_NONE && a->group != w->group))
+    return fail(CONVROT_ERR_INVALID_ARG, "activation and weight were rotated differently (group %d/%d, transform %d/%d)",
+                a->group, w->group, a->transform, w->transform);
+  convrot_status s = check_shape(a->K, a->group, a->transform);
+  if (s != CONVROT_OK) return s;
+  if (!aligned(a->q, 16) || !aligned(w->q, 16) || (a->q_f16 && !aligned(a->q_f16, 16)) ||
+      (w->q_f16 && !aligned(w->q_f16, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "operand pointers must be 16-byte aligned");
+  if (!aligned(a->scale, 4) || !aligned(w->scale, 4)) return fail(CONVROT_ERR_ALIGNMENT, "scale pointers must be 4-byte aligned");
+  return CONVROT_OK;
+}
+
+convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw, cudaStream_t stream) {
+  if (a->M == 0) return ok();
+  bool all_f16 = a->q_f16 != nullptr;
+  for (int i = 0; i < outs.count; ++i) all_f16 = all_f16 && outs.o[i].qw16 != nullptr;
+  cudaError_t e;
+  if (all_f16 && gemm_tc_supported(a->M, static_cast<int>(a->K))) {
+    e = gemm_tc_launch(a->q_f16, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
+  } else {
+    e = gemm_mma_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 MMA GEMM launch");
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t convrot_version(void) { return 100; }
+
+const char* convrot_status_str(convrot_status s) {
+  switch (s) {
+    case CONVROT_OK: return "ok";
+    case CONVROT_ERR_INVALID_ARG: return "invalid argument";
+    case CONVROT_ERR_UNSUPPORTED_GROUP: return "unsupported group size";
+    case CONVROT_ERR_ALIGNMENT: return "misaligned pointer or size";
+    case CONVROT_ERR_CUDA: return "CUDA error";
+    case CONVROT_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* convrot_last_error(void) { return g_last_error; }
+
+convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N, int64_t K, int32_t group,
+                                       int32_t transform, const int8_t* signs, int8_t* Qw, float* sw,
+                                       uint16_t* Qw_f16, cudaStream_t stream) {
+  if (!W || !Qw || !sw) return fail(CONVROT_ERR_INVALID_ARG, "W, Qw and sw must be non-null");
+  if (w_dtype != CONVROT_DTYPE_F32 && w_dtype != CONVROT_DTYPE_BF16)
+    return fail(CONVROT_ERR_INVALID_ARG, "w_dtype %d is neither fp32 nor bf16", w_dtype);
+  if (N <= 0) return fail(CONVROT_ERR_INVALID_ARG, "N=%lld must be >= 1", static_cast<long long>(N));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (transform == CONVROT_T_RHT && !signs) return fail(CONVROT_ERR_INVALID_ARG, "RHT needs the sign vector");
+  if (!aligned(W, 16) || !aligned(Qw, 16) || !aligned(sw, 4) || (Qw_f16 && !aligned(Qw_f16, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "pointers must be 16-byte aligned (scales 4-byte)");
+  int path = 0;
+  cudaError_t e = rotquant_launch(W, w_dtype, N, static_cast<int>(K), K, group, transform, signs, Qw, sw, Qw_f16,
+                                  w_dtype == CONVROT_DTYPE_F32, stream, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "weight rotate/quantize launch");
+  return ok();
+}
+
+convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                    int32_t transform, const int8_t* signs, int8_t* Qx, float* sx,
+                                    uint16_t* Qx_f16, cudaStream_t stream) {
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (M == 0) return ok();
+  if (!X || !Qx || !sx) return fail(CONVROT_ERR_INVALID_ARG, "X, Qx and sx must be non-null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (transform == CONVROT_T_RHT && !signs) return fail(CONVROT_ERR_INVALID_ARG, "RHT needs the sign vector");
+  if (!aligned(X, 16) || ldx % 8 || !aligned(Qx, 16) || !aligned(sx, 4) || (Qx_f16 && !aligned(Qx_f16, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "X, Qx, Qx_f16 must be 16-byte aligned and ldx a multiple of 8");
+  int path = 0;
+  cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs, Qx,
+                                  sx, Qx_f16, 0, stream, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "activation rotate/quantize launch");
+  return ok();
+}
+
+convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                            int8_t* Qx, float* sx, uint16_t* Qx_f16, cudaStream_t stream) {
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, CONVROT_T_REGULAR_H4);
+  if (s != CONVROT_OK) return s;
+  if (group != 16 && group != 64 && group != 256)
+    return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "the matmul variant supports G in {16, 64, 256}, got %d", group);
+  if (M == 0) return ok();
+  if (!X || !Qx || !sx) return fail(CONVROT_ERR_INVALID_ARG, "X, Qx and sx must be non-null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (!aligned(X, 16) || ldx % 8 || !aligned(Qx, 16) || !aligned(sx, 4) || (Qx_f16 && !aligned(Qx_f16, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "X, Qx, Qx_f16 must be 16-byte aligned and ldx a multiple of 8");
+  cudaError_t e = hmatmul_launch(X, M, static_cast<int>(K), ldx, group, Qx, sx, Qx_f16, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "matmul rotate/quantize launch");
+  return ok();
+}
+
+convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_weight* w, const float* bias,
+                              uint16_t* Y, int64_t ldy, cudaStream_t stream) {
+  convrot_status s = check_pair(a, w);
+  if (s != CONVROT_OK) return s;
+  if (a->M > 0 && !Y) return fail(CONVROT_ERR_INVALID_ARG, "Y is null");
+  if (ldy < w->N) return fail(CONVROT_ERR_INVALID_ARG, "ldy=%lld < N=%lld", static_cast<long long>(ldy), static_cast<long long>(w->N));
+  if (!aligned(Y, 16) || ldy % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y must be 16-byte aligned and ldy a multiple of 8");
+  if (bias && !aligned(bias, 4)) return fail(CONVROT_ERR_ALIGNMENT, "bias must be 4-byte aligned");
+  GemmOutputs outs{};
+  outs.count = 1;
+  outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, bias, Y, ldy, static_cast<int>(w->N), 0};
+  return run_gemm(a, outs, false, stream);
+}
+
+convrot_status convrot_linear_multi(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                                    const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
+                                    cudaStream_t stream) {
+  if (n < 1 || n > kMaxLinears) return fail(CONVROT_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, kMaxLinears);
+  if (!w || !Y || !ldy) return fail(CONVROT_ERR_INVALID_ARG, "w, Y and ldy arrays must be non-null");
+  GemmOutputs outs{};
+  outs.count = n;
+  for (int i = 0; i < n; ++i) {
+    convrot_status s = check_pair(a, &w[i]);
+    if (s != CONVROT_OK) return s;
+    const float* b = bias ? bias[i] : nullptr;
+    if (a->M > 0 && !Y[i]) return fail(CONVROT_ERR_INVALID_ARG, "Y[%d] is null", i);
+    if (ldy[i] < w[i].N) return fail(CONVROT_ERR_INVALID_ARG, "ldy[%d] < N", i);
+    if (!aligned(Y[i], 16) || ldy[i] % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y[%d] alignment", i);
+    if (b && !aligned(b, 4)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] alignment", i);
+    outs.o[i] = GemmOut{w[i].q, w[i].q_f16, w[i].scale, b, Y[i], ldy[i], static_cast<int>(w[i].N), 0};
+  }
+  return run_gemm(a, outs, false, stream);
+}
+
+convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
+                                int64_t lda, cudaStream_t stream) {
+  convrot_status s = check_pair(a, w);
+  if (s != CONVROT_OK) return s;
+  if (a->M > 0 && !A) return fail(CONVROT_ERR_INVALID_ARG, "A is null");
+  if (lda < w->N) return fail(CONVROT_ERR_INVALID_ARG, "lda < N");
+  if (!aligned(A, 16) || lda % 4) return fail(CONVROT_ERR_ALIGNMENT, "A must be 16-byte aligned and lda a multiple of 4");
+  GemmOutputs outs{};
+  outs.count = 1;
+  outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, nullptr, A, lda, static_cast<int>(w->N), 0};
+  return run_gemm(a, outs, true, stream);
+}
+
+convrot_status convrot_get_device_status(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int words[4] = {status_word_rotquant(), status_word_gemm_mma(), status_word_gemm_tc(), status_word_api()};
+  for (int w : words) {
+    if (w != 0) {
+      return fail(static_cast<convrot_status>(w), "a kernel recorded status %d (%s)", w,
+                  convrot_status_str(static_cast<convrot_status>(w)));
+    }
+  }
+  return ok();
+}
+
+convrot_status convrot_selftest_wait_timeout(int64_t spin_limit, cudaStream_t stream) {
+  if (spin_limit < 1 || spin_limit > (1ll << 30)) return fail(CONVROT_ERR_INVALID_ARG, "spin_limit out of range");
+  cudaError_t e = selftest_wait_launch(spin_limit, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ok();
+}
+
+}  // extern "C"
+
+namespace convrot {
+
+// One warp waits on an mbarrier that expects one arrival nobody makes. The
+// bounded wait gives up, records CONVROT_ERR_TIMEOUT and the kernel ends.
+__global__ void selftest_wait_kernel(long long spin_limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) mbar_init(&bar, 1);
+  __syncwarp();
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+  const bool done = mbar_wait_bounded(&bar, 0, spin_limit);
+  if (!done && threadIdx.x == 0) record_status(CONVROT_ERR_TIMEOUT);
+}
+
+cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(spin_limit);
+  return cudaGetLastError();
+}
+
+}  // namespace convrot

@@ -1,0 +1,138 @@
+// Internal helpers shared by the CUDA translation units of libconvrot.
+// Nothing here is part of the public ABI (see include/convrot.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/convrot.h"
+
+namespace convrot {
+
+// ---------------------------------------------------------------- status ----
+// Each translation unit owns a device error word (internal linkage, no
+// relocatable device code needed). Kernels record the first failure with
+// atomicCAS; the host reads and clears every unit's word through the
+// functions declared below.
+#define CONVROT_DEFINE_STATUS_WORD(NAME)                                         \
+  static __device__ int g_status_word;                                           \
+  __device__ __forceinline__ void record_status(int code) {                      \
+    atomicCAS(&g_status_word, 0, code);                                          \
+  }                                                                              \
+  int NAME() {                                                                   \
+    int v = 0, z = 0;                                                            \
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess)     \
+      return CONVROT_ERR_CUDA;                                                   \
+    if (v != 0 && cudaMemcpyToSymbol(g_status_word, &z, sizeof(int)) != cudaSuccess) \
+      return CONVROT_ERR_CUDA;                                                   \
+    return v;                                                                    \
+  }
+
+int status_word_rotquant();
+int status_word_gemm_mma();
+int status_word_gemm_tc();
+
+// Spin limit of every bounded device-side wait (iterations of a try_wait
+// loop with nanosleep back-off); about a second on a GB300.
+constexpr long long kDefaultSpinLimit = 1ll << 22;
+
+// ------------------------------------------------------------- small math --
+__host__ __device__ constexpr int ilog2_c(int v) { return v <= 1 ? 0 : 1 + ilog2_c(v >> 1); }
+__host__ __device__ constexpr int ilog4_c(int v) { return v <= 1 ? 0 : 1 + ilog4_c(v >> 2); }
+
+// Rounding of a pre-scaled code to int8 without a conversion instruction:
+// t = fma(y, inv, 1.5 * 2^23) is the exact product y*inv rounded once to the
+// nearest integer (ties to even, since 1.5*2^23 is even and the fp32 ulp on
+// [2^23, 2^24) is 1), and the low byte of t's bits is that integer in two's
+// complement, valid for |y*inv| < 2^22.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+
+__device__ __forceinline__ int code_from_magic(float t) {
+  return static_cast<int>(__float_as_uint(t) - kRoundMagicBits);
+}
+
+// ------------------------------------------------------- packed fp32 math --
+// add/sub/fma on two fp32 lanes at once (sm_100+ packed fp32 pipe). Each lane
+// is an ordinary IEEE fp32 operation, bit-identical to the scalar one.
+__device__ __forceinline__ unsigned long long f2_pack(float2 a) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// ------------------------------------------------------------ memory ops --
+struct alignas(32) U32x8 { uint32_t w[8]; };
+
+// 32-byte read-only load (sm_100+), no L1 allocation: streaming input.
+__device__ __forceinline__ U32x8 ldg_nc_256(const void* p) {
+  U32x8 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]),
+                 "=r"(r.w[4]), "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void stg_128(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// bf16 pair in one 32-bit word -> two fp32 (exact widening).
+__device__ __forceinline__ float bf16lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ------------------------------------------------------------ mbarriers ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on an mbarrier phase. Returns false after `limit` failed
+// polls (the caller records CONVROT_ERR_TIMEOUT and winds down).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, long long limit) {
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, phase)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+}  // namespace convrot

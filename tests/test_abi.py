@@ -1,0 +1,92 @@
+"""Host-side checks of the C-ABI library: it loads, exports every entry point
+declared in include/convrot.h, and rejects bad arguments on the host before
+touching the GPU. Needs no GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "convrot.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(convrot_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def cr():
+    import int8_convrot_w8a8_gb300 as cr
+    return cr
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["convrot_prepare_weights", "convrot_quantize_act", "convrot_linear",
+                     "convrot_linear_multi", "convrot_gemm_s32", "convrot_get_device_status"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(cr):
+    raw = ctypes.CDLL(cr.lib_path)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+    assert set(declared_functions()) == set(cr.EXPORTED)
+
+
+def test_version_and_status_strings(cr):
+    assert cr.lib.convrot_version() == 100
+    for code in range(6):
+        assert cr.lib.convrot_status_str(code)
+    assert cr.lib.convrot_status_str(99) == b"unknown status"
+
+
+def _qa(cr, M=4, K=256, ldx=256, group=256, transform=0, X=0x1000, Qx=0x2000, sx=0x3000, signs=None):
+    return cr.lib.convrot_quantize_act(X, M, K, ldx, group, transform, signs, Qx, sx, None, None)
+
+
+def test_host_validation_rejects_bad_groups(cr):
+    assert _qa(cr, group=8) == 2                    # not a power of four
+    assert _qa(cr, K=2688, ldx=2688, group=256) == 2  # does not divide K
+    assert _qa(cr, group=8192, K=8192, ldx=8192) == 2  # too large
+    assert _qa(cr, transform=1, group=96, K=1152, ldx=1152) == 2  # RHT block not a power of two
+    assert b"power of two" in cr.lib.convrot_last_error()
+    assert _qa(cr, group=8) == 2
+    assert b"power of four" in cr.lib.convrot_last_error()
+
+
+def test_host_validation_rejects_bad_arguments(cr):
+    assert _qa(cr, K=100, ldx=100, group=4) == 3     # K % 16
+    assert _qa(cr, X=0x1001) == 3                    # misaligned X
+    assert _qa(cr, ldx=100) == 1                     # ldx < K
+    assert _qa(cr, X=None) == 1                      # null input
+    assert _qa(cr, M=-1) == 1
+    assert _qa(cr, transform=7) == 1
+    assert _qa(cr, transform=1, group=128, K=1152, ldx=1152, signs=None) == 1  # RHT without signs
+    assert _qa(cr, K=40000, ldx=40000, transform=2) == 1  # K above the maximum
+
+
+def test_empty_batch_is_a_no_op(cr):
+    assert _qa(cr, M=0, X=None, Qx=None, sx=None) == 0
+
+
+def test_linear_validation(cr):
+    act = cr._Act(0x1000, 0x2000, None, 4, 256, 256, 0)
+    w_ok = cr._Weight(0x4000, 0x5000, None, 16, 256, 256, 0)
+    w_k = cr._Weight(0x4000, 0x5000, None, 16, 512, 256, 0)
+    w_g = cr._Weight(0x4000, 0x5000, None, 16, 256, 64, 0)
+    f = cr.lib.convrot_linear
+    assert f(ctypes.byref(act), ctypes.byref(w_k), None, 0x8000, 16, None) == 1   # K mismatch
+    assert f(ctypes.byref(act), ctypes.byref(w_g), None, 0x8000, 16, None) == 1   # group mismatch
+    assert f(ctypes.byref(act), ctypes.byref(w_ok), None, 0x8000, 8, None) == 1   # ldy < N
+    assert f(ctypes.byref(act), ctypes.byref(w_ok), None, 0x8004, 16, None) == 3  # misaligned Y
+    assert f(None, ctypes.byref(w_ok), None, 0x8000, 16, None) == 1
+    n_bad = cr.lib.convrot_linear_multi(ctypes.byref(act), 9, None, None, None, None, None)
+    assert n_bad == 1
+
+
+def test_selftest_argument_check(cr):
+    assert cr.lib.convrot_selftest_wait_timeout(0, None) == 1

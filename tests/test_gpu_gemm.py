@@ -1,0 +1,207 @@
+"""Parity of the int8 GEMM + fused epilogue with the CPU oracle.
+
+The accumulators must be bit-exact when the GPU is fed the oracle's codes;
+Y from those codes must match the oracle's fp64 reconstruction within one
+bf16 ulp; end to end from X, Y must be within 1e-2 of max|Y|. Every check
+runs on both GEMM paths: the tensor-core path (fp16 operand copies given)
+and the int8 warp-MMA path (no copies)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+from parity import check_codes, check_y_e2e, check_y_same_codes, to_np
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ["tc", "mma"]
+
+
+@pytest.fixture(scope="module")
+def cr():
+    import int8_convrot_w8a8_gb300 as cr
+    return cr
+
+
+def packed_from_codes(cr, Q, s, G, transform, f16, kind):
+    q = torch.from_numpy(np.ascontiguousarray(Q)).cuda()
+    sc = torch.from_numpy(np.ascontiguousarray(s.astype(np.float32))).cuda()
+    q16 = q.to(torch.float16) if f16 else None
+    t = cr.TRANSFORMS[transform]
+    cls = cr.PackedAct if kind == "act" else cr.PackedWeight
+    return cls(q, sc, q16, G, t)
+
+
+def oracle_case(wl, i=0):
+    sg = None if wl.signs is None else wl.signs.numpy()
+    X64 = wl.X.float().numpy().astype(np.float64)
+    W64 = wl.weights[i].numpy().astype(np.float64)
+    Qw, sw, _ = O.prepare_weights(W64, wl.group, wl.transform, sg)
+    Qx, sx, v = O.quantize_act(X64, wl.group, wl.transform, sg)
+    return Qx, sx, v, Qw, sw
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,N,K", [(64, 256, 256), (200, 384, 1024), (129, 300, 3072), (16, 1000, 1152),
+                                   (1, 64, 256), (300, 128, 6144), (257, 136, 2688)])
+def test_gemm_s32_bit_exact_on_oracle_codes(cr, path, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    Qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", path == "tc", "act")
+    w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", path == "tc", "w")
+    A = to_np(cr.convrot_gemm_s32(a, w))
+    assert np.array_equal(A.astype(np.int64), O.int_gemm(Qx, Qw))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("K", [1024, 1040, 3072, 6144])
+def test_gemm_s32_adversarial_magnitudes(cr, path, K):
+    """All-127 rows give |A| = 16129 K, far above 2^24 for K = 6144: any
+    accumulation that is not exact over the whole K shows up here. Mixed
+    rows put large and small partial sums next to each other."""
+    M, N = 130, 136
+    Qx = np.full((M, K), 127, dtype=np.int8)
+    Qx[1::2] = -127
+    Qx[2::5, ::3] = 1
+    Qw = np.full((N, K), 127, dtype=np.int8)
+    Qw[3::4] = -127
+    Qw[5::7, 1::2] = -1
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", path == "tc", "act")
+    w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", path == "tc", "w")
+    A = to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64)
+    ref = O.int_gemm(Qx, Qw)
+    assert np.array_equal(A, ref)
+    assert np.abs(ref).max() == 16129 * K
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", ["tiny", "dit", "ffn_rht", "g64_2688"])
+def test_linear_on_oracle_codes(cr, path, case):
+    wl = {"tiny": lambda: WL.tiny(),
+          "dit": lambda: WL.dit6144(M=96),
+          "ffn_rht": lambda: WL.ffn_pair(),
+          "g64_2688": lambda: WL.k2688(M=70)}[case]()
+    Qx, sx, v, Qw, sw = oracle_case(wl)
+    a = packed_from_codes(cr, Qx, sx, wl.group, wl.transform, path == "tc", "act")
+    w = packed_from_codes(cr, Qw, sw, wl.group, wl.transform, path == "tc", "w")
+    bias = wl.biases[0]
+    Y = cr.convrot_linear(a, w, bias.cuda())
+    A = O.int_gemm(Qx, Qw)
+    assert np.array_equal(to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64), A)
+    check_y_same_codes(to_np(Y.float()), A, sx, sw, bias.numpy(), f"{case}/{path}")
+    Y0 = cr.convrot_linear(a, w, None)
+    check_y_same_codes(to_np(Y0.float()), A, sx, sw, None, f"{case}/{path}/nobias")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", ["tiny", "dit", "ffn_rht", "g16", "g1024"])
+def test_linear_end_to_end(cr, path, case):
+    wl = {"tiny": lambda: WL.tiny(),
+          "dit": lambda: WL.dit6144(M=200),
+          "ffn_rht": lambda: WL.ffn_pair(),
+          "g16": lambda: WL.gsweep(16, M=130),
+          "g1024": lambda: WL.gsweep(1024, M=130)}[case]()
+    f16 = path == "tc"
+    sg = None if wl.signs is None else wl.signs.cuda()
+    pw = cr.convrot_prepare_weights(wl.weights[0].cuda(), wl.group, wl.transform, sg, with_f16=f16)
+    a = cr.convrot_quantize_act(wl.X.cuda(), wl.group, wl.transform, sg, with_f16=f16)
+    Y = cr.convrot_linear(a, pw, wl.biases[0].cuda())
+    Qx, sx, v, Qw, sw = oracle_case(wl)
+    ref = O.reconstruct(O.int_gemm(Qx, Qw), sx, sw, wl.biases[0].numpy())
+    check_codes(to_np(a.q), Qx, v, case)
+    check_y_e2e(to_np(Y.float()), ref, case)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_linear_multi_equals_separate_calls_and_concatenation(cr, path):
+    wl = WL.qkv32700(M=300)
+    f16 = path == "tc"
+    a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4", with_f16=f16)
+    ws = [cr.convrot_prepare_weights(W.cuda(), 256, "h4", with_f16=f16) for W in wl.weights]
+    bs = [b.cuda() for b in wl.biases]
+    Ys = cr.convrot_linear_multi(a, ws, bs)
+    for Y, w, b in zip(Ys, ws, bs):
+        assert torch.equal(Y, cr.convrot_linear(a, w, b))
+    cat = cr.PackedWeight(torch.cat([w.q for w in ws]), torch.cat([w.scale for w in ws]),
+                          torch.cat([w.q_f16 for w in ws]) if f16 else None, 256, 0)
+    Ycat = cr.convrot_linear(a, cat, torch.cat(bs))
+    assert torch.equal(Ycat, torch.cat(Ys, dim=1))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_row_split_is_bit_identical(cr, path):
+    """Every row's arithmetic is the same however the rows are split (the
+    sglang digest's row split of large-M calls)."""
+    wl = WL.dit6144(M=300)
+    f16 = path == "tc"
+    pw = cr.convrot_prepare_weights(wl.weights[0][:512].cuda(), 256, "h4", with_f16=f16)
+    X = wl.X.cuda()
+    full = cr.convrot_linear(cr.convrot_quantize_act(X, 256, "h4", with_f16=f16), pw)
+    parts = [cr.convrot_linear(cr.convrot_quantize_act(X[r:r + 100], 256, "h4", with_f16=f16), pw)
+             for r in range(0, 300, 100)]
+    assert torch.equal(full, torch.cat(parts))
+
+
+def test_paths_agree(cr):
+    wl = WL.dit6144(M=257)
+    pw = cr.convrot_prepare_weights(wl.weights[0][:640].cuda(), 256, "h4", with_f16=True)
+    a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4", with_f16=True)
+    a_int8 = cr.PackedAct(a.q, a.scale, None, a.group, a.transform)
+    assert torch.equal(cr.convrot_gemm_s32(a, pw), cr.convrot_gemm_s32(a_int8, pw))
+    assert torch.equal(cr.convrot_linear(a, pw), cr.convrot_linear(a_int8, pw))
+
+
+def test_output_stride_and_empty(cr):
+    wl = WL.dit6144(M=40)
+    pw = cr.convrot_prepare_weights(wl.weights[0][:200].cuda(), 256, "h4")
+    a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4")
+    big = torch.full((40, 264), 7.0, dtype=torch.bfloat16, device="cuda")
+    Y = cr.convrot_linear(a, pw, out=big[:, :200])
+    assert torch.equal(Y, cr.convrot_linear(a, pw))
+    assert torch.all(big[:, 200:] == 7.0)
+    e = cr.convrot_quantize_act(torch.empty((0, 6144), dtype=torch.bfloat16, device="cuda"), 256, "h4")
+    assert cr.convrot_linear(e, pw).shape == (0, 200)
+
+
+def test_convrot_linear_module_flattens_leading_dims(cr):
+    wl = WL.dit6144(M=64)
+    lin = cr.ConvRotLinear.from_float(wl.weights[0][:256].cuda(), wl.biases[0][:256], 256)
+    x = wl.X.cuda().reshape(4, 16, 6144)
+    y = lin(x)
+    assert y.shape == (4, 16, 256)
+    assert torch.equal(y.reshape(64, 256), lin(wl.X.cuda()))
+    with pytest.raises(TypeError):
+        cr.ConvRotLinear.from_float(torch.zeros((4, 256), dtype=torch.int8), None, 256)
+
+
+@pytest.mark.parametrize("name", ["dit6144", "qkv32700"])
+def test_full_size_sampled_outputs(cr, name):
+    """Full-size workloads in the bench's launch configuration; the oracle
+    checks a seeded sample of (row, column) outputs from the GPU's own codes
+    (bit-exact accumulators) and from X (end-to-end bound)."""
+    wl = WL.dit6144() if name == "dit6144" else WL.qkv32700()
+    a = cr.convrot_quantize_act(wl.X.cuda(), wl.group, "h4")
+    ws = [cr.convrot_prepare_weights(W.cuda(), wl.group, "h4") for W in wl.weights]
+    Ys = cr.convrot_linear_multi(a, ws, [b.cuda() for b in wl.biases])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([rng.choice(wl.M, 256, replace=False), np.arange(wl.M - 40, wl.M)]))
+    qx = to_np(a.q)[rows].astype(np.int8)
+    sx = to_np(a.scale)[rows]
+    X64 = wl.X[torch.from_numpy(rows)].float().numpy().astype(np.float64)
+    Qx_or, sx_or, v = O.quantize_act(X64, wl.group, "h4")
+    check_codes(qx, Qx_or, v, name)
+    for i, (W, b, Y) in enumerate(zip(wl.weights, wl.biases, Ys)):
+        cols = np.unique(np.concatenate([rng.choice(W.shape[0], 256, replace=False),
+                                         np.arange(W.shape[0] - 8, W.shape[0])]))
+        qw = to_np(ws[i].q)[cols].astype(np.int8)
+        sw = to_np(ws[i].scale)[cols]
+        A = O.int_gemm(qx, qw)
+        Ys_np = to_np(Y.float())[np.ix_(rows, cols)]
+        check_y_same_codes(Ys_np, A, sx, sw, b.numpy()[cols], f"{name}[{i}]")
+        W64 = W.numpy().astype(np.float64)[cols]
+        Qw_or, sw_or, _ = O.prepare_weights(W64, wl.group, "h4")
+        ref = O.reconstruct(O.int_gemm(Qx_or, Qw_or), sx_or, sw_or, b.numpy()[cols])
+        check_y_e2e(Ys_np, ref, f"{name}[{i}] e2e")

@@ -1,0 +1,163 @@
+"""Parity of the rotate + quantize kernels (activations and weights) with the
+CPU oracle, on seeded inputs of the pages' shapes. Runs through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+from parity import check_codes, check_scales, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cr():
+    import int8_convrot_w8a8_gb300 as cr
+    return cr
+
+
+def _oracle_act(X_bf16, G, transform, signs=None):
+    """(Q, s as fp64 before rounding to fp32, v) from the oracle."""
+    X64 = X_bf16.float().numpy().astype(np.float64)
+    Q, _, v, s64 = O.quantize_rows(O.rotate_rows(X64, G, transform, None if signs is None else signs.numpy()))
+    return Q, s64, v
+
+
+def _run_act(cr, X_bf16, G, transform, signs=None, with_f16=True):
+    Xd = X_bf16.cuda()
+    sd = None if signs is None else signs.cuda()
+    a = cr.convrot_quantize_act(Xd, G, transform, sd, with_f16=with_f16)
+    torch.cuda.synchronize()
+    return a
+
+
+@pytest.mark.parametrize("M,K,G", [
+    (64, 256, 256),     # the tiny workload
+    (37, 6144, 256),    # DiT width, ragged rows
+    (50, 3072, 256),    # qkv width
+    (33, 4096, 16), (33, 4096, 64), (33, 4096, 256), (33, 4096, 1024),  # group sweep
+    (45, 2688, 64),     # AdaLN width
+    (7, 64, 4), (3, 4096, 4096), (1, 1024, 1024),
+])
+def test_quantize_act_h4_matches_oracle(cr, M, K, G):
+    wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.001, outlier_scale=50.0, group=G, seed=M * 7 + G)
+    a = _run_act(cr, wl.X, G, "h4")
+    Q, s, v = _oracle_act(wl.X, G, "h4")
+    check_codes(to_np(a.q), Q, v, f"M{M} K{K} G{G}")
+    check_scales(to_np(a.scale), s, f"M{M} K{K} G{G}")
+    # the fp16 operand copy holds exactly the int8 codes
+    assert torch.equal(a.q_f16.float(), a.q.float())
+
+
+def test_tiny_workload_spikes_spread(cr):
+    wl = WL.tiny()
+    a = _run_act(cr, wl.X, 256, "h4")
+    Q, s, v = _oracle_act(wl.X, 256, "h4")
+    check_codes(to_np(a.q), Q, v, "tiny")
+    # +-40 spikes in a N(0,1) row: after the rotation the spike spreads over
+    # the group, so the codes use a wide range instead of saturating one slot
+    assert np.mean(np.abs(to_np(a.q)) > 10) > 0.5
+
+
+def test_fast_and_generic_paths_are_bit_identical(cr):
+    """An X view that is 16- but not 32-byte aligned takes the generic kernel;
+    both kernels run the same fp32 operations, so the results are equal."""
+    wl = WL.make_case(40, 6144 + 8, [], seed=11)
+    Xfull = wl.X.cuda()
+    X_al = Xfull[:, :6144].contiguous()
+    X_un = Xfull[:, 8:]            # 16-byte offset, row stride 6152 -> generic path
+    X_un_copy = X_un.contiguous()  # same values, aligned -> fast path
+    a_gen = cr.convrot_quantize_act(X_un, 256, "h4")
+    a_fast = cr.convrot_quantize_act(X_un_copy, 256, "h4")
+    torch.cuda.synchronize()
+    assert torch.equal(a_gen.q, a_fast.q)
+    assert torch.equal(a_gen.scale, a_fast.scale)
+    assert torch.equal(a_gen.q_f16, a_fast.q_f16)
+    del X_al
+
+
+def test_without_f16_copy(cr):
+    wl = WL.make_case(20, 3072, [], seed=12)
+    a = _run_act(cr, wl.X, 256, "h4", with_f16=False)
+    b = _run_act(cr, wl.X, 256, "h4", with_f16=True)
+    assert a.q_f16 is None and torch.equal(a.q, b.q) and torch.equal(a.scale, b.scale)
+
+
+def test_zero_rows_and_basis_rows(cr):
+    K, G = 1024, 256
+    X = torch.zeros((6, K), dtype=torch.bfloat16)
+    X[1, 5] = 1.0                # basis vector: whole group +-127
+    X[3, 300] = -2.0
+    X[5, :] = 3.0                # constant row: R fixes the all-ones vector
+    a = _run_act(cr, X, G, "h4")
+    Q, s, v = _oracle_act(X, G, "h4")
+    assert np.array_equal(to_np(a.q), Q)
+    check_scales(to_np(a.scale), s)
+    assert float(a.scale[0]) == 0.0 and float(a.scale[2]) == 0.0
+    assert np.all(np.abs(to_np(a.q)[1, :256]) == 127) and np.all(to_np(a.q)[1, 256:] == 0)
+    assert np.all(to_np(a.q)[5] == 127)
+
+
+def test_single_row_and_empty(cr):
+    wl = WL.make_case(1, 6144, [], seed=13)
+    a = _run_act(cr, wl.X, 256, "h4")
+    Q, s, v = _oracle_act(wl.X, 256, "h4")
+    check_codes(to_np(a.q), Q, v, "M=1")
+    e = cr.convrot_quantize_act(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"), 256, "h4")
+    assert e.q.shape == (0, 256)
+
+
+@pytest.mark.parametrize("M,K,B", [(16, 1152, 128), (9, 256, 16), (5, 4096, 1024)])
+def test_quantize_act_rht_matches_oracle(cr, M, K, B):
+    wl = WL.make_case(M, K, [], dist="normal", outlier_frac=0.005, outlier_scale=30.0, group=B,
+                      transform="rht", seed=B + M)
+    a = _run_act(cr, wl.X, B, "rht", wl.signs)
+    Q, s, v = _oracle_act(wl.X, B, "rht", wl.signs)
+    check_codes(to_np(a.q), Q, v, f"rht B{B}")
+    check_scales(to_np(a.scale), s, f"rht B{B}")
+
+
+def test_quantize_act_none_matches_oracle(cr):
+    wl = WL.make_case(21, 1152, [], seed=14)
+    a = _run_act(cr, wl.X, 0, "none")
+    Q, s, v = _oracle_act(wl.X, 0, "none")
+    check_codes(to_np(a.q), Q, v, "none")
+
+
+@pytest.mark.parametrize("N,K,G,transform,dtype", [
+    (256, 256, 256, "h4", torch.float32),
+    (300, 6144, 256, "h4", torch.float32),
+    (129, 4096, 1024, "h4", torch.float32),
+    (77, 2688, 64, "h4", torch.float32),
+    (200, 1152, 128, "rht", torch.float32),
+    (64, 3072, 256, "h4", torch.bfloat16),
+])
+def test_prepare_weights_matches_oracle(cr, N, K, G, transform, dtype):
+    g = torch.Generator().manual_seed(N + K)
+    W = torch.randn((N, K), generator=g) * 0.02
+    W = W.to(dtype)
+    signs = WL.draw_signs(g, G) if transform == "rht" else None
+    pw = cr.convrot_prepare_weights(W.cuda(), G, transform, None if signs is None else signs.cuda())
+    torch.cuda.synchronize()
+    W64 = W.float().numpy().astype(np.float64)
+    sg = None if signs is None else signs.numpy()
+    Q, s, v = O.prepare_weights(W64, G, transform, sg)
+    check_codes(to_np(pw.q), Q, v, f"W {N}x{K}")
+    check_scales(to_np(pw.scale), O.quantize_rows(O.rotate_rows(W64, G, transform, sg))[3])
+    assert torch.equal(pw.q_f16.float(), pw.q.float())
+
+
+@pytest.mark.parametrize("name", ["dit6144", "qkv32700", "gsweep1024", "k2688"])
+def test_full_size_sampled_rows(cr, name):
+    """Full-size workloads in the launch configuration the bench times;
+    the oracle checks a seeded sample of rows (rows are independent)."""
+    wl = {"dit6144": lambda: WL.dit6144(), "qkv32700": lambda: WL.qkv32700(),
+          "gsweep1024": lambda: WL.gsweep(1024), "k2688": lambda: WL.k2688()}[name]()
+    a = _run_act(cr, wl.X, wl.group, "h4")
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(wl.M, 512, replace=False), np.arange(wl.M - 70, wl.M)]))
+    Xs = wl.X[torch.from_numpy(rows)]
+    Q, s, v = _oracle_act(Xs, wl.group, "h4")
+    check_codes(to_np(a.q)[rows], Q, v, name)
+    check_scales(to_np(a.scale)[rows], s, name)
