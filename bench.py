@@ -1,0 +1,368 @@
+"""Benchmark of the ConvRot W8A8 linear on GB300.
+
+One step = one pass of the runtime path over one batch: the fused
+rotate + row-absmax + quantize kernel on X, then the int8 GEMM with the
+fused dequant/bias/bf16 epilogue for every linear that shares the packed
+activation. Weights are prepared once before timing (the offline path).
+
+Timing: W warm-up steps, then K timed steps; each step is bracketed by CUDA
+events on the launching stream, and L2 is flushed between steps (a 256 MiB
+write, outside the events). Clocks are sampled with nvidia-smi during the
+timed region. The e2e figure repeats the step through the public API with
+host buffers: pinned X copied in, Y copied back, inside the timed region.
+
+`--impl reference` times the CPU oracle (fp64 numpy) on a bounded row
+sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as WL  # noqa: E402
+
+METRIC = "ConvRot W8A8 linear int8 TOPS and rotate+quant GB/s, % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+WORKLOADS = {
+    "dit6144": lambda: WL.dit6144(),
+    "qkv32700": lambda: WL.qkv32700(),
+    "qkv32700_cat": lambda: _concat(WL.qkv32700()),
+    "ffn_pair": lambda: WL.ffn_pair(),
+    "gsweep16": lambda: WL.gsweep(16),
+    "gsweep64": lambda: WL.gsweep(64),
+    "gsweep256": lambda: WL.gsweep(256),
+    "gsweep1024": lambda: WL.gsweep(1024),
+    "k2688": lambda: WL.k2688(),
+    "tiny": lambda: WL.tiny(),
+}
+
+
+def _concat(wl):
+    wl.weights = [torch.cat(wl.weights)]
+    wl.biases = [torch.cat(wl.biases)]
+    wl.name = wl.name.replace("(3x3072)", "9216cat")
+    return wl
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ oracle ---
+
+def oracle_sample(wl, rows: int, seed: int = 0):
+    """Times the CPU oracle on a seeded sample of `rows` rows (full K, all N)."""
+    import oracle as O
+    sg = None if wl.signs is None else wl.signs.numpy()
+    Ws = [O.prepare_weights(W.numpy().astype(np.float64), wl.group, wl.transform, sg) for W in wl.weights]
+    rng = np.random.default_rng(seed)
+    idx = np.sort(rng.choice(wl.M, size=min(rows, wl.M), replace=False))
+    X64 = wl.X[torch.from_numpy(idx)].float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    Qx, sx, _ = O.quantize_act(X64, wl.group, wl.transform, sg)
+    t1 = time.perf_counter()
+    for (Qw, sw, _), b in zip(Ws, wl.biases):
+        O.round_to_bf16(O.reconstruct(O.int_gemm(Qx, Qw), sx, sw, b.numpy()))
+    t2 = time.perf_counter()
+    ops = 2.0 * len(idx) * sum(wl.Ns) * wl.K
+    return {"rows": len(idx), "seconds": t2 - t0, "quant_seconds": t1 - t0, "ops": ops}
+
+
+def reference_main(args, world, rank):
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]()
+    rows = args.ref_rows
+    res = []
+    for _ in range(args.warmup):
+        oracle_sample(wl, max(8, rows // 8))
+    for s in range(args.steps):
+        res.append(oracle_sample(wl, rows, seed=s))
+    secs = sum(r["seconds"] for r in res)
+    ops = sum(r["ops"] for r in res)
+    value = ops / secs / 1e12
+    cores = blas_threads()
+    sample = f"{rows} seeded rows of {wl.M} per step (full K={wl.K}, all N={sum(wl.Ns)}), fp64 numpy"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- GPU ---
+
+def gpu_main(args, world, rank, local):
+    import int8_convrot_w8a8_gb300 as cr
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]()
+    stream = torch.cuda.current_stream()
+    sg = None if wl.signs is None else wl.signs.to(dev)
+    use_f16 = wl.M > 64
+    ws = [cr.convrot_prepare_weights(W.to(dev), wl.group, wl.transform, sg, with_f16=use_f16) for W in wl.weights]
+    bs = [b.to(dev) for b in wl.biases]
+    X = wl.X.to(dev)
+    M, K, Ns = wl.M, wl.K, wl.Ns
+    act = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16)
+    outs = [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16, out=act)
+        e_mid.record(stream)
+        if len(ws) == 1:
+            cr.convrot_linear(act, ws[0], bs[0], out=outs[0])
+        else:
+            cr.convrot_linear_multi(act, ws, bs, outs=outs)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        e_mid = torch.cuda.Event(enable_timing=True)
+        step()
+    torch.cuda.synchronize()
+    assert cr.convrot_get_device_status() == 0
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e_mid, e1 = ev[i]
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+    barrier(world)
+    status = cr.convrot_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    step_ms = [e0.elapsed_time(e1) for e0, _, e1 in ev]
+    quant_ms = [e0.elapsed_time(em) for e0, em, _ in ev]
+    gemm_ms = [em.elapsed_time(e1) for _, em, e1 in ev]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+
+    ops_step = 2.0 * M * sum(Ns) * K
+    value = world * ops_step * args.steps / total_s / 1e12
+    pk = peaks()
+    gemm_s = statistics.mean(gemm_ms) / 1e3
+    quant_s = statistics.mean(quant_ms) / 1e3
+    gemm_tflops = ops_step / gemm_s / 1e12
+    # algorithmic bytes of rotate+quantize: bf16 in, int8 out, fp32 scales
+    q_bytes = 2 * M * K + M * K + 4 * M
+    q_bytes_f16 = q_bytes + 2 * M * K if use_f16 else q_bytes
+    quant_gbs = q_bytes / quant_s / 1e9
+    if use_f16:
+        dominant = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": gemm_tflops,
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
+                    "traffic": None,
+                    "peak_note": f"{pk['source']} bf16 dense burst; the fp16 tensor rate is the same (nominal ratio 1)"}
+    else:
+        w_bytes = sum(n * K + 4 * n for n in Ns) + M * K + 4 * M + 2 * M * sum(Ns)
+        gbs = w_bytes / gemm_s / 1e9
+        dominant = {"kernel": "gemm_mma_kernel", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                    "peak_note": f"{pk['source']} HBM copy bandwidth"}
+
+    # ---- end to end through the public API with host buffers
+    Xh = wl.X.pin_memory()
+    Yh = [torch.empty((M, n), dtype=torch.bfloat16).pin_memory() for n in Ns]
+    Xd = torch.empty_like(X)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        Xd.copy_(Xh, non_blocking=True)
+        cr.convrot_quantize_act(Xd, wl.group, wl.transform, sg, with_f16=use_f16, out=act)
+        if len(ws) == 1:
+            cr.convrot_linear(act, ws[0], bs[0], out=outs[0])
+        else:
+            cr.convrot_linear_multi(act, ws, bs, outs=outs)
+        for y, yh in zip(outs, Yh):
+            yh.copy_(y, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a0.elapsed_time(a1))
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world)
+    e2e_value = world * ops_step * args.steps / e2e_s / 1e12
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": wl.name, "M": M, "K": K, "N": Ns, "group": wl.group, "transform": wl.transform,
+                   "seed": wl.seed, "l2": "flushed between steps (256 MiB write outside the events)",
+                   "inputs": wl.description, "gemm_path": "tcgen05 fp16-exact" if use_f16 else "mma.sync s8"},
+        "roofline": dominant,
+        "rotate_quant": {"kernel": "rq_fast_kernel" if wl.transform == "h4" else "rq_generic_kernel",
+                         "us": quant_s * 1e6, "gbs": quant_gbs, "peak_gbs": pk["hbm_gbs"],
+                         "frac": quant_gbs / pk["hbm_gbs"], "algorithmic_bytes": q_bytes,
+                         "bytes_with_f16_copy": q_bytes_f16, "gbs_with_f16_copy": q_bytes_f16 / quant_s / 1e9},
+        "gemm_us": gemm_s * 1e6,
+        "gpu_launches": 2 * args.steps,
+        "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": 2 * M * K,
+                "d2h_bytes_per_step": 2 * M * sum(Ns), "ms_per_step": statistics.mean(e2e_ms)},
+        "clocks": clocks.summary(),
+        "wall_s_timed": wall1 - wall0,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        ref = oracle_sample(wl, args.ref_rows)
+        cores = blas_threads()
+        cv = ref["ops"] / ref["seconds"] / 1e12
+        line["cpu_baseline"] = {"value": cv, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                                "sample": f"{ref['rows']} seeded rows of {M} (full K, all N), fp64 numpy, "
+                                          f"{ref['seconds']:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="dit6144", choices=sorted(WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            reference_main(args, world, rank)
+        else:
+            gpu_main(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

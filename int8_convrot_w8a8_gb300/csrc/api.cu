@@ -81,7 +81,7 @@ convrot_status check_shape(long long K, int group, int transform) {
 
 convrot_status check_pair(const convrot_packed_act* a, const convrot_packed_weight* w) {
   if (!a || !w) return fail(CONVROT_ERR_INVALID_ARG, "null descriptor");
-  if (!a->q || !a->scale) return fail(CONVROT_ERR_INVALID_ARG, "activation q/scale is null");
+  if (a->M > 0 && (!a->q || !a->scale)) return fail(CONVROT_ERR_INVALID_ARG, "activation q/scale is null");
   if (!w->q || !w->scale) return fail(CONVROT_ERR_INVALID_ARG, "weight q/scale is null");
   if (a->M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(a->M));
   if (w->N <= 0) return fail(CONVROT_ERR_INVALID_ARG, "N=%lld must be >= 1", static_cast<long long>(w->N));
@@ -196,7 +196,7 @@ convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_
   if (s != CONVROT_OK) return s;
   if (a->M > 0 && !Y) return fail(CONVROT_ERR_INVALID_ARG, "Y is null");
   if (ldy < w->N) return fail(CONVROT_ERR_INVALID_ARG, "ldy=%lld < N=%lld", static_cast<long long>(ldy), static_cast<long long>(w->N));
-  if (!aligned(Y, 16) || ldy % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y must be 16-byte aligned and ldy a multiple of 8");
+  if ((a->M > 0 && !aligned(Y, 16)) || ldy % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y must be 16-byte aligned and ldy a multiple of 8");
   if (bias && !aligned(bias, 4)) return fail(CONVROT_ERR_ALIGNMENT, "bias must be 4-byte aligned");
   GemmOutputs outs{};
   outs.count = 1;

@@ -1,4 +1,41 @@
-// Tensor-core (tcgen05) GEMM path -- placeholder until the kernel lands.
+// Int8-exact GEMM on the 5th-generation tensor cores (tcgen05), with the
+// dequant / bias / bf16 epilogue fused.
+//
+//   A[r, o] = sum_i Q_x[r, i] * Q_w[o, i]          (exact, int32)
+//   Y[r, o] = bf16( fma(float(A[r,o]), s_x[r] * s_w[o], b[o]) )
+//
+// ("INT8 Convrot Safetensors", "Runtime activation quantization".)
+//
+// sm_103a has no integer tcgen05 MMA, so the int8 codes enter the tensor
+// cores as fp16 values (every integer in [-127, 127] is exact in fp16) with
+// an fp32 accumulator in tensor memory. Products are exact (|q*q| <= 16129)
+// and so is every partial sum while it stays below 2^24 in magnitude:
+// 127 * 127 * 1024 = 16 516 096 < 2^24 = 16 777 216. The K loop therefore
+// runs in chunks of at most 1024; each chunk accumulates into a fresh TMEM
+// buffer, and the epilogue warps convert the chunk (an exact integer in
+// fp32) to int32 and add it into int32 registers. Two TMEM buffers
+// alternate, so the tensor cores fill chunk c+1 while chunk c drains.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: 128 x 64 A tiles and BN x 64 B tiles, 128-byte
+//               swizzle, into a STAGES-deep shared-memory ring.
+//   warp 1      TMEM allocation and the MMA issuer: tcgen05.mma kind::f16,
+//               M = 128, N = BN, K = 16, cta_group::1.
+//   warps 2..9  epilogue: TMEM -> registers (tcgen05.ld 32x32b), int32
+//               accumulation, then scaling, bias, bf16 and the store.
+// Tiles are handed out statically (tile = blockIdx.x + i * gridDim.x) in a
+// grouped order for L2 reuse; the schedule is data-parallel (no split-K), so
+// every output is computed by exactly one CTA in a fixed order and results
+// do not depend on how the rows are partitioned.
+//
+// Every mbarrier wait is bounded. A wait that gives up records
+// CONVROT_ERR_TIMEOUT in the device error word and raises a CTA-wide abort
+// flag; the roles stop issuing work, wait (bounded) for their copies and MMAs
+// in flight, free the tensor memory and return.
+#include <cuda.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemm_common.cuh"
 
@@ -6,10 +43,448 @@ namespace convrot {
 
 CONVROT_DEFINE_STATUS_WORD(status_word_gemm_tc)
 
-bool gemm_tc_supported(long long, int) { return false; }
+namespace {
 
-cudaError_t gemm_tc_launch(const uint16_t*, const float*, long long, int, const GemmOutputs&, bool, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128;
+constexpr int BK = 64;           // fp16 elements per stage row = 128 bytes = one swizzle atom
+constexpr int KCHUNK = 1024;     // exact fp32 accumulation span (see above)
+constexpr int KITER_PER_CHUNK = KCHUNK / BK;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 32 * (2 + NUM_EPI_WARPS);
+constexpr int TMEM_COLS = 512;
+constexpr int GROUP_M = 16;
+
+template <int BN>
+struct Cfg {
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int HALF = BN / 2;  // columns per epilogue thread
+  // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16
+  // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
+  // M >> 4 at bit 24.
+  static constexpr uint32_t IDESC = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                    (static_cast<uint32_t>(BM >> 4) << 24);
+};
+
+struct TcParams {
+  CUtensorMap tmap_a;
+  CUtensorMap tmap_b[kMaxLinears];
+  GemmOutputs outs;
+  const float* sx;
+  long long M;
+  int K;
+  int m_tiles;
+  int n_tiles;
+  int num_tiles;
+  long long spin_limit;
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// tile whose rows are 128 bytes (64 fp16) and whose 8-row core groups are
+// 1024 bytes apart: start address >> 4 (bits 0-13), leading byte offset
+// (bits 16-29, unused for this layout), stride byte offset 1024 >> 4
+// (bits 32-45), descriptor version 1 (bits 46-47), swizzle mode 128B = 2
+// (bits 61-63). Moving along K inside the 128-byte atom adds the byte
+// offset to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Wait for a phase, giving up after `limit` polls or when another role has
+// aborted; returns false on give-up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
+                                              volatile int* abort_flag) {
+  for (long long i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort_flag) return false;
+    if (i > 128) __nanosleep(32);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
+  *abort_flag = 1;
+  record_status(CONVROT_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& m_blk, int& n_glob, int& li,
+                                            int& n_local) {
+  const int per_group = GROUP_M * p.n_tiles;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(p.m_tiles - first_m, GROUP_M);
+  const int r = t - g * per_group;
+  m_blk = first_m + r % gm;
+  n_glob = r / gm;
+  li = 0;
+  while (li + 1 < p.outs.count && n_glob >= p.outs.o[li + 1].tile_begin) ++li;
+  n_local = n_glob - p.outs.o[li].tile_begin;
+}
+
+template <int BN, bool RAW>
+__global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* final_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = p.K / BK;
+  const int nch = (nk + KITER_PER_CHUNK - 1) / KITER_PER_CHUNK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], NUM_EPI_WARPS);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int armed_round[C::STAGES];
+      for (int s = 0; s < C::STAGES; ++s) armed_round[s] = -1;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int m_blk, n_glob, li, n_local;
+        decode_tile(p, t, m_blk, n_glob, li, n_local);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::STAGES, round = it / C::STAGES;
+          if (!wait_or_abort(&empty[s], (round & 1) ^ 1, p.spin_limit, abort_flag)) {
+            raise_abort(abort_flag);
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+          mbar_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(sa, &p.tmap_a, kb * BK, m_blk * BM, &full[s]);
+          tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN, &full[s]);
+          armed_round[s] = round;
+        }
+      }
+      // every armed copy must have landed before the CTA may exit
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed_round[s] >= 0 && !mbar_wait_bounded(&full[s], armed_round[s] & 1, p.spin_limit))
+          raise_abort(abort_flag);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0, chunk = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nk && ok;) {
+          const int b = chunk & 1, u = chunk >> 1;
+          if (!wait_or_abort(&acc_empty[b], (u & 1) ^ 1, p.spin_limit, abort_flag)) {
+            raise_abort(abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+          const int kend = min(kb + KITER_PER_CHUNK, nk);
+          const int kstart = kb;
+          for (; kb < kend; ++kb, ++it) {
+            const int s = it % C::STAGES, round = it / C::STAGES;
+            if (!wait_or_abort(&full[s], round & 1, p.spin_limit, abort_flag)) {
+              raise_abort(abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+            const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              tc_mma_f16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
+                         (kb != kstart || k > 0) ? 1u : 0u);
+            }
+            tc_commit(&empty[s]);
+          }
+          if (!ok) break;
+          tc_commit(&acc_full[b]);
+          ++chunk;
+        }
+      }
+      // all issued MMAs complete before the tensor memory is released
+      tc_commit(final_bar);
+      if (!mbar_wait_bounded(final_bar, 0, p.spin_limit)) raise_abort(abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;    // which half of the BN columns
+    const int row_in_tile = q * 32 + lane;
+    const int col0 = half * C::HALF;
+    int chunk = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      int m_blk, n_glob, li, n_local;
+      decode_tile(p, t, m_blk, n_glob, li, n_local);
+      int acc[C::HALF];
+#pragma unroll
+      for (int j = 0; j < C::HALF; ++j) acc[j] = 0;
+      for (int c = 0; c < nch; ++c, ++chunk) {
+        const int b = chunk & 1, u = chunk >> 1;
+        // every lane waits; the warp proceeds only if all lanes saw the phase
+        // (the TMEM loads below are warp-collective)
+        const bool got = wait_or_abort(&acc_full[b], u & 1, p.spin_limit, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) raise_abort(abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN + col0);
+#pragma unroll
+        for (int j = 0; j < C::HALF / 32; ++j) {
+          uint32_t r[32];
+          tc_ld_32x32b_x32(taddr + j * 32, r);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[j * 32 + e] += __float2int_rz(__uint_as_float(r[e]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+      }
+      if (!ok) break;
+
+      const GemmOut& o = p.outs.o[li];
+      const long long m = static_cast<long long>(m_blk) * BM + row_in_tile;
+      const int nb = n_local * BN + col0;
+      if (m < p.M) {
+        if constexpr (RAW) {
+          int* yrow = static_cast<int*>(o.y) + m * o.ldy;
+#pragma unroll
+          for (int j = 0; j < C::HALF; j += 4) {
+            const int n = nb + j;
+            if (n + 4 <= o.n) {
+              *reinterpret_cast<int4*>(yrow + n) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (n + e < o.n) yrow[n + e] = acc[j + e];
+            }
+          }
+        } else {
+          const float srow = p.sx[m];
+          __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(o.y) + m * o.ldy;
+#pragma unroll
+          for (int j = 0; j < C::HALF; j += 8) {
+            const int n = nb + j;
+            if (n + 8 <= o.n) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                const float b0 = o.bias ? __ldg(o.bias + n + e) : 0.0f;
+                const float b1 = o.bias ? __ldg(o.bias + n + e + 1) : 0.0f;
+                const float y0 = fmaf(static_cast<float>(acc[j + e]), srow * __ldg(o.sw + n + e), b0);
+                const float y1 = fmaf(static_cast<float>(acc[j + e + 1]), srow * __ldg(o.sw + n + e + 1), b1);
+                const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+                w[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              stg_128(yrow + n, make_uint4(w[0], w[1], w[2], w[3]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                if (n + e < o.n) {
+                  const float be = o.bias ? __ldg(o.bias + n + e) : 0.0f;
+                  yrow[n + e] = __float2bfloat16_rn(fmaf(static_cast<float>(acc[j + e]), srow * __ldg(o.sw + n + e), be));
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---- host -------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<EncodeTiledFn>(fn);
+}
+
+bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long rows, int K, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// Column tile: the BN whose last wave wastes the least, by the estimate
+// waves(BN) * BN (a tile's time grows with BN); ties go to the wider tile.
+int choose_bn(long long M, const GemmOutputs& outs, int sms) {
+  const long long mt = (M + BM - 1) / BM;
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : {256, 192, 128}) {
+    long long nt = 0;
+    for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + bn - 1) / bn;
+    const long long tiles = mt * nt;
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long cost = waves * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <int BN, bool RAW>
+cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K, GemmOutputs outs,
+                      cudaStream_t st, int sms) {
+  using C = Cfg<BN>;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_map(enc, &p.tmap_a, Qx16, M, K, BM)) return cudaErrorInvalidValue;
+  int nt = 0;
+  for (int i = 0; i < outs.count; ++i) {
+    outs.o[i].tile_begin = nt;
+    nt += (outs.o[i].n + BN - 1) / BN;
+    if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN)) return cudaErrorInvalidValue;
+  }
+  p.outs = outs;
+  p.sx = sx;
+  p.M = M;
+  p.K = K;
+  p.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.n_tiles = nt;
+  const long long tiles = static_cast<long long>(p.m_tiles) * nt;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.num_tiles = static_cast<int>(tiles);
+  p.spin_limit = kDefaultSpinLimit;
+  auto kern = gemm_tc_kernel<BN, RAW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(std::min<long long>(tiles, sms));
+  kern<<<grid, THREADS, C::SMEM, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_supported(long long M, int K) { return M > 64 && K % BK == 0 && K >= BK; }
+
+cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
+                           bool raw, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int sms = sm_count();
+  const int bn = choose_bn(M, outs, sms);
+  switch (bn) {
+    case 256: return raw ? launch_bn<256, true>(enc, Qx16, sx, M, K, outs, st, sms)
+                         : launch_bn<256, false>(enc, Qx16, sx, M, K, outs, st, sms);
+    case 192: return raw ? launch_bn<192, true>(enc, Qx16, sx, M, K, outs, st, sms)
+                         : launch_bn<192, false>(enc, Qx16, sx, M, K, outs, st, sms);
+    default: return raw ? launch_bn<128, true>(enc, Qx16, sx, M, K, outs, st, sms)
+                        : launch_bn<128, false>(enc, Qx16, sx, M, K, outs, st, sms);
+  }
 }
 
 }  // namespace convrot
