@@ -20,8 +20,9 @@
  *
  * Conventions for every entry point:
  *  - Pointers marked "device" are caller-allocated device memory; the library
- *    allocates nothing and keeps no state between calls except the device
- *    error word read by convrot_get_device_status().
+ *    allocates no device memory and keeps no data between calls. It holds
+ *    only the device error word read by convrot_get_device_status() and, on
+ *    the host, per-device kernel attributes it has already set.
  *  - Work is enqueued on the given stream and runs asynchronously. Argument
  *    errors are detected on the host and returned BEFORE anything is
  *    launched; CONVROT_ERR_CUDA reports a failed launch.

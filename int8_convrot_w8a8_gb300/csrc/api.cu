@@ -3,6 +3,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "gemm_common.cuh"
@@ -22,6 +25,54 @@ bool gemm_tc_supported(long long M, int K);
 cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st);
 
 CONVROT_DEFINE_STATUS_WORD(status_word_api)
+
+namespace {
+std::mutex g_cache_mu;
+std::map<std::pair<const void*, int>, int> g_smem_set;                 // (kernel, device) -> bytes
+std::map<std::tuple<const void*, int, int, int>, int> g_occupancy;     // (kernel, device, threads, smem)
+std::map<int, int> g_sms;                                              // device -> SM count
+}  // namespace
+
+cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto it = g_smem_set.find({kernel, dev});
+  if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem_set[{kernel, dev}] = bytes;
+  return e;
+}
+
+cudaError_t blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto key = std::make_tuple(kernel, dev, threads, smem_bytes);
+  auto it = g_occupancy.find(key);
+  if (it != g_occupancy.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kernel, threads, smem_bytes);
+  if (e == cudaSuccess) g_occupancy[key] = *out;
+  return e;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n < 1) n = 1;
+  g_sms[dev] = n;
+  return n;
+}
 
 }  // namespace convrot
 

@@ -31,6 +31,13 @@ namespace convrot {
   }
 
 int status_word_rotquant();
+
+// Host-side launch helpers. They remember, per device, the kernel attributes
+// already set and the occupancy / SM-count queries already answered, so a
+// call costs no repeated driver round trips. No device memory is involved.
+cudaError_t set_smem_limit(const void* kernel, int bytes);
+cudaError_t blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* out);
+int device_sm_count();
 int status_word_gemm_mma();
 int status_word_gemm_tc();
 
@@ -102,6 +109,13 @@ __device__ __forceinline__ U32x8 ldg_nc_256(const void* p) {
 }
 __device__ __forceinline__ void stg_128(void* p, uint4 v) {
   asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 32-byte store (sm_100+).
+__device__ __forceinline__ void stg_256(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                : "memory");
 }
 

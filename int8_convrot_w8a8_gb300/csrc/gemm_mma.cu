@@ -202,7 +202,7 @@ cudaError_t launch_cfg(const int8_t* Qx, const float* sx, long long M, int K, Ge
     tiles_n += (outs.o[i].n + BN - 1) / BN;
   }
   auto kern = gemm_mma_kernel<BM, BN, WM, WN, STAGES, RAW>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), SMEM);
   if (e != cudaSuccess) return e;
   const long long tiles_m = (M + BM - 1) / BM;
   if (tiles_m > 0x7fffffffLL || tiles_n > 65535) return cudaErrorInvalidConfiguration;

@@ -389,7 +389,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
+EncodeTiledFn lookup_encode_fn() {
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -408,11 +408,10 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+// The driver's tensor-map encoder, looked up once per process.
+EncodeTiledFn encode_fn() {
+  static const EncodeTiledFn fn = lookup_encode_fn();
+  return fn;
 }
 
 // Column tile: the BN whose last wave wastes the least, by the estimate
@@ -459,7 +458,7 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   p.num_tiles = static_cast<int>(tiles);
   p.spin_limit = kDefaultSpinLimit;
   auto kern = gemm_tc_kernel<BN, RAW>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::min<long long>(tiles, sms));
   kern<<<grid, THREADS, C::SMEM, st>>>(p);
@@ -475,7 +474,7 @@ cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, i
   if (M <= 0) return cudaSuccess;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  const int sms = sm_count();
+  const int sms = device_sm_count();
   const int bn = choose_bn(M, outs, sms);
   switch (bn) {
     case 256: return raw ? launch_bn<256, true>(enc, Qx16, sx, M, K, outs, st, sms)

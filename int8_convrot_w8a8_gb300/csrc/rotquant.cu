@@ -125,24 +125,25 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
 }
 
 // =============================================================== fast ======
-// Register-resident kernel for bf16 input and the regular Hadamard.
+// Fast kernel for bf16 input and the regular Hadamard.
 //
-// A CTA owns a tile of R consecutive rows and keeps all R*K values in
-// registers, EPT per thread, across the row-absmax reduction.
+// A CTA owns a tile of R consecutive rows (persistent grid-stride loop).
 //  Phase R: each thread takes SEGS segments of G1 consecutive elements,
 //    loaded with 32-byte loads (a warp reads 1 KB contiguous per load), and
 //    runs the radix-4 stages of the low digits in registers (G1 = 16: two
-//    digits, G1 = 64: three).
-//  Phase C (G > G1 only): the segments go through shared memory (fp32,
-//    XOR-swizzled against bank conflicts) and come back as blocks of
-//    G2 = G/G1 rows x 4 consecutive columns of the group viewed as a
-//    G2 x G1 matrix; the high digits run in registers on those blocks.
-//  Row absmax: shared-memory atomicMax per row.
-//  Quantize: codes of 4 consecutive columns form one 32-bit word; they are
-//    staged in shared memory (aliasing the fp32 buffer) and leave as 16-byte
-//    coalesced stores. With G <= G1 each thread stores its segments directly.
-// The loads of the next tile are issued before the output copy of the
-// current one.
+//    digits, G1 = 64: three). The loads of the next tile are issued as soon
+//    as these registers are free.
+//  Phase C (G > G1): the rotated segments are parked in shared memory as
+//    fp32 (XOR-swizzled against bank conflicts), where the row stays across
+//    the reduction. Each thread then runs the high digits on units of
+//    G2 = G/G1 rows x 2 adjacent columns of the group seen as a G2 x G1
+//    matrix, two columns per packed fp32x2 operation, and writes the unit
+//    back in place.
+//  Row absmax: a warp reduction over the lanes of each row (lanes of one
+//    warp may straddle two rows), then one shared-memory atomicMax.
+//  Quantize: in the load layout again, so the int8 codes (16-byte stores)
+//    and the fp16 copies (32-byte stores) leave coalesced, straight to HBM.
+// With G <= 16 a segment holds whole groups and nothing leaves registers.
 
 template <int G, int G1, int SEGS>
 struct FastCfg {
@@ -151,7 +152,7 @@ struct FastCfg {
   static constexpr int ND2 = ilog4_c(G2);
   static constexpr int EPT = SEGS * G1;
   static constexpr bool PHASE_C = G2 > 1;
-  static constexpr int NB = PHASE_C ? EPT / (4 * G2) : 0;
+  static constexpr int NU = PHASE_C ? EPT / (2 * G2) : 0;  // phase-C units per thread
   static constexpr int LOADS = G1 / 16;
 };
 
@@ -166,15 +167,38 @@ __device__ __forceinline__ int swz_chunk(int c) {
     return c ^ ((c >> 4) & 7);
   }
 }
-// Staging buffers: word (4 codes) / 8-byte unit (4 fp16) index -> physical
-// index; only bits >= 2 change, so aligned runs of 4 stay contiguous.
-template <int G, int G1>
-__device__ __forceinline__ int swz_word(int w) {
-  constexpr int GS = ilog2_c(G / 4 > 1 ? G / 4 : 2);
-  if constexpr (G1 == 16) {
-    return w ^ (((w >> GS) & 7) << 2);
-  } else {
-    return w ^ (((w >> GS) & 1) << 4);
+// Quantize N consecutive values of one row (N a multiple of 16) and store the
+// codes (16-byte stores) and, if requested, their fp16 copies (32-byte
+// stores) at dense element offset e, if e lies inside the matrix.
+template <int N>
+__device__ __forceinline__ void quantize_store(const float (&p)[N], float inv, long long e, long long total_elems,
+                                               int8_t* __restrict__ Q, __half* __restrict__ Q16) {
+  const float2 inv2 = make_float2(inv, inv);
+  const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+#pragma unroll
+  for (int k16 = 0; k16 < N / 16; ++k16) {
+    uint32_t words[4];
+    uint32_t hw[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int o = 16 * k16 + 4 * k;
+      const float2 t01 = f2_fma(make_float2(p[o], p[o + 1]), inv2, mg2);
+      const float2 t23 = f2_fma(make_float2(p[o + 2], p[o + 3]), inv2, mg2);
+      const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
+      const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
+      words[k] = __byte_perm(b01, b23, 0x5410);
+      if (Q16) {
+        const float2 c01 = f2_sub(t01, mg2), c23 = f2_sub(t23, mg2);
+        const __half2 h01 = __floats2half2_rn(c01.x, c01.y);
+        const __half2 h23 = __floats2half2_rn(c23.x, c23.y);
+        hw[2 * k] = *reinterpret_cast<const uint32_t*>(&h01);
+        hw[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+      }
+    }
+    if (e < total_elems) {
+      stg_128(Q + e + 16 * k16, make_uint4(words[0], words[1], words[2], words[3]));
+      if (Q16) stg_256(Q16 + e + 16 * k16, hw);
+    }
   }
 }
 
@@ -182,52 +206,57 @@ template <int G, int G1, int SEGS>
 __global__ void __launch_bounds__(384) rq_fast_kernel(const __nv_bfloat16* __restrict__ X, long long M, int K,
                                                        long long ldx, int R, int NT, int8_t* __restrict__ Q,
                                                        float* __restrict__ S, __half* __restrict__ Q16,
-                                                       float s_div, int stage_bytes) {
+                                                       float s_div, int fbytes) {
   using C = FastCfg<G, G1, SEGS>;
   extern __shared__ __align__(128) unsigned char smem[];
   float* fbuf = reinterpret_cast<float*>(smem);
-  uint32_t* stage_q = reinterpret_cast<uint32_t*>(smem);
-  uint2* stage_h = reinterpret_cast<uint2*>(smem + stage_bytes);
-  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + 4 * stage_bytes);  // [2][R]
+  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + fbytes);  // [2][R]
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const bool active = tid < NT;
   const long long ntiles = (M + R - 1) / R;
   const int tile_elems = R * K;
+  const long long total_elems = M * static_cast<long long>(K);
 
-  // Static per-thread geometry: segment starts and phase-C block bases.
-  int seg_off[SEGS];
+  // Tile-invariant geometry, computed once: the row of each of this
+  // thread's segments and its offset in X. The outputs are dense [M, K], so
+  // their offsets need no row / column split.
+  int seg_row[SEGS];
+  long long seg_xoff[SEGS];
 #pragma unroll
-  for (int j = 0; j < SEGS; ++j) seg_off[j] = (tid + j * NT) * G1;
-  int blk_base[C::NB > 0 ? C::NB : 1];
-  int blk_row[C::NB > 0 ? C::NB : 1];
+  for (int j = 0; j < SEGS; ++j) {
+    const int e = (tid + j * NT) * G1;
+    seg_row[j] = e / K;
+    seg_xoff[j] = seg_row[j] * ldx + (e - seg_row[j] * K);
+  }
+  // Phase-C units: G2 rows x 2 adjacent columns of one group matrix.
+  int unit_base[C::NU > 0 ? C::NU : 1];
+  int unit_row[C::NU > 0 ? C::NU : 1];
   if constexpr (C::PHASE_C) {
     const int groups = K / G;
 #pragma unroll
-    for (int i = 0; i < C::NB; ++i) {
+    for (int i = 0; i < C::NU; ++i) {
       const int b = tid + i * NT;
-      const int c = b % (G1 / 4);
-      const int rest = b / (G1 / 4);
+      const int cp = b % (G1 / 2);
+      const int rest = b / (G1 / 2);
       const int g = rest % groups;
       const int r = rest / groups;
-      blk_row[i] = r;
-      blk_base[i] = r * K + g * G + 4 * c;
+      unit_row[i] = r;
+      unit_base[i] = r * K + g * G + 2 * cp;
     }
   }
 
   U32x8 raw[SEGS][C::LOADS];
   auto issue_loads = [&](long long tile) {
+    const long long rbase = tile * R;
+    const __nv_bfloat16* xt = X + rbase * ldx;
 #pragma unroll
     for (int j = 0; j < SEGS; ++j) {
-      const int e = seg_off[j];
-      const int r = e / K, col = e % K;
-      const long long row = tile * R + r;
-      const bool ok = active && row < M;
-      const __nv_bfloat16* p = X + row * ldx + col;
+      const bool ok = active && rbase + seg_row[j] < M;
 #pragma unroll
       for (int l = 0; l < C::LOADS; ++l) {
         if (ok) {
-          raw[j][l] = ldg_nc_256(p + 16 * l);
+          raw[j][l] = ldg_nc_256(xt + seg_xoff[j] + 16 * l);
         } else {
 #pragma unroll
           for (int k = 0; k < 8; ++k) raw[j][l].w[k] = 0u;
@@ -248,207 +277,153 @@ __global__ void __launch_bounds__(384) rq_fast_kernel(const __nv_bfloat16* __res
   for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
     unsigned int* rowmax = rowmax_buf + (it & 1) * R;
     for (int i = tid; i < R; i += blockDim.x) rowmax_buf[((it + 1) & 1) * R + i] = 0u;
-
-    float v[C::EPT];
-    // ---- phase R: widen, low-digit stages
-#pragma unroll
-    for (int j = 0; j < SEGS; ++j) {
-#pragma unroll
-      for (int l = 0; l < C::LOADS; ++l) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          v[j * G1 + l * 16 + 2 * k] = bf16lo_f32(raw[j][l].w[k]);
-          v[j * G1 + l * 16 + 2 * k + 1] = bf16hi_f32(raw[j][l].w[k]);
-        }
-      }
-    }
-#pragma unroll
-    for (int d = 0; d < C::ND1; ++d) {
-      const int st = 1 << (2 * d);
-#pragma unroll
-      for (int j = 0; j < SEGS; ++j) {
-#pragma unroll
-        for (int base = 0; base < G1; base += 4 * st) {
-#pragma unroll
-          for (int o = 0; o < st; ++o) {
-            float* p = v + j * G1 + base + o;
-            h4_stage(p[0], p[st], p[2 * st], p[3 * st]);
-          }
-        }
-      }
-    }
+    const long long tile_off = tile * static_cast<long long>(tile_elems);
+    const long long next = tile + gridDim.x;
 
     if constexpr (C::PHASE_C) {
-      // ---- transpose through shared memory
+      // ---- phase R: widen, low-digit stages, park the row in shared memory
       if (active) {
 #pragma unroll
         for (int j = 0; j < SEGS; ++j) {
-          const int c0 = seg_off[j] >> 2;
+          float v[G1];
 #pragma unroll
-          for (int k = 0; k < G1 / 4; ++k) {
-            float4 f = make_float4(v[j * G1 + 4 * k], v[j * G1 + 4 * k + 1], v[j * G1 + 4 * k + 2],
-                                   v[j * G1 + 4 * k + 3]);
-            reinterpret_cast<float4*>(fbuf)[swz_chunk<G, G1>(c0 + k)] = f;
+          for (int l = 0; l < C::LOADS; ++l)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              v[l * 16 + 2 * k] = bf16lo_f32(raw[j][l].w[k]);
+              v[l * 16 + 2 * k + 1] = bf16hi_f32(raw[j][l].w[k]);
+            }
+#pragma unroll
+          for (int d = 0; d < C::ND1; ++d) {
+            const int st = 1 << (2 * d);
+#pragma unroll
+            for (int base = 0; base < G1; base += 4 * st)
+#pragma unroll
+              for (int o = 0; o < st; ++o) h4_stage(v[base + o], v[base + o + st], v[base + o + 2 * st], v[base + o + 3 * st]);
+          }
+          const int c0 = ((tid + j * NT) * G1) >> 2;
+#pragma unroll
+          for (int k = 0; k < G1 / 4; ++k)
+            reinterpret_cast<float4*>(fbuf)[swz_chunk<G, G1>(c0 + k)] =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+      }
+      // the raw registers are free: start the next tile's loads now
+      if (next < ntiles) issue_loads(next);
+      __syncthreads();
+
+      // ---- phase C: high-digit stages in place, two columns per packed op
+      float m_unit[C::NU];
+#pragma unroll
+      for (int i = 0; i < C::NU; ++i) {
+        float m = 0.0f;
+        if (active) {
+          float2 w[C::G2];
+          int addr[C::G2];
+#pragma unroll
+          for (int h = 0; h < C::G2; ++h) {
+            const int e = unit_base[i] + h * G1;
+            addr[h] = 2 * swz_chunk<G, G1>(e >> 2) + ((e >> 1) & 1);  // float2 slot
+            w[h] = reinterpret_cast<const float2*>(fbuf)[addr[h]];
+          }
+#pragma unroll
+          for (int d = 0; d < C::ND2; ++d) {
+            const int st = 1 << (2 * d);
+#pragma unroll
+            for (int base = 0; base < C::G2; base += 4 * st)
+#pragma unroll
+              for (int o = 0; o < st; ++o)
+                h4_stage(w[base + o], w[base + o + st], w[base + o + 2 * st], w[base + o + 3 * st]);
+          }
+#pragma unroll
+          for (int h = 0; h < C::G2; ++h) {
+            reinterpret_cast<float2*>(fbuf)[addr[h]] = w[h];
+            m = fmax3(m, fabsf(w[h].x), fabsf(w[h].y));
           }
         }
+        m_unit[i] = m;
+      }
+      // per-row absmax: warp max over lanes of the same row, one atomic each
+#pragma unroll
+      for (int i = 0; i < C::NU; ++i) {
+        const int row = active ? unit_row[i] : -1;
+        const unsigned grp = __match_any_sync(0xffffffffu, row);
+        const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m_unit[i]));
+        if (active && lane == __ffs(grp) - 1) atomicMax(&rowmax[row], mx);
+      }
+      __syncthreads();
+
+      // ---- quantize in the load layout: coalesced stores straight to HBM
+      if (active) {
+#pragma unroll
+        for (int j = 0; j < SEGS; ++j) {
+          const int seg = tid + j * NT;
+          const float amax = __uint_as_float(rowmax[seg_row[j]]);
+          const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+          const int c0 = (seg * G1) >> 2;
+#pragma unroll
+          for (int s16 = 0; s16 < G1 / 16; ++s16) {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float4 f = reinterpret_cast<const float4*>(fbuf)[swz_chunk<G, G1>(c0 + 4 * s16 + k)];
+              v[4 * k] = f.x;
+              v[4 * k + 1] = f.y;
+              v[4 * k + 2] = f.z;
+              v[4 * k + 3] = f.w;
+            }
+            quantize_store<16>(v, inv, tile_off + static_cast<long long>(seg) * G1 + 16 * s16, total_elems, Q, Q16);
+          }
+        }
+      }
+    } else {
+      // ---- G <= 16: a segment holds whole groups; everything stays in registers
+      float v[SEGS][G1];
+#pragma unroll
+      for (int j = 0; j < SEGS; ++j)
+#pragma unroll
+        for (int l = 0; l < C::LOADS; ++l)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            v[j][l * 16 + 2 * k] = bf16lo_f32(raw[j][l].w[k]);
+            v[j][l * 16 + 2 * k + 1] = bf16hi_f32(raw[j][l].w[k]);
+          }
+      if (next < ntiles) issue_loads(next);
+#pragma unroll
+      for (int d = 0; d < C::ND1; ++d) {
+        const int st = 1 << (2 * d);
+#pragma unroll
+        for (int j = 0; j < SEGS; ++j)
+#pragma unroll
+          for (int base = 0; base < G1; base += 4 * st)
+#pragma unroll
+            for (int o = 0; o < st; ++o)
+              h4_stage(v[j][base + o], v[j][base + o + st], v[j][base + o + 2 * st], v[j][base + o + 3 * st]);
+      }
+#pragma unroll
+      for (int j = 0; j < SEGS; ++j) {
+        float m = 0.0f;
+        if (active) {
+#pragma unroll
+          for (int e = 0; e < G1; e += 2) m = fmax3(m, fabsf(v[j][e]), fabsf(v[j][e + 1]));
+        }
+        const int row = active ? seg_row[j] : -1;
+        const unsigned grp = __match_any_sync(0xffffffffu, row);
+        const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
+        if (active && lane == __ffs(grp) - 1) atomicMax(&rowmax[row], mx);
       }
       __syncthreads();
       if (active) {
 #pragma unroll
-        for (int i = 0; i < C::NB; ++i) {
-#pragma unroll
-          for (int h = 0; h < C::G2; ++h) {
-            const float4 f =
-                reinterpret_cast<const float4*>(fbuf)[swz_chunk<G, G1>((blk_base[i] >> 2) + h * (G1 / 4))];
-            float* p = v + i * 4 * C::G2 + 4 * h;
-            p[0] = f.x;
-            p[1] = f.y;
-            p[2] = f.z;
-            p[3] = f.w;
-          }
-        }
-        // high-digit stages: digit d of h has stride 4^d rows = 4 * 4^d floats
-#pragma unroll
-        for (int d = 0; d < C::ND2; ++d) {
-          const int st = 4 << (2 * d);
-#pragma unroll
-          for (int i = 0; i < C::NB; ++i) {
-#pragma unroll
-            for (int base = 0; base < 4 * C::G2; base += 4 * st) {
-#pragma unroll
-              for (int o = 0; o < st; o += 2) {
-                float* p = v + i * 4 * C::G2 + base + o;
-                float2 a0 = make_float2(p[0], p[1]), a1 = make_float2(p[st], p[st + 1]);
-                float2 a2 = make_float2(p[2 * st], p[2 * st + 1]), a3 = make_float2(p[3 * st], p[3 * st + 1]);
-                h4_stage(a0, a1, a2, a3);
-                p[0] = a0.x; p[1] = a0.y;
-                p[st] = a1.x; p[st + 1] = a1.y;
-                p[2 * st] = a2.x; p[2 * st + 1] = a2.y;
-                p[3 * st] = a3.x; p[3 * st + 1] = a3.y;
-              }
-            }
-          }
-        }
-        // per-row absmax of each block
-#pragma unroll
-        for (int i = 0; i < C::NB; ++i) {
-          float m = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 4 * C::G2; e += 2)
-            m = fmax3(m, fabsf(v[i * 4 * C::G2 + e]), fabsf(v[i * 4 * C::G2 + e + 1]));
-          atomicMax(&rowmax[blk_row[i]], __float_as_uint(m));
-        }
-      }
-    } else {
-      if (active) {
-#pragma unroll
         for (int j = 0; j < SEGS; ++j) {
-          float m = 0.0f;
-#pragma unroll
-          for (int e = 0; e < G1; e += 2) m = fmax3(m, fabsf(v[j * G1 + e]), fabsf(v[j * G1 + e + 1]));
-          atomicMax(&rowmax[seg_off[j] / K], __float_as_uint(m));
-        }
-      }
-    }
-    __syncthreads();
-
-    // ---- quantize
-    if (active) {
-      if constexpr (C::PHASE_C) {
-#pragma unroll
-        for (int i = 0; i < C::NB; ++i) {
-          const float amax = __uint_as_float(rowmax[blk_row[i]]);
+          const float amax = __uint_as_float(rowmax[seg_row[j]]);
           const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
-#pragma unroll
-          for (int h = 0; h < C::G2; ++h) {
-            const float* p = v + i * 4 * C::G2 + 4 * h;
-            const float t0 = fmaf(p[0], inv, kRoundMagic), t1 = fmaf(p[1], inv, kRoundMagic);
-            const float t2 = fmaf(p[2], inv, kRoundMagic), t3 = fmaf(p[3], inv, kRoundMagic);
-            const uint32_t b01 = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040);
-            const uint32_t b23 = __byte_perm(__float_as_uint(t2), __float_as_uint(t3), 0x0040);
-            const int w = (blk_base[i] >> 2) + h * (G1 / 4);
-            stage_q[swz_word<G, G1>(w)] = __byte_perm(b01, b23, 0x5410);
-            if (Q16) {
-              const __half2 h01 = __floats2half2_rn(t0 - kRoundMagic, t1 - kRoundMagic);
-              const __half2 h23 = __floats2half2_rn(t2 - kRoundMagic, t3 - kRoundMagic);
-              uint2 u;
-              u.x = *reinterpret_cast<const uint32_t*>(&h01);
-              u.y = *reinterpret_cast<const uint32_t*>(&h23);
-              stage_h[swz_word<G, G1>(w)] = u;
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < SEGS; ++j) {
-          const int e = seg_off[j];
-          const int r = e / K, col = e % K;
-          const long long row = tile * R + r;
-          const float amax = __uint_as_float(rowmax[r]);
-          const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
-          uint32_t words[G1 / 4];
-          uint32_t hw[G1 / 2];
-#pragma unroll
-          for (int k = 0; k < G1 / 4; ++k) {
-            const float* p = v + j * G1 + 4 * k;
-            const float t0 = fmaf(p[0], inv, kRoundMagic), t1 = fmaf(p[1], inv, kRoundMagic);
-            const float t2 = fmaf(p[2], inv, kRoundMagic), t3 = fmaf(p[3], inv, kRoundMagic);
-            const uint32_t b01 = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040);
-            const uint32_t b23 = __byte_perm(__float_as_uint(t2), __float_as_uint(t3), 0x0040);
-            words[k] = __byte_perm(b01, b23, 0x5410);
-            if (Q16) {
-              const __half2 h01 = __floats2half2_rn(t0 - kRoundMagic, t1 - kRoundMagic);
-              const __half2 h23 = __floats2half2_rn(t2 - kRoundMagic, t3 - kRoundMagic);
-              hw[2 * k] = *reinterpret_cast<const uint32_t*>(&h01);
-              hw[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-            }
-          }
-          if (row < M) {
-            int8_t* q = Q + row * (long long)K + col;
-#pragma unroll
-            for (int k = 0; k < G1 / 16; ++k)
-              stg_128(q + 16 * k, make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]));
-            if (Q16) {
-              __half* qh = Q16 + row * (long long)K + col;
-#pragma unroll
-              for (int k = 0; k < G1 / 8; ++k)
-                stg_128(qh + 8 * k, make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]));
-            }
-          }
+          quantize_store<G1>(v[j], inv, tile_off + static_cast<long long>(tid + j * NT) * G1, total_elems, Q, Q16);
         }
       }
     }
     for (int i = tid; i < R; i += blockDim.x)
       if (tile * R + i < M) S[tile * R + i] = __uint_as_float(rowmax[i]) / s_div;
-
-    // ---- prefetch the next tile, then drain the staging buffers
-    const long long next = tile + gridDim.x;
-    if (next < ntiles) issue_loads(next);
-    if constexpr (C::PHASE_C) {
-      __syncthreads();
-      const int pieces = tile_elems / 16;
-      for (int pc = tid; pc < pieces; pc += blockDim.x) {
-        const int e = pc * 16;
-        const int r = e / K, col = e % K;
-        const long long row = tile * R + r;
-        if (row < M) {
-          const uint4 val = reinterpret_cast<const uint4*>(stage_q)[swz_word<G, G1>(4 * pc) >> 2];
-          stg_128(Q + row * (long long)K + col, val);
-        }
-      }
-      if (Q16) {
-        const int hpieces = tile_elems / 8;
-        for (int pc = tid; pc < hpieces; pc += blockDim.x) {
-          const int e = pc * 8;
-          const int r = e / K, col = e % K;
-          const long long row = tile * R + r;
-          if (row < M) {
-            const uint4 val = reinterpret_cast<const uint4*>(stage_h)[swz_word<G, G1>(2 * pc) >> 1];
-            stg_128(Q16 + row * (long long)K + col, val);
-          }
-        }
-      }
-    }
     __syncthreads();
   }
 }
@@ -461,12 +436,6 @@ static float scale_divisor(int transform, int G) {
   return 127.0f;
 }
 
-static int num_sms() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
-}
 
 // Rows per tile: the smallest R for which R*K/EPT threads fill whole warps
 // (or nearly), within the thread and shared-memory limits.
@@ -505,24 +474,20 @@ static cudaError_t launch_fast(const __nv_bfloat16* X, long long M, int K, long 
   int R = 0, NT = 0;
   if (!choose_rows(K, C::EPT, C::PHASE_C, &R, &NT)) return cudaSuccess;
   const int threads = (NT + 31) / 32 * 32;
-  const int tile_elems = R * K;
-  // staging: int8 codes [tile] then fp16 copies [tile], each padded to 256 B;
-  // the fp32 transpose buffer [tile] aliases both. rowmax follows.
-  const int stage_bytes = ((tile_elems + 255) / 256) * 256;
-  const int fbytes = ((tile_elems * 4 + 511) / 512) * 512;
-  const int need = std::max(fbytes, 3 * stage_bytes);
-  const int smem = std::max(need, 4 * stage_bytes) + 2 * R * 4;
+  // fp32 tile buffer (rounded up to whole swizzle blocks), then the row maxima
+  const int fbytes = C::PHASE_C ? ((R * K * 4 + 511) / 512) * 512 : 0;
+  const int smem = fbytes + 2 * R * 4;
   auto kern = rq_fast_kernel<G, G1, SEGS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  e = blocks_per_sm(reinterpret_cast<const void*>(kern), threads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaSuccess;
   const long long tiles = (M + R - 1) / R;
-  const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * num_sms());
+  const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(X, M, K, ldx, R, NT, Q, S, Q16,
-                                                             scale_divisor(CONVROT_T_REGULAR_H4, G), stage_bytes);
+                                                             scale_divisor(CONVROT_T_REGULAR_H4, G), fbytes);
   *launched = true;
   return cudaGetLastError();
 }
@@ -547,7 +512,7 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
       case 4: e = launch_fast<4, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
       case 16: e = launch_fast<16, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
       case 64: e = launch_fast<64, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 256: e = launch_fast<256, 16, 4>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 256: e = launch_fast<256, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
       case 1024: e = launch_fast<1024, 64, 1>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
       default: break;
     }
@@ -559,17 +524,17 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
   }
   const int threads = 256;
   const size_t smem = static_cast<size_t>(K) * sizeof(float);
-  const long long grid = std::min<long long>(M, 64LL * num_sms());
+  const long long grid = std::min<long long>(M, 64LL * device_sm_count());
   const float sdiv = scale_divisor(transform, G);
   if (in_dtype == CONVROT_DTYPE_BF16) {
     auto kern = rq_generic_kernel<__nv_bfloat16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(static_cast<const __nv_bfloat16*>(X), M, K, ldx,
                                                              transform, G, signs, Q, S, q16, sdiv);
   } else {
     auto kern = rq_generic_kernel<float>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(static_cast<const float*>(X), M, K, ldx, transform, G,
                                                              signs, Q, S, q16, sdiv);
