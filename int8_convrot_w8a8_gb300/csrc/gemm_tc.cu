@@ -85,12 +85,6 @@ struct TcParams {
 };
 
 // ---- PTX wrappers ----------------------------------------------------------
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -385,19 +379,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
 // ---- host -------------------------------------------------------------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn lookup_encode_fn() {
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return nullptr;
-  return reinterpret_cast<EncodeTiledFn>(fn);
-}
-
 bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long rows, int K, int box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
@@ -408,11 +389,6 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The driver's tensor-map encoder, looked up once per process.
-EncodeTiledFn encode_fn() {
-  static const EncodeTiledFn fn = lookup_encode_fn();
-  return fn;
-}
 
 // Column tile: the BN whose last wave wastes the least, by the estimate
 // waves(BN) * BN (a tile's time grows with BN); ties go to the wider tile.
@@ -472,7 +448,7 @@ bool gemm_tc_supported(long long M, int K) { return M > 64 && K % BK == 0 && K >
 cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
                            bool raw, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const int sms = device_sm_count();
   const int bn = choose_bn(M, outs, sms);

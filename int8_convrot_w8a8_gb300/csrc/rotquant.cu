@@ -125,306 +125,203 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
 }
 
 // =============================================================== fast ======
-// Fast kernel for bf16 input and the regular Hadamard.
+// Fast kernel for bf16 input and the regular Hadamard (K a multiple of 64,
+// G <= 1024).
 //
 // A CTA owns a tile of R consecutive rows (persistent grid-stride loop).
-//  Phase R: each thread takes SEGS segments of G1 consecutive elements,
-//    loaded with 32-byte loads (a warp reads 1 KB contiguous per load), and
-//    runs the radix-4 stages of the low digits in registers (G1 = 16: two
-//    digits, G1 = 64: three). The loads of the next tile are issued as soon
-//    as these registers are free.
-//  Phase C (G > G1): the rotated segments are parked in shared memory as
-//    fp32 (XOR-swizzled against bank conflicts), where the row stays across
-//    the reduction. Each thread then runs the high digits on units of
-//    G2 = G/G1 rows x 2 adjacent columns of the group seen as a G2 x G1
-//    matrix, two columns per packed fp32x2 operation, and writes the unit
-//    back in place.
-//  Row absmax: a warp reduction over the lanes of each row (lanes of one
-//    warp may straddle two rows), then one shared-memory atomicMax.
-//  Quantize: in the load layout again, so the int8 codes (16-byte stores)
-//    and the fp16 copies (32-byte stores) leave coalesced, straight to HBM.
-// With G <= 16 a segment holds whole groups and nothing leaves registers.
+//  Load: one 3-D TMA copy per tile brings the R rows into shared memory as
+//    128-byte lines (64 bf16) with the 128B swizzle; two stage buffers
+//    alternate and the next tile's copy is issued when the current starts.
+//  Each thread owns one line: 64 consecutive elements of a row, held in
+//    registers as 32 fp32 pairs from load to store.
+//  In-lane digits: the radix-4 stages of the three low digits (d0 scalar,
+//    d1 and d2 on packed fp32x2 pairs of adjacent elements).
+//  Cross-lane digits (G = 256: one, G = 1024: two): the lanes that share a
+//    group exchange values with two shuffles per element, u = x + x[a^1],
+//    w = x - x[a^1], y = u + w[a^2], which is the same operation sequence,
+//    bit for bit, as the in-register stage.
+//  Row absmax: warp reduction (one instruction when the warp lies in one
+//    row), one shared-memory atomicMax per warp and row, one barrier.
+//  Quantize straight from registers: the 64 int8 codes leave as two 32-byte
+//    stores, the fp16 copies as four, each a whole 32-byte sector.
 
-template <int G, int G1, int SEGS>
-struct FastCfg {
-  static constexpr int G2 = G > G1 ? G / G1 : 1;
-  static constexpr int ND1 = ilog4_c(G < G1 ? G : G1);
-  static constexpr int ND2 = ilog4_c(G2);
-  static constexpr int EPT = SEGS * G1;
-  static constexpr bool PHASE_C = G2 > 1;
-  static constexpr int NU = PHASE_C ? EPT / (2 * G2) : 0;  // phase-C units per thread
-  static constexpr int LOADS = G1 / 16;
+template <int G>
+struct LaneCfg {
+  static constexpr int N = ilog4_c(G);
+  static constexpr int NIN = N < 3 ? N : 3;  // digits inside a 64-element line
+  static constexpr int NX = N - NIN;         // digits across lanes
+  static_assert(NX <= 2, "G <= 1024");
 };
 
-// fp32 buffer: 16-byte chunk index -> physical chunk (a bijection inside each
-// aligned block of 8 chunks).
-template <int G, int G1>
-__device__ __forceinline__ int swz_chunk(int c) {
-  if constexpr (G1 == 16) {
-    constexpr int GS = ilog2_c(G / 4 > 1 ? G / 4 : 2);
-    return c ^ ((c >> 3) & 7) ^ (((c >> GS) & 1) << 2);
-  } else {
-    return c ^ ((c >> 4) & 7);
-  }
-}
-// Quantize N consecutive values of one row (N a multiple of 16) and store the
-// codes (16-byte stores) and, if requested, their fp16 copies (32-byte
-// stores) at dense element offset e, if e lies inside the matrix.
-template <int N>
-__device__ __forceinline__ void quantize_store(const float (&p)[N], float inv, long long e, long long total_elems,
-                                               int8_t* __restrict__ Q, __half* __restrict__ Q16) {
-  const float2 inv2 = make_float2(inv, inv);
-  const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
-#pragma unroll
-  for (int k16 = 0; k16 < N / 16; ++k16) {
-    uint32_t words[4];
-    uint32_t hw[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int o = 16 * k16 + 4 * k;
-      const float2 t01 = f2_fma(make_float2(p[o], p[o + 1]), inv2, mg2);
-      const float2 t23 = f2_fma(make_float2(p[o + 2], p[o + 3]), inv2, mg2);
-      const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
-      const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
-      words[k] = __byte_perm(b01, b23, 0x5410);
-      if (Q16) {
-        const float2 c01 = f2_sub(t01, mg2), c23 = f2_sub(t23, mg2);
-        const __half2 h01 = __floats2half2_rn(c01.x, c01.y);
-        const __half2 h23 = __floats2half2_rn(c23.x, c23.y);
-        hw[2 * k] = *reinterpret_cast<const uint32_t*>(&h01);
-        hw[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-      }
-    }
-    if (e < total_elems) {
-      stg_128(Q + e + 16 * k16, make_uint4(words[0], words[1], words[2], words[3]));
-      if (Q16) stg_256(Q16 + e + 16 * k16, hw);
-    }
-  }
+// One radix-4 stage, unnormalized, on lanes: this lane holds digit value
+// a = (lane >> shift) & 3 of the quad it exchanges with.
+template <int SHIFT>
+__device__ __forceinline__ float2 h4_xlane(float2 x) {
+  constexpr int m1 = 1 << SHIFT, m2 = 2 << SHIFT;
+  float2 t;
+  t.x = __shfl_xor_sync(0xffffffffu, x.x, m1);
+  t.y = __shfl_xor_sync(0xffffffffu, x.y, m1);
+  const float2 u = f2_add(x, t);
+  float2 w = f2_sub(x, t);
+  w.x = __shfl_xor_sync(0xffffffffu, w.x, m2);
+  w.y = __shfl_xor_sync(0xffffffffu, w.y, m2);
+  return f2_add(u, w);
 }
 
-template <int G, int G1, int SEGS>
-__global__ void __launch_bounds__(384) rq_fast_kernel(const __nv_bfloat16* __restrict__ X, long long M, int K,
-                                                       long long ldx, int R, int NT, int8_t* __restrict__ Q,
-                                                       float* __restrict__ S, __half* __restrict__ Q16,
-                                                       float s_div, int fbytes) {
-  using C = FastCfg<G, G1, SEGS>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  float* fbuf = reinterpret_cast<float*>(smem);
-  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + fbytes);  // [2][R]
+template <int G>
+__global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CUtensorMap xmap, long long M, int K,
+                                                       int R, int NT, int8_t* __restrict__ Q, float* __restrict__ S,
+                                                       __half* __restrict__ Q16, float s_div, int stage_bytes,
+                                                       long long spin_limit) {
+  using C = LaneCfg<G>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_base = smem_u32(smem);
+  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + 2 * stage_bytes);  // [3][R]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));         // [2]
 
   const int tid = threadIdx.x, lane = tid & 31;
   const bool active = tid < NT;
   const long long ntiles = (M + R - 1) / R;
-  const int tile_elems = R * K;
+  const int lines_per_row = K >> 6;
+  const int my_row = active ? tid / lines_per_row : -1;
+  const uint32_t tile_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(K) * 2u;
   const long long total_elems = M * static_cast<long long>(K);
+  // whether this warp's active lanes all belong to one row
+  const int row_first = __shfl_sync(0xffffffffu, my_row, 0);
+  const bool warp_one_row = __all_sync(0xffffffffu, my_row == row_first);
 
-  // Tile-invariant geometry, computed once: the row of each of this
-  // thread's segments and its offset in X. The outputs are dense [M, K], so
-  // their offsets need no row / column split.
-  int seg_row[SEGS];
-  long long seg_xoff[SEGS];
-#pragma unroll
-  for (int j = 0; j < SEGS; ++j) {
-    const int e = (tid + j * NT) * G1;
-    seg_row[j] = e / K;
-    seg_xoff[j] = seg_row[j] * ldx + (e - seg_row[j] * K);
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // Phase-C units: G2 rows x 2 adjacent columns of one group matrix.
-  int unit_base[C::NU > 0 ? C::NU : 1];
-  int unit_row[C::NU > 0 ? C::NU : 1];
-  if constexpr (C::PHASE_C) {
-    const int groups = K / G;
-#pragma unroll
-    for (int i = 0; i < C::NU; ++i) {
-      const int b = tid + i * NT;
-      const int cp = b % (G1 / 2);
-      const int rest = b / (G1 / 2);
-      const int g = rest % groups;
-      const int r = rest / groups;
-      unit_row[i] = r;
-      unit_base[i] = r * K + g * G + 2 * cp;
-    }
-  }
-
-  U32x8 raw[SEGS][C::LOADS];
-  auto issue_loads = [&](long long tile) {
-    const long long rbase = tile * R;
-    const __nv_bfloat16* xt = X + rbase * ldx;
-#pragma unroll
-    for (int j = 0; j < SEGS; ++j) {
-      const bool ok = active && rbase + seg_row[j] < M;
-#pragma unroll
-      for (int l = 0; l < C::LOADS; ++l) {
-        if (ok) {
-          raw[j][l] = ldg_nc_256(xt + seg_xoff[j] + 16 * l);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) raw[j][l].w[k] = 0u;
-        }
-      }
-    }
-  };
-
-  // Row maxima are double-buffered by iteration parity: the buffer of the
-  // next iteration is cleared during this one, after every read of it by the
-  // previous iteration has passed that iteration's final barrier.
-  for (int i = tid; i < 2 * R; i += blockDim.x) rowmax_buf[i] = 0u;
+  // Row maxima cycle through three buffers. Iteration `it` uses buffer
+  // it % 3 and clears (it + 1) % 3, last used two iterations earlier: every
+  // thread has passed the barrier of iteration it - 1, so every thread has
+  // finished reading it.
+  for (int i = tid; i < 3 * R; i += blockDim.x) rowmax_buf[i] = 0u;
   __syncthreads();
 
   long long tile = blockIdx.x;
-  if (tile < ntiles) issue_loads(tile);
+  if (tid == 0 && tile < ntiles) {
+    mbar_expect_tx(&bar[0], tile_bytes);
+    tma_load_3d(stage_base, &xmap, 0, 0, static_cast<int>(tile * R), &bar[0]);
+  }
 
   for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
-    unsigned int* rowmax = rowmax_buf + (it & 1) * R;
-    for (int i = tid; i < R; i += blockDim.x) rowmax_buf[((it + 1) & 1) * R + i] = 0u;
-    const long long tile_off = tile * static_cast<long long>(tile_elems);
+    const int buf = it & 1;
+    unsigned int* rowmax = rowmax_buf + (it % 3) * R;
+    for (int i = tid; i < R; i += blockDim.x) rowmax_buf[((it + 1) % 3) * R + i] = 0u;
     const long long next = tile + gridDim.x;
+    // the other stage buffer was last read before the previous iteration's
+    // barrier: refill it with the next tile now
+    if (tid == 0 && next < ntiles) {
+      mbar_expect_tx(&bar[buf ^ 1], tile_bytes);
+      tma_load_3d(stage_base + (buf ^ 1) * stage_bytes, &xmap, 0, 0, static_cast<int>(next * R), &bar[buf ^ 1]);
+    }
+    if (!mbar_wait_bounded(&bar[buf], (it >> 1) & 1, spin_limit) && tid == 0) record_status(CONVROT_ERR_TIMEOUT);
 
-    if constexpr (C::PHASE_C) {
-      // ---- phase R: widen, low-digit stages, park the row in shared memory
-      if (active) {
+    // ---- this thread's line: 64 bf16 -> 32 fp32 pairs
+    float2 v[32];
+    {
+      const uint32_t lb = stage_base + buf * stage_bytes + (static_cast<uint32_t>(tid) << 7);
 #pragma unroll
-        for (int j = 0; j < SEGS; ++j) {
-          float v[G1];
-#pragma unroll
-          for (int l = 0; l < C::LOADS; ++l)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              v[l * 16 + 2 * k] = bf16lo_f32(raw[j][l].w[k]);
-              v[l * 16 + 2 * k + 1] = bf16hi_f32(raw[j][l].w[k]);
-            }
-#pragma unroll
-          for (int d = 0; d < C::ND1; ++d) {
-            const int st = 1 << (2 * d);
-#pragma unroll
-            for (int base = 0; base < G1; base += 4 * st)
-#pragma unroll
-              for (int o = 0; o < st; ++o) h4_stage(v[base + o], v[base + o + st], v[base + o + 2 * st], v[base + o + 3 * st]);
-          }
-          const int c0 = ((tid + j * NT) * G1) >> 2;
-#pragma unroll
-          for (int k = 0; k < G1 / 4; ++k)
-            reinterpret_cast<float4*>(fbuf)[swz_chunk<G, G1>(c0 + k)] =
-                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        }
-      }
-      // the raw registers are free: start the next tile's loads now
-      if (next < ntiles) issue_loads(next);
-      __syncthreads();
-
-      // ---- phase C: high-digit stages in place, two columns per packed op
-      float m_unit[C::NU];
-#pragma unroll
-      for (int i = 0; i < C::NU; ++i) {
-        float m = 0.0f;
+      for (int k = 0; k < 8; ++k) {
+        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
         if (active) {
-          float2 w[C::G2];
-          int addr[C::G2];
-#pragma unroll
-          for (int h = 0; h < C::G2; ++h) {
-            const int e = unit_base[i] + h * G1;
-            addr[h] = 2 * swz_chunk<G, G1>(e >> 2) + ((e >> 1) & 1);  // float2 slot
-            w[h] = reinterpret_cast<const float2*>(fbuf)[addr[h]];
-          }
-#pragma unroll
-          for (int d = 0; d < C::ND2; ++d) {
-            const int st = 1 << (2 * d);
-#pragma unroll
-            for (int base = 0; base < C::G2; base += 4 * st)
-#pragma unroll
-              for (int o = 0; o < st; ++o)
-                h4_stage(w[base + o], w[base + o + st], w[base + o + 2 * st], w[base + o + 3 * st]);
-          }
-#pragma unroll
-          for (int h = 0; h < C::G2; ++h) {
-            reinterpret_cast<float2*>(fbuf)[addr[h]] = w[h];
-            m = fmax3(m, fabsf(w[h].x), fabsf(w[h].y));
-          }
+          const uint32_t addr = lb + ((k ^ (tid & 7)) << 4);
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
         }
-        m_unit[i] = m;
+        v[4 * k + 0] = make_float2(bf16lo_f32(w0), bf16hi_f32(w0));
+        v[4 * k + 1] = make_float2(bf16lo_f32(w1), bf16hi_f32(w1));
+        v[4 * k + 2] = make_float2(bf16lo_f32(w2), bf16hi_f32(w2));
+        v[4 * k + 3] = make_float2(bf16lo_f32(w3), bf16hi_f32(w3));
       }
-      // per-row absmax: warp max over lanes of the same row, one atomic each
+    }
+    // ---- digit 0: elements (4q .. 4q+3) = v[2q].x, v[2q].y, v[2q+1].x, v[2q+1].y
+    if constexpr (C::NIN >= 1) {
 #pragma unroll
-      for (int i = 0; i < C::NU; ++i) {
-        const int row = active ? unit_row[i] : -1;
-        const unsigned grp = __match_any_sync(0xffffffffu, row);
-        const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m_unit[i]));
-        if (active && lane == __ffs(grp) - 1) atomicMax(&rowmax[row], mx);
-      }
-      __syncthreads();
+      for (int q = 0; q < 16; ++q) h4_stage(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y);
+    }
+    // ---- digit 1 (stride 4 elements = 2 pairs) and digit 2 (stride 16 = 8 pairs), packed
+    if constexpr (C::NIN >= 2) {
+#pragma unroll
+      for (int b = 0; b < 32; b += 8)
+#pragma unroll
+        for (int o = 0; o < 2; ++o) h4_stage(v[b + o], v[b + o + 2], v[b + o + 4], v[b + o + 6]);
+    }
+    if constexpr (C::NIN >= 3) {
+#pragma unroll
+      for (int o = 0; o < 8; ++o) h4_stage(v[o], v[o + 8], v[o + 16], v[o + 24]);
+    }
+    // ---- cross-lane digits: lane bits 0-1 hold digit 3, bits 2-3 digit 4
+    if constexpr (C::NX >= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = h4_xlane<0>(v[i]);
+    }
+    if constexpr (C::NX >= 2) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = h4_xlane<2>(v[i]);
+    }
 
-      // ---- quantize in the load layout: coalesced stores straight to HBM
-      if (active) {
+    // ---- row absmax
+    float m = 0.0f;
 #pragma unroll
-        for (int j = 0; j < SEGS; ++j) {
-          const int seg = tid + j * NT;
-          const float amax = __uint_as_float(rowmax[seg_row[j]]);
-          const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
-          const int c0 = (seg * G1) >> 2;
-#pragma unroll
-          for (int s16 = 0; s16 < G1 / 16; ++s16) {
-            float v[16];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float4 f = reinterpret_cast<const float4*>(fbuf)[swz_chunk<G, G1>(c0 + 4 * s16 + k)];
-              v[4 * k] = f.x;
-              v[4 * k + 1] = f.y;
-              v[4 * k + 2] = f.z;
-              v[4 * k + 3] = f.w;
-            }
-            quantize_store<16>(v, inv, tile_off + static_cast<long long>(seg) * G1 + 16 * s16, total_elems, Q, Q16);
-          }
-        }
-      }
+    for (int i = 0; i < 32; ++i) m = fmax3(m, fabsf(v[i].x), fabsf(v[i].y));
+    if (warp_one_row) {
+      const unsigned mx = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      if (lane == 0 && row_first >= 0) atomicMax(&rowmax[row_first], mx);
     } else {
-      // ---- G <= 16: a segment holds whole groups; everything stays in registers
-      float v[SEGS][G1];
+      const unsigned grp = __match_any_sync(0xffffffffu, my_row);
+      const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
+      if (active && lane == __ffs(grp) - 1) atomicMax(&rowmax[my_row], mx);
+    }
+    __syncthreads();
+
+    // ---- quantize and store
+    if (active) {
+      const float amax = __uint_as_float(rowmax[my_row]);
+      const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+      const float2 inv2 = make_float2(inv, inv);
+      const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+      const long long e0 = (tile * R) * static_cast<long long>(K) + (static_cast<long long>(tid) << 6);
+      if (e0 < total_elems) {
 #pragma unroll
-      for (int j = 0; j < SEGS; ++j)
-#pragma unroll
-        for (int l = 0; l < C::LOADS; ++l)
+        for (int h = 0; h < 2; ++h) {
+          uint32_t words[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            v[j][l * 16 + 2 * k] = bf16lo_f32(raw[j][l].w[k]);
-            v[j][l * 16 + 2 * k + 1] = bf16hi_f32(raw[j][l].w[k]);
+            const float2 t01 = f2_fma(v[16 * h + 2 * k], inv2, mg2);
+            const float2 t23 = f2_fma(v[16 * h + 2 * k + 1], inv2, mg2);
+            const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
+            const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
+            words[k] = __byte_perm(b01, b23, 0x5410);
+            if (Q16) {
+              // reuse the rounded values: code = t - magic, exact in fp16
+              v[16 * h + 2 * k] = f2_sub(t01, mg2);
+              v[16 * h + 2 * k + 1] = f2_sub(t23, mg2);
+            }
           }
-      if (next < ntiles) issue_loads(next);
-#pragma unroll
-      for (int d = 0; d < C::ND1; ++d) {
-        const int st = 1 << (2 * d);
-#pragma unroll
-        for (int j = 0; j < SEGS; ++j)
-#pragma unroll
-          for (int base = 0; base < G1; base += 4 * st)
-#pragma unroll
-            for (int o = 0; o < st; ++o)
-              h4_stage(v[j][base + o], v[j][base + o + st], v[j][base + o + 2 * st], v[j][base + o + 3 * st]);
-      }
-#pragma unroll
-      for (int j = 0; j < SEGS; ++j) {
-        float m = 0.0f;
-        if (active) {
-#pragma unroll
-          for (int e = 0; e < G1; e += 2) m = fmax3(m, fabsf(v[j][e]), fabsf(v[j][e + 1]));
+          stg_256(Q + e0 + 32 * h, words);
         }
-        const int row = active ? seg_row[j] : -1;
-        const unsigned grp = __match_any_sync(0xffffffffu, row);
-        const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
-        if (active && lane == __ffs(grp) - 1) atomicMax(&rowmax[row], mx);
-      }
-      __syncthreads();
-      if (active) {
+        if (Q16) {
 #pragma unroll
-        for (int j = 0; j < SEGS; ++j) {
-          const float amax = __uint_as_float(rowmax[seg_row[j]]);
-          const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
-          quantize_store<G1>(v[j], inv, tile_off + static_cast<long long>(tid + j * NT) * G1, total_elems, Q, Q16);
+          for (int h = 0; h < 4; ++h) {
+            uint32_t hw[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const __half2 p = __floats2half2_rn(v[8 * h + k].x, v[8 * h + k].y);
+              hw[k] = *reinterpret_cast<const uint32_t*>(&p);
+            }
+            stg_256(Q16 + e0 + 16 * h, hw);
+          }
         }
       }
     }
     for (int i = tid; i < R; i += blockDim.x)
       if (tile * R + i < M) S[tile * R + i] = __uint_as_float(rowmax[i]) / s_div;
-    __syncthreads();
   }
 }
 
@@ -438,7 +335,7 @@ static float scale_divisor(int transform, int G) {
 
 
 // Rows per tile: the smallest R for which R*K/EPT threads fill whole warps
-// (or nearly), within the thread and shared-memory limits.
+// (or nearly), within the thread, TMA box and shared-memory limits.
 static bool choose_rows(int K, int ept, bool phase_c, int* R_out, int* NT_out) {
   int bestR = -1, bestNT = 0;
   double best_eff = -1.0;
@@ -446,7 +343,8 @@ static bool choose_rows(int K, int ept, bool phase_c, int* R_out, int* NT_out) {
     if ((static_cast<long long>(R) * K) % ept) continue;
     const int NT = static_cast<int>(static_cast<long long>(R) * K / ept);
     if (NT > 384) break;
-    if (phase_c && static_cast<long long>(R) * K * 4 > 96 * 1024) break;
+    const long long bytes = static_cast<long long>(R) * K * (phase_c ? 8 : 4);
+    if (bytes > 100 * 1024) break;
     const int pad = (NT + 31) / 32 * 32;
     const double eff = static_cast<double>(NT) / pad;
     if (NT >= 96 && eff >= 0.95) {
@@ -466,18 +364,29 @@ static bool choose_rows(int K, int ept, bool phase_c, int* R_out, int* NT_out) {
   return true;
 }
 
-template <int G, int G1, int SEGS>
-static cudaError_t launch_fast(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
+template <int G>
+static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
                                __half* Q16, cudaStream_t st, bool* launched) {
-  using C = FastCfg<G, G1, SEGS>;
   *launched = false;
+  if (K % 64 != 0 || K / 64 > 256 || M > 0x7fffffffLL) return cudaSuccess;
   int R = 0, NT = 0;
-  if (!choose_rows(K, C::EPT, C::PHASE_C, &R, &NT)) return cudaSuccess;
+  if (!choose_rows(K, 64, false, &R, &NT)) return cudaSuccess;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return cudaSuccess;
+  // X viewed as [M][K/64][64] bf16; one box is one tile of R rows.
+  CUtensorMap map;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(ldx) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(K / 64), static_cast<cuuint32_t>(R)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(X), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaSuccess;
   const int threads = (NT + 31) / 32 * 32;
-  // fp32 tile buffer (rounded up to whole swizzle blocks), then the row maxima
-  const int fbytes = C::PHASE_C ? ((R * K * 4 + 511) / 512) * 512 : 0;
-  const int smem = fbytes + 2 * R * 4;
-  auto kern = rq_fast_kernel<G, G1, SEGS>;
+  const int stage_bytes = ((R * K * 2 + 1023) / 1024) * 1024;
+  const int smem = 1024 + 2 * stage_bytes + ((3 * R + 1) & ~1) * 4 + 2 * 8;
+  auto kern = rq_lane_kernel<G>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -486,8 +395,9 @@ static cudaError_t launch_fast(const __nv_bfloat16* X, long long M, int K, long 
   if (per_sm < 1) return cudaSuccess;
   const long long tiles = (M + R - 1) / R;
   const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
-  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(X, M, K, ldx, R, NT, Q, S, Q16,
-                                                             scale_divisor(CONVROT_T_REGULAR_H4, G), fbytes);
+  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, Q, S, Q16,
+                                                             scale_divisor(CONVROT_T_REGULAR_H4, G), stage_bytes,
+                                                             kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
 }
@@ -500,20 +410,22 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
   *path = 0;
   if (M <= 0) return cudaSuccess;
   __half* q16 = reinterpret_cast<__half*>(Q16);
-  const bool aligned32 = (reinterpret_cast<uintptr_t>(X) % 32 == 0) && (ldx % 16 == 0) &&
-                         (reinterpret_cast<uintptr_t>(Q) % 16 == 0) &&
-                         (Q16 == nullptr || reinterpret_cast<uintptr_t>(Q16) % 16 == 0);
+  // the fast kernel reads X by TMA (16-byte aligned base, row stride a
+  // multiple of 16 bytes) and stores 32-byte pieces
+  const bool aligned32 = (reinterpret_cast<uintptr_t>(X) % 16 == 0) && (ldx % 8 == 0) &&
+                         (reinterpret_cast<uintptr_t>(Q) % 32 == 0) &&
+                         (Q16 == nullptr || reinterpret_cast<uintptr_t>(Q16) % 32 == 0);
   if (!force_generic && in_dtype == CONVROT_DTYPE_BF16 && transform == CONVROT_T_REGULAR_H4 && aligned32 &&
       K % 16 == 0) {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
     bool launched = false;
     cudaError_t e = cudaSuccess;
     switch (G) {
-      case 4: e = launch_fast<4, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 16: e = launch_fast<16, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 64: e = launch_fast<64, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 256: e = launch_fast<256, 16, 2>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 1024: e = launch_fast<1024, 64, 1>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 4: e = launch_lane<4>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 16: e = launch_lane<16>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 64: e = launch_lane<64>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 256: e = launch_lane<256>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 1024: e = launch_lane<1024>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
       default: break;
     }
     if (e != cudaSuccess) return e;

@@ -61,20 +61,25 @@ def test_tiny_workload_spikes_spread(cr):
 
 
 def test_fast_and_generic_paths_are_bit_identical(cr):
-    """An X view that is 16- but not 32-byte aligned takes the generic kernel;
-    both kernels run the same fp32 operations, so the results are equal."""
-    wl = WL.make_case(40, 6144 + 8, [], seed=11)
-    Xfull = wl.X.cuda()
-    X_al = Xfull[:, :6144].contiguous()
-    X_un = Xfull[:, 8:]            # 16-byte offset, row stride 6152 -> generic path
-    X_un_copy = X_un.contiguous()  # same values, aligned -> fast path
-    a_gen = cr.convrot_quantize_act(X_un, 256, "h4")
-    a_fast = cr.convrot_quantize_act(X_un_copy, 256, "h4")
-    torch.cuda.synchronize()
-    assert torch.equal(a_gen.q, a_fast.q)
-    assert torch.equal(a_gen.scale, a_fast.scale)
-    assert torch.equal(a_gen.q_f16, a_fast.q_f16)
-    del X_al
+    """Outputs at a 16- but not 32-byte aligned address make the library take
+    the generic kernel; both kernels run the same fp32 operations in the same
+    order, so codes, scales and fp16 copies are equal bit for bit."""
+    for G in (16, 64, 256, 1024):
+        wl = WL.make_case(40, 4096, [], seed=11 + G, group=G)
+        X = wl.X.cuda()
+        M, K = X.shape
+        fast = cr.convrot_quantize_act(X, G, "h4")
+        qbuf = torch.empty(M * K + 16, dtype=torch.int8, device="cuda")
+        hbuf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
+        q_un = qbuf[16:].view(M, K)
+        h_un = hbuf[8:].view(M, K)
+        assert q_un.data_ptr() % 32 == 16 and h_un.data_ptr() % 32 == 16
+        out = cr.PackedAct(q_un, torch.empty(M, dtype=torch.float32, device="cuda"), h_un, G, 0)
+        gen = cr.convrot_quantize_act(X, G, "h4", out=out)
+        torch.cuda.synchronize()
+        assert torch.equal(gen.q, fast.q), G
+        assert torch.equal(gen.scale, fast.scale), G
+        assert torch.equal(gen.q_f16, fast.q_f16), G
 
 
 def test_without_f16_copy(cr):
