@@ -246,9 +246,14 @@ def gpu_main(args, world, rank, local):
     torch.cuda.synchronize()
     assert cr.convrot_get_device_status() == 0
     if args.profile:
-        # one more step and nothing else: a short, fixed launch list for ncu
+        # a short, fixed launch list for ncu: one more step, then one int8-only
+        # rotate+quantize and (where supported) one matmul-form rotate+quantize
         e_mid = torch.cuda.Event(enable_timing=True)
         step()
+        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
+        if wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
+                and K // max(wl.group, 64) <= 128:
+            cr.convrot_quantize_act_hmatmul(X, wl.group, with_f16=False)
         torch.cuda.synchronize()
         return
 
@@ -284,6 +289,22 @@ def gpu_main(args, world, rank, local):
             q_only_ms.append((b0, b1))
     torch.cuda.synchronize()
     q_only_ms = [b0.elapsed_time(b1) for b0, b1 in q_only_ms]
+    # the same contract with the rotation applied as a dense tensor-core matmul
+    hm_ms = None
+    if wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
+            and K // max(wl.group, 64) <= 128:
+        hm_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            cr.convrot_quantize_act_hmatmul(X, wl.group, with_f16=False)
+            b1.record(stream)
+            if i >= args.warmup:
+                hm_ms.append((b0, b1))
+        torch.cuda.synchronize()
+        hm_ms = [b0.elapsed_time(b1) for b0, b1 in hm_ms]
     step_ms = [e0.elapsed_time(e1) for e0, _, e1 in ev]
     quant_ms = [e0.elapsed_time(em) for e0, em, _ in ev]
     gemm_ms = [em.elapsed_time(e1) for _, em, e1 in ev]
@@ -352,6 +373,11 @@ def gpu_main(args, world, rank, local):
                          "note": "int8 codes + scales only; in the step the kernel also writes the fp16 operand copy",
                          "in_step_us": quant_s * 1e6, "in_step_bytes": q_bytes_f16,
                          "in_step_gbs": q_bytes_f16 / quant_s / 1e9},
+        "rotate_quant_hmatmul": None if hm_ms is None else {
+            "kernel": "hmatmul_kernel", "us": statistics.mean(hm_ms) * 1e3,
+            "gbs": q_bytes / (statistics.mean(hm_ms) / 1e3) / 1e9,
+            "frac": q_bytes / (statistics.mean(hm_ms) / 1e3) / 1e9 / pk["hbm_gbs"],
+            "tensor_tflops": 2.0 * M * K * max(wl.group, 64) / (statistics.mean(hm_ms) / 1e3) / 1e12},
         "gemm_us": gemm_s * 1e6,
         "gpu_launches": 2 * args.steps * len(ws) // len(ws),
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": 2 * M * K,

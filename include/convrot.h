@@ -135,7 +135,8 @@ convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t
  * and per-channel int8 safetensors", section "The rotation": the rotation
  * applied as one matmul against a shared constant), then quantized as above.
  * Same arguments and results (up to fp32 rounding) as convrot_quantize_act;
- * CONVROT_T_REGULAR_H4 with G in {16, 64, 256} only. Kept for comparison. */
+ * CONVROT_T_REGULAR_H4 with G in {16, 64, 256} only, X dense (ldx == K),
+ * K / max(G, 64) <= 128, Qx and Qx_f16 32-byte aligned. Kept for comparison. */
 convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K, int64_t ldx,
                                             int32_t group, int8_t* Qx, float* sx,
                                             uint16_t* Qx_f16, cudaStream_t stream);

@@ -17,6 +17,7 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
                             cudaStream_t st, int* path);
 cudaError_t hmatmul_launch(const void* X, long long M, int K, long long ldx, int G, int8_t* Q, float* S,
                            uint16_t* Q16, cudaStream_t st);
+bool hmatmul_supported(long long K, long long ldx, int G);
 cudaError_t gemm_mma_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                             bool raw, cudaStream_t st);
 cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
@@ -246,8 +247,10 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
   if (M == 0) return ok();
   if (!X || !Qx || !sx) return fail(CONVROT_ERR_INVALID_ARG, "X, Qx and sx must be non-null");
   if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
-  if (!aligned(X, 16) || ldx % 8 || !aligned(Qx, 16) || !aligned(sx, 4) || (Qx_f16 && !aligned(Qx_f16, 16)))
-    return fail(CONVROT_ERR_ALIGNMENT, "X, Qx, Qx_f16 must be 16-byte aligned and ldx a multiple of 8");
+  if (!aligned(X, 16) || ldx % 8 || !aligned(Qx, 32) || !aligned(sx, 4) || (Qx_f16 && !aligned(Qx_f16, 32)))
+    return fail(CONVROT_ERR_ALIGNMENT, "X must be 16-byte aligned, Qx and Qx_f16 32-byte aligned, ldx a multiple of 8");
+  if (!hmatmul_supported(K, ldx, group))
+    return fail(CONVROT_ERR_INVALID_ARG, "the matmul variant needs dense X (ldx == K) and K / max(G, 64) <= 128");
   cudaError_t e = hmatmul_launch(X, M, static_cast<int>(K), ldx, group, Qx, sx, Qx_f16, stream);
   if (e != cudaSuccess) return cuda_fail(e, "matmul rotate/quantize launch");
   return ok();
@@ -303,7 +306,8 @@ convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packe
 convrot_status convrot_get_device_status(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  int words[4] = {status_word_rotquant(), status_word_gemm_mma(), status_word_gemm_tc(), status_word_api()};
+  int words[5] = {status_word_rotquant(), status_word_gemm_mma(), status_word_gemm_tc(), status_word_hmatmul(),
+                  status_word_api()};
   for (int w : words) {
     if (w != 0) {
       return fail(static_cast<convrot_status>(w), "a kernel recorded status %d (%s)", w,

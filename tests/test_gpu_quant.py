@@ -166,3 +166,36 @@ def test_full_size_sampled_rows(cr, name):
     Q, s, v = _oracle_act(Xs, wl.group, "h4")
     check_codes(to_np(a.q)[rows], Q, v, name)
     check_scales(to_np(a.scale)[rows], s, name)
+
+
+@pytest.mark.parametrize("M,K,G", [(64, 256, 256), (37, 6144, 256), (130, 3072, 256), (33, 4096, 64),
+                                   (45, 2688, 64), (20, 2048, 16), (3, 64, 16)])
+def test_hmatmul_variant_matches_oracle(cr, M, K, G):
+    """The rotation applied as a dense tensor-core matmul gives the same
+    codes as the oracle (within the code tolerance) and the same scales."""
+    wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.001, outlier_scale=50.0, group=G, seed=M + K + G)
+    X = wl.X.cuda()
+    a = cr.convrot_quantize_act_hmatmul(X, G)
+    torch.cuda.synchronize()
+    Q, s, v = _oracle_act(wl.X, G, "h4")
+    check_codes(to_np(a.q), Q, v, f"hmatmul M{M} K{K} G{G}")
+    check_scales(to_np(a.scale), s, f"hmatmul M{M} K{K} G{G}")
+    assert torch.equal(a.q_f16.float(), a.q.float())
+    # against the butterfly kernel: at most one code apart, rarely
+    b = cr.convrot_quantize_act(X, G, "h4")
+    d = (a.q.int() - b.q.int()).abs()
+    assert int(d.max()) <= 1 and int((d > 0).sum()) <= max(1, int(1e-4 * d.numel()))
+
+
+def test_hmatmul_zero_rows_and_rejections(cr):
+    X = torch.zeros((5, 1024), dtype=torch.bfloat16, device="cuda")
+    X[2, 7] = 3.0
+    a = cr.convrot_quantize_act_hmatmul(X, 256)
+    torch.cuda.synchronize()
+    assert float(a.scale[0]) == 0.0 and torch.all(a.q[0] == 0)
+    assert torch.all(a.q[2, :256].abs() == 127)
+    with pytest.raises(cr.ConvRotError):
+        cr.convrot_quantize_act_hmatmul(X, 1024)            # G outside {16, 64, 256}
+    with pytest.raises(cr.ConvRotError):
+        big = torch.zeros((2, 16 * 1024 + 64 * 0), dtype=torch.bfloat16, device="cuda")
+        cr.convrot_quantize_act_hmatmul(big, 64)            # K / 64 > 128
