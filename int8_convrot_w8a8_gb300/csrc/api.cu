@@ -32,6 +32,7 @@ std::mutex g_cache_mu;
 std::map<std::pair<const void*, int>, int> g_smem_set;                 // (kernel, device) -> bytes
 std::map<std::tuple<const void*, int, int, int>, int> g_occupancy;     // (kernel, device, threads, smem)
 std::map<int, int> g_sms;                                              // device -> SM count
+std::map<std::tuple<const void*, int, int, int>, int> g_clusters;      // (kernel, device, smem, cluster)
 }  // namespace
 
 cudaError_t set_smem_limit(const void* kernel, int bytes) {
@@ -59,6 +60,33 @@ cudaError_t blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* 
   }
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kernel, threads, smem_bytes);
   if (e == cudaSuccess) g_occupancy[key] = *out;
+  return e;
+}
+
+cudaError_t max_active_clusters(const void* kernel, int threads, int smem_bytes, int cluster, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto key = std::make_tuple(kernel, dev, smem_bytes, cluster * 4096 + threads);
+  auto it = g_clusters.find(key);
+  if (it != g_clusters.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaOccupancyMaxActiveClusters(out, kernel, &cfg);
+  if (e == cudaSuccess) g_clusters[key] = *out;
   return e;
 }
 

@@ -39,6 +39,8 @@ int status_word_rotquant();
 cudaError_t set_smem_limit(const void* kernel, int bytes);
 cudaError_t blocks_per_sm(const void* kernel, int threads, int smem_bytes, int* out);
 int device_sm_count();
+// Clusters of `cluster` CTAs of this kernel that can be resident at once.
+cudaError_t max_active_clusters(const void* kernel, int threads, int smem_bytes, int cluster, int* out);
 
 // The driver's cuTensorMapEncodeTiled, looked up once per process through
 // the runtime (no link-time dependency on libcuda); nullptr if unavailable.

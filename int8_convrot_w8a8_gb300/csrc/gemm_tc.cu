@@ -82,7 +82,7 @@ struct TcParams {
   int K;
   int m_tiles;
   int n_tiles;
-  int num_tiles;
+  int num_tiles;   // cluster tiles: (m tiles / cluster size, rounded up) x n tiles
   long long spin_limit;
 };
 
@@ -103,23 +103,28 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
   record_status(CONVROT_ERR_TIMEOUT);
 }
 
-__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& m_blk, int& n_glob, int& li,
+// Cluster tile t -> (m block of this CTA, n tile). The CL CTAs of a cluster
+// take CL adjacent m blocks of the same n tile (they share its B tile).
+template <int CL>
+__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int rank, int& m_blk, int& n_glob, int& li,
                                             int& n_local) {
+  const int m_pairs = (p.m_tiles + CL - 1) / CL;
   const int per_group = GROUP_M * p.n_tiles;
   const int g = t / per_group;
   const int first_m = g * GROUP_M;
-  const int gm = min(p.m_tiles - first_m, GROUP_M);
+  const int gm = min(m_pairs - first_m, GROUP_M);
   const int r = t - g * per_group;
-  m_blk = first_m + r % gm;
+  m_blk = (first_m + r % gm) * CL + rank;
   n_glob = r / gm;
   li = 0;
   while (li + 1 < p.outs.count && n_glob >= p.outs.o[li + 1].tile_begin) ++li;
   n_local = n_glob - p.outs.o[li].tile_begin;
 }
 
-template <int BN, bool RAW>
+template <int BN, bool RAW, int CL>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<BN>;
+  static_assert(CL == 1 || CL == 2, "cluster of 1 or 2 CTAs");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -133,11 +138,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / BK;
   const int nch = (nk + KITER_PER_CHUNK - 1) / KITER_PER_CHUNK;
+  const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cluster_id = blockIdx.x / CL, nclusters = gridDim.x / CL;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // released by the MMAs of every CTA that reads it
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -155,6 +162,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
+  // the peer may multicast into this CTA's buffers only after its barriers exist
+  if constexpr (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
@@ -166,9 +175,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       for (int s = 0; s < C::STAGES; ++s) armed_round[s] = -1;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
         int m_blk, n_glob, li, n_local;
-        decode_tile(p, t, m_blk, n_glob, li, n_local);
+        decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % C::STAGES, round = it / C::STAGES;
           if (!wait_or_abort(&empty[s], (round & 1) ^ 1, p.spin_limit, abort_flag)) {
@@ -179,7 +188,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           mbar_expect_tx(&full[s], C::STAGE_BYTES);
           tma_load_2d(sa, &p.tmap_a, kb * BK, m_blk * BM, &full[s]);
-          tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN, &full[s]);
+          if constexpr (CL == 1) {
+            tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN, &full[s]);
+          } else {
+            // this CTA's half of the shared B tile, written into both CTAs
+            tma_load_2d_multicast(sa + C::A_BYTES + rank * (BN / 2) * 128, &p.tmap_b[li], kb * BK,
+                                  n_local * BN + rank * (BN / 2), &full[s], static_cast<uint16_t>((1 << CL) - 1));
+          }
           armed_round[s] = round;
         }
       }
@@ -193,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if (lane == 0) {
       int it = 0, chunk = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
         for (int kb = 0; kb < nk && ok;) {
           const int b = chunk & 1, u = chunk >> 1;
           if (!wait_or_abort(&acc_empty[b], (u & 1) ^ 1, p.spin_limit, abort_flag)) {
@@ -220,7 +235,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
               tc_mma_f16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
                          (kb != kstart || k > 0) ? 1u : 0u);
             }
-            tc_commit(&empty[s]);
+            if constexpr (CL == 1) {
+              tc_commit(&empty[s]);
+            } else {
+              tc_commit_multicast(&empty[s], static_cast<uint16_t>((1 << CL) - 1));
+            }
           }
           if (!ok) break;
           tc_commit(&acc_full[b]);
@@ -239,9 +258,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int col0 = half * C::HALF;
     int chunk = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
       int m_blk, n_glob, li, n_local;
-      decode_tile(p, t, m_blk, n_glob, li, n_local);
+      decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
       int acc[C::HALF];
 #pragma unroll
       for (int j = 0; j < C::HALF; ++j) acc[j] = 0;
@@ -323,6 +342,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA leaves while the other may still write into it
+  if constexpr (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
@@ -344,15 +365,17 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long r
 
 // Column tile: the BN whose last wave wastes the least, by the estimate
 // waves(BN) * BN (a tile's time grows with BN); ties go to the wider tile.
-int choose_bn(long long M, const GemmOutputs& outs, int sms) {
-  const long long mt = (M + BM - 1) / BM;
+// A wave is one cluster tile per resident cluster.
+int choose_bn(long long M, const GemmOutputs& outs, int sms, int cl) {
+  const long long mt = ((M + BM - 1) / BM + cl - 1) / cl;
+  const long long slots = std::max(1, sms / cl);
   int best = 256;
   long long best_cost = -1;
   for (int bn : {256, 192, 128}) {
     long long nt = 0;
     for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + bn - 1) / bn;
     const long long tiles = mt * nt;
-    const long long waves = (tiles + sms - 1) / sms;
+    const long long waves = (tiles + slots - 1) / slots;
     const long long cost = waves * bn;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
@@ -362,7 +385,7 @@ int choose_bn(long long M, const GemmOutputs& outs, int sms) {
   return best;
 }
 
-template <int BN, bool RAW>
+template <int BN, bool RAW, int CL>
 cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K, GemmOutputs outs,
                       cudaStream_t st, int sms) {
   using C = Cfg<BN>;
@@ -373,7 +396,8 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   for (int i = 0; i < outs.count; ++i) {
     outs.o[i].tile_begin = nt;
     nt += (outs.o[i].n + BN - 1) / BN;
-    if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN)) return cudaErrorInvalidValue;
+    // with a cluster, each CTA loads (and multicasts) BN / CL rows of B
+    if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN / CL)) return cudaErrorInvalidValue;
   }
   p.outs = outs;
   p.sx = sx;
@@ -381,16 +405,47 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   p.K = K;
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);
   p.n_tiles = nt;
-  const long long tiles = static_cast<long long>(p.m_tiles) * nt;
+  const long long tiles = static_cast<long long>((p.m_tiles + CL - 1) / CL) * nt;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.num_tiles = static_cast<int>(tiles);
   p.spin_limit = kDefaultSpinLimit;
-  auto kern = gemm_tc_kernel<BN, RAW>;
+  auto kern = gemm_tc_kernel<BN, RAW, CL>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(std::min<long long>(tiles, sms));
-  kern<<<grid, THREADS, C::SMEM, st>>>(p);
-  return cudaGetLastError();
+  if constexpr (CL == 1) {
+    const int grid = static_cast<int>(std::min<long long>(tiles, sms));
+    kern<<<grid, THREADS, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+  } else {
+    int clusters = 0;
+    e = max_active_clusters(reinterpret_cast<const void*>(kern), THREADS, C::SMEM, CL, &clusters);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    const int grid = CL * static_cast<int>(std::min<long long>(tiles, clusters));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+  }
+}
+
+template <bool RAW, int CL>
+cudaError_t launch_cl(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K,
+                      const GemmOutputs& outs, cudaStream_t st, int sms) {
+  switch (choose_bn(M, outs, sms, CL)) {
+    case 256: return launch_bn<256, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
+    case 192: return launch_bn<192, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
+    default: return launch_bn<128, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
+  }
 }
 
 }  // namespace
@@ -403,15 +458,13 @@ cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, i
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const int sms = device_sm_count();
-  const int bn = choose_bn(M, outs, sms);
-  switch (bn) {
-    case 256: return raw ? launch_bn<256, true>(enc, Qx16, sx, M, K, outs, st, sms)
-                         : launch_bn<256, false>(enc, Qx16, sx, M, K, outs, st, sms);
-    case 192: return raw ? launch_bn<192, true>(enc, Qx16, sx, M, K, outs, st, sms)
-                         : launch_bn<192, false>(enc, Qx16, sx, M, K, outs, st, sms);
-    default: return raw ? launch_bn<128, true>(enc, Qx16, sx, M, K, outs, st, sms)
-                        : launch_bn<128, false>(enc, Qx16, sx, M, K, outs, st, sms);
+  // CTA pairs share B tiles when there are at least two row blocks
+  if (M > BM) {
+    return raw ? launch_cl<true, 2>(enc, Qx16, sx, M, K, outs, st, sms)
+               : launch_cl<false, 2>(enc, Qx16, sx, M, K, outs, st, sms);
   }
+  return raw ? launch_cl<true, 1>(enc, Qx16, sx, M, K, outs, st, sms)
+             : launch_cl<false, 1>(enc, Qx16, sx, M, K, outs, st, sms);
 }
 
 }  // namespace convrot
