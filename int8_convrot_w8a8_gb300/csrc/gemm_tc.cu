@@ -57,20 +57,27 @@ constexpr int THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 
-template <int BN>
+// CL = 1: one CTA computes a 128 x BN tile with cta_group::1 MMAs.
+// CL = 2: a cluster pair computes a 256 x BN tile with cta_group::2 MMAs
+// issued by the leader (rank 0); each CTA holds its own 128 A rows and half
+// of the B tile (BN / 2 rows), and receives its 128 x BN half of D in its
+// own tensor memory.
+template <int BN, int CL>
 struct Cfg {
-  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_ROWS = BN / CL;  // rows of B held by one CTA
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
   static constexpr int HALF = BN / 2;  // columns per epilogue thread
+  static_assert(HALF % 16 == 0, "the drain loads 32 or 16 columns at a time");
   // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16
   // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
   // M >> 4 at bit 24.
-  static constexpr uint32_t IDESC = idesc_f16(BM, BN, false);
+  static constexpr uint32_t IDESC = idesc_f16(BM * CL, BN, false);
 };
 
 struct TcParams {
@@ -123,7 +130,7 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int rank, 
 
 template <int BN, bool RAW, int CL>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, CL>;
   static_assert(CL == 1 || CL == 2, "cluster of 1 or 2 CTAs");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,21 +151,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);  // released by the MMAs of every CTA that reads it
+      mbar_init(&empty[s], 1);  // released by the (leader's) MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], NUM_EPI_WARPS);
+      mbar_init(&acc_empty[b], NUM_EPI_WARPS * CL);  // the epilogue warps of every CTA of the pair
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CL == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -186,26 +200,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             break;
           }
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
-          mbar_expect_tx(&full[s], C::STAGE_BYTES);
-          tma_load_2d(sa, &p.tmap_a, kb * BK, m_blk * BM, &full[s]);
           if constexpr (CL == 1) {
+            mbar_expect_tx(&full[s], C::STAGE_BYTES);
+            tma_load_2d(sa, &p.tmap_a, kb * BK, m_blk * BM, &full[s]);
             tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN, &full[s]);
           } else {
-            // this CTA's half of the shared B tile, written into both CTAs
-            tma_load_2d_multicast(sa + C::A_BYTES + rank * (BN / 2) * 128, &p.tmap_b[li], kb * BK,
-                                  n_local * BN + rank * (BN / 2), &full[s], static_cast<uint16_t>((1 << CL) - 1));
+            // both CTAs' bytes complete on the leader's barrier, which the
+            // leader arms for the pair
+            if (rank == 0) mbar_expect_tx(&full[s], CL * C::STAGE_BYTES);
+            const uint32_t lb = mapa_shared(&full[s], 0);
+            tma_load_2d_pair(sa, &p.tmap_a, kb * BK, m_blk * BM, lb);
+            tma_load_2d_pair(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN + rank * C::B_ROWS, lb);
           }
           armed_round[s] = round;
         }
       }
-      // every armed copy must have landed before the CTA may exit
-      for (int s = 0; s < C::STAGES; ++s)
-        if (armed_round[s] >= 0 && !mbar_wait_bounded(&full[s], armed_round[s] & 1, p.spin_limit))
-          raise_abort(abort_flag);
+      // every armed copy must have landed before the CTA may exit (in a pair
+      // the leader's barriers count both CTAs' copies; the closing cluster
+      // barrier holds the peer until the leader has seen them)
+      if (CL == 1 || rank == 0)
+        for (int s = 0; s < C::STAGES; ++s)
+          if (armed_round[s] >= 0 && !mbar_wait_bounded(&full[s], armed_round[s] & 1, p.spin_limit))
+            raise_abort(abort_flag);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && CL == 2 && rank != 0) {
+      // the peer issues nothing; its half of D is complete when the leader's
+      // final commit arrives here
+      if (!mbar_wait_bounded(final_bar, 0, p.spin_limit)) raise_abort(abort_flag);
+    } else if (lane == 0) {
       int it = 0, chunk = 0;
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
@@ -232,22 +256,35 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              tc_mma_f16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
-                         (kb != kstart || k > 0) ? 1u : 0u);
+              if constexpr (CL == 1) {
+                tc_mma_f16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
+                           (kb != kstart || k > 0) ? 1u : 0u);
+              } else {
+                tc_mma_f16_pair(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
+                                (kb != kstart || k > 0) ? 1u : 0u);
+              }
             }
             if constexpr (CL == 1) {
               tc_commit(&empty[s]);
             } else {
-              tc_commit_multicast(&empty[s], static_cast<uint16_t>((1 << CL) - 1));
+              tc_commit_pair_multicast(&empty[s], 3);
             }
           }
           if (!ok) break;
-          tc_commit(&acc_full[b]);
+          if constexpr (CL == 1) {
+            tc_commit(&acc_full[b]);
+          } else {
+            tc_commit_pair_multicast(&acc_full[b], 3);
+          }
           ++chunk;
         }
       }
       // all issued MMAs complete before the tensor memory is released
-      tc_commit(final_bar);
+      if constexpr (CL == 1) {
+        tc_commit(final_bar);
+      } else {
+        tc_commit_pair_multicast(final_bar, 3);
+      }
       if (!mbar_wait_bounded(final_bar, 0, p.spin_limit)) raise_abort(abort_flag);
     }
   } else {
@@ -284,9 +321,23 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[j * 32 + e] += __float2int_rz(__uint_as_float(r[e]));
         }
+        if constexpr (C::HALF % 32 == 16) {  // e.g. BN = 224: 112 columns = 3 x 32 + 16
+          constexpr int j0 = C::HALF - 16;
+          uint32_t r[16];
+          tc_ld_32x32b_x16(taddr + j0, r);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[j0 + e] += __float2int_rz(__uint_as_float(r[e]));
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        if (lane == 0) {
+          if (CL == 1 || rank == 0) {
+            mbar_arrive(&acc_empty[b]);
+          } else {
+            mbar_arrive_cluster(mapa_shared(&acc_empty[b], 0));  // the leader reuses the buffer
+          }
+        }
       }
       if (!ok) break;
 
@@ -346,7 +397,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if constexpr (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    if constexpr (CL == 1) {
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    } else {
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
   }
 }
 
@@ -363,21 +418,32 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long r
 }
 
 
-// Column tile: the BN whose last wave wastes the least, by the estimate
-// waves(BN) * BN (a tile's time grows with BN); ties go to the wider tile.
-// A wave is one cluster tile per resident cluster.
+// Column tile width. One MMA reads 4 KB of A per SM whatever N is, plus
+// N * 16 bytes of B, while it does 128 * N * 32 flops per SM; at ~64 bytes of
+// operand reads per cycle and 8192 flops per cycle the cycles per MMA are
+// max(N / 2, (4096 + 16 N) / 64), so narrow tiles run the tensor cores below
+// peak (measured on GB300, 2-SM MMA: N = 256 / 192 / 128 reach 0.85 / 0.71 /
+// 0.50 of the bf16 peak on the same shapes; 128 is therefore not offered).
+// The choice minimizes
+// waves x (time of one tile), a wave being one tile per resident cluster.
+double mma_cycles_per_column(int bn) {
+  const double compute = bn / 2.0;
+  const double operands = (4096.0 + 16.0 * bn) / 64.0;
+  return std::max(compute, operands) / bn;
+}
+
 int choose_bn(long long M, const GemmOutputs& outs, int sms, int cl) {
   const long long mt = ((M + BM - 1) / BM + cl - 1) / cl;
   const long long slots = std::max(1, sms / cl);
   int best = 256;
-  long long best_cost = -1;
-  for (int bn : {256, 192, 128}) {
+  double best_cost = -1.0;
+  for (int bn : {256, 224, 192}) {
     long long nt = 0;
     for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + bn - 1) / bn;
     const long long tiles = mt * nt;
     const long long waves = (tiles + slots - 1) / slots;
-    const long long cost = waves * bn;
-    if (best_cost < 0 || cost < best_cost) {
+    const double cost = static_cast<double>(waves) * bn * mma_cycles_per_column(bn);
+    if (best_cost < 0 || cost < best_cost * 0.999) {
       best_cost = cost;
       best = bn;
     }
@@ -388,7 +454,7 @@ int choose_bn(long long M, const GemmOutputs& outs, int sms, int cl) {
 template <int BN, bool RAW, int CL>
 cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K, GemmOutputs outs,
                       cudaStream_t st, int sms) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, CL>;
   TcParams p;
   memset(&p, 0, sizeof(p));
   if (!make_map(enc, &p.tmap_a, Qx16, M, K, BM)) return cudaErrorInvalidValue;
@@ -396,7 +462,7 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   for (int i = 0; i < outs.count; ++i) {
     outs.o[i].tile_begin = nt;
     nt += (outs.o[i].n + BN - 1) / BN;
-    // with a cluster, each CTA loads (and multicasts) BN / CL rows of B
+    // in a pair each CTA loads its BN / 2 rows of the B tile
     if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN / CL)) return cudaErrorInvalidValue;
   }
   p.outs = outs;
@@ -443,8 +509,8 @@ cudaError_t launch_cl(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
                       const GemmOutputs& outs, cudaStream_t st, int sms) {
   switch (choose_bn(M, outs, sms, CL)) {
     case 256: return launch_bn<256, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
-    case 192: return launch_bn<192, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
-    default: return launch_bn<128, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
+    case 224: return launch_bn<224, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
+    default: return launch_bn<192, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
   }
 }
 
@@ -458,7 +524,7 @@ cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, i
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const int sms = device_sm_count();
-  // CTA pairs share B tiles when there are at least two row blocks
+  // CTA pairs run the 2-SM MMA when there are at least two row blocks
   if (M > BM) {
     return raw ? launch_cl<true, 2>(enc, Qx16, sx, M, K, outs, st, sms)
                : launch_cl<false, 2>(enc, Qx16, sx, M, K, outs, st, sms);

@@ -205,3 +205,18 @@ def test_full_size_sampled_outputs(cr, name):
         Qw_or, sw_or, _ = O.prepare_weights(W64, wl.group, "h4")
         ref = O.reconstruct(O.int_gemm(Qx_or, Qw_or), sx_or, sw_or, b.numpy()[cols])
         check_y_e2e(Ys_np, ref, f"{name}[{i}] e2e")
+
+
+@pytest.mark.parametrize("M,N", [(1024, 4608), (4096, 4096), (300, 2688)])
+def test_every_column_tile_width_is_exact(cr, M, N):
+    """Shapes on which the library's tile chooser picks each of its column
+    widths on the pair (2-SM) path (256, 224 and 192 columns respectively);
+    the raw accumulators must be bit-exact against the oracle."""
+    rng = np.random.default_rng(M + N)
+    K = 1024
+    Qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", True, "act")
+    w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", True, "w")
+    A = to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64)
+    assert np.array_equal(A, O.int_gemm(Qx, Qw))
