@@ -145,7 +145,7 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
  * quantization", reconstruction).
  *   a, w    host pointers to descriptors of device data; a->K == w->K and
  *           the group/transform of both must match.
- *   bias    device fp32 [N] or NULL.
+ *   bias    device fp32 [N] or NULL, 16-byte aligned (as must be w->scale).
  *   Y       device bf16 [M, N], row stride ldy >= N (multiple of 8, 16-byte aligned).
  * The tensor-core path is used when both a->q_f16 and w->q_f16 are given and
  * K is a multiple of 64; otherwise the int8 warp-MMA path. */

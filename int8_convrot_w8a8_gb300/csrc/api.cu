@@ -188,7 +188,8 @@ convrot_status check_pair(const convrot_packed_act* a, const convrot_packed_weig
   if (!aligned(a->q, 16) || !aligned(w->q, 16) || (a->q_f16 && !aligned(a->q_f16, 16)) ||
       (w->q_f16 && !aligned(w->q_f16, 16)))
     return fail(CONVROT_ERR_ALIGNMENT, "operand pointers must be 16-byte aligned");
-  if (!aligned(a->scale, 4) || !aligned(w->scale, 4)) return fail(CONVROT_ERR_ALIGNMENT, "scale pointers must be 4-byte aligned");
+  if (!aligned(a->scale, 4) || !aligned(w->scale, 16))
+    return fail(CONVROT_ERR_ALIGNMENT, "activation scales must be 4-byte and weight scales 16-byte aligned");
   return CONVROT_OK;
 }
 
@@ -291,7 +292,7 @@ convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_
   if (a->M > 0 && !Y) return fail(CONVROT_ERR_INVALID_ARG, "Y is null");
   if (ldy < w->N) return fail(CONVROT_ERR_INVALID_ARG, "ldy=%lld < N=%lld", static_cast<long long>(ldy), static_cast<long long>(w->N));
   if ((a->M > 0 && !aligned(Y, 16)) || ldy % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y must be 16-byte aligned and ldy a multiple of 8");
-  if (bias && !aligned(bias, 4)) return fail(CONVROT_ERR_ALIGNMENT, "bias must be 4-byte aligned");
+  if (bias && !aligned(bias, 16)) return fail(CONVROT_ERR_ALIGNMENT, "bias must be 16-byte aligned");
   GemmOutputs outs{};
   outs.count = 1;
   outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, bias, Y, ldy, static_cast<int>(w->N), 0};
@@ -312,7 +313,7 @@ convrot_status convrot_linear_multi(const convrot_packed_act* a, int32_t n, cons
     if (a->M > 0 && !Y[i]) return fail(CONVROT_ERR_INVALID_ARG, "Y[%d] is null", i);
     if (ldy[i] < w[i].N) return fail(CONVROT_ERR_INVALID_ARG, "ldy[%d] < N", i);
     if (!aligned(Y[i], 16) || ldy[i] % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y[%d] alignment", i);
-    if (b && !aligned(b, 4)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] alignment", i);
+    if (b && !aligned(b, 16)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] must be 16-byte aligned", i);
     outs.o[i] = GemmOut{w[i].q, w[i].q_f16, w[i].scale, b, Y[i], ldy[i], static_cast<int>(w[i].N), 0};
   }
   return run_gemm(a, outs, false, stream);

@@ -365,13 +365,22 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           for (int j = 0; j < C::HALF; j += 8) {
             const int n = nb + j;
             if (n + 8 <= o.n) {
+              // 8 scales and 8 biases in 16-byte loads (n is a multiple of 8)
+              float swv[8], bv[8];
+              *reinterpret_cast<float4*>(swv) = __ldg(reinterpret_cast<const float4*>(o.sw + n));
+              *reinterpret_cast<float4*>(swv + 4) = __ldg(reinterpret_cast<const float4*>(o.sw + n + 4));
+              if (o.bias) {
+                *reinterpret_cast<float4*>(bv) = __ldg(reinterpret_cast<const float4*>(o.bias + n));
+                *reinterpret_cast<float4*>(bv + 4) = __ldg(reinterpret_cast<const float4*>(o.bias + n + 4));
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) bv[e] = 0.0f;
+              }
               uint32_t w[4];
 #pragma unroll
               for (int e = 0; e < 8; e += 2) {
-                const float b0 = o.bias ? __ldg(o.bias + n + e) : 0.0f;
-                const float b1 = o.bias ? __ldg(o.bias + n + e + 1) : 0.0f;
-                const float y0 = fmaf(static_cast<float>(acc[j + e]), srow * __ldg(o.sw + n + e), b0);
-                const float y1 = fmaf(static_cast<float>(acc[j + e + 1]), srow * __ldg(o.sw + n + e + 1), b1);
+                const float y0 = fmaf(static_cast<float>(acc[j + e]), srow * swv[e], bv[e]);
+                const float y1 = fmaf(static_cast<float>(acc[j + e + 1]), srow * swv[e + 1], bv[e + 1]);
                 const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
                 w[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
               }
