@@ -259,15 +259,18 @@ def gpu_main(args, world, rank, local):
 
     barrier(world)
     torch.cuda.synchronize()
+    host_us = []
     with ClockSampler(local) as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
             torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
             e0, e_mid, e1 = ev[i]
+            h0 = time.perf_counter()
             e0.record(stream)
             step()
             e1.record(stream)
+            host_us.append(1e6 * (time.perf_counter() - h0))
         torch.cuda.synchronize()
         wall1 = time.perf_counter()
     barrier(world)
@@ -453,15 +456,18 @@ def gpu_main(args, world, rank, local):
 
     barrier(world)
     torch.cuda.synchronize()
+    host_us = []
     with ClockSampler(local) as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
             torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
             e0, e_mid, e1 = ev[i]
+            h0 = time.perf_counter()
             e0.record(stream)
             step()
             e1.record(stream)
+            host_us.append(1e6 * (time.perf_counter() - h0))
         torch.cuda.synchronize()
         wall1 = time.perf_counter()
     barrier(world)
@@ -579,6 +585,7 @@ def gpu_main(args, world, rank, local):
                 "pipelining": "2 streams, copies of one step overlap kernels of the next"},
         "clocks": clocks.summary(),
         "wall_s_timed": wall1 - wall0,
+        "host_us_per_step": statistics.median(host_us),
     }
     if world == 1 and not args.no_cpu_baseline:
         # about 10 s of oracle work: seeded row samples of the same workload

@@ -147,8 +147,9 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
  *           the group/transform of both must match.
  *   bias    device fp32 [N] or NULL, 16-byte aligned (as must be w->scale).
  *   Y       device bf16 [M, N], row stride ldy >= N (multiple of 8, 16-byte aligned).
- * The tensor-core path is used when both a->q_f16 and w->q_f16 are given and
- * K is a multiple of 64; otherwise the int8 warp-MMA path. */
+ * Paths: M <= 64 streams the int8 weights (warp-level int8 MMA); larger M
+ * uses the tcgen05 tensor-core path when both a->q_f16 and w->q_f16 are given
+ * and K is a multiple of 64, otherwise the int8 warp-MMA path. */
 convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_weight* w,
                               const float* bias, uint16_t* Y, int64_t ldy, cudaStream_t stream);
 

@@ -51,6 +51,7 @@ EncodeTiledFn tensor_map_encoder();
 int status_word_gemm_mma();
 int status_word_gemm_tc();
 int status_word_hmatmul();
+int status_word_gemm_small();
 
 // Spin limit of every bounded device-side wait (iterations of a try_wait
 // loop with nanosleep back-off); about a second on a GB300.

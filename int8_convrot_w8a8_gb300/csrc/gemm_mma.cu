@@ -6,10 +6,9 @@
 // ("INT8 Convrot Safetensors", "Runtime activation quantization": the int32
 // accumulation and the reconstruction Y = A * s_x * s_w + b.)
 //
-// This path reads the int8 operands directly. It serves small M, where the
-// linear is a weight stream bound by HBM (the whole weight matrix passes
-// through once and every byte feeds M rows), and any shape for which no
-// fp16 operand copies were provided. Operands are K-contiguous ("TN"); tiles
+// This path reads the int8 operands directly. It serves any shape with more
+// than 64 rows for which no fp16 operand copies were provided (fewer rows go
+// to the weight-stream kernel in gemm_small.cu). Operands are K-contiguous ("TN"); tiles
 // of BK = 128 bytes of K are staged by cp.async in a multi-stage ring, rows
 // XOR-swizzled by 16-byte chunk, and fed to the MMAs with ldmatrix.
 #include <algorithm>
@@ -216,16 +215,6 @@ cudaError_t launch_cfg(const int8_t* Qx, const float* sx, long long M, int K, Ge
 cudaError_t gemm_mma_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                             bool raw, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  // Small M: one m-tile, narrow N tiles so the weight stream spreads over
-  // every SM. Otherwise a 128 x 128 tile.
-  if (M <= 16) {
-    return raw ? launch_cfg<16, 64, 16, 16, 4, true>(Qx, sx, M, K, outs, st)
-               : launch_cfg<16, 64, 16, 16, 4, false>(Qx, sx, M, K, outs, st);
-  }
-  if (M <= 64) {
-    return raw ? launch_cfg<64, 64, 32, 16, 4, true>(Qx, sx, M, K, outs, st)
-               : launch_cfg<64, 64, 32, 16, 4, false>(Qx, sx, M, K, outs, st);
-  }
   return raw ? launch_cfg<128, 128, 64, 32, 3, true>(Qx, sx, M, K, outs, st)
              : launch_cfg<128, 128, 64, 32, 3, false>(Qx, sx, M, K, outs, st);
 }

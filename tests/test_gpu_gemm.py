@@ -44,7 +44,8 @@ def oracle_case(wl, i=0):
 
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M,N,K", [(64, 256, 256), (200, 384, 1024), (129, 300, 3072), (16, 1000, 1152),
-                                   (1, 64, 256), (300, 128, 6144), (257, 136, 2688)])
+                                   (1, 64, 256), (300, 128, 6144), (257, 136, 2688), (3, 40, 80),
+                                   (33, 100, 1040), (48, 13824, 1152), (16, 96, 6144)])
 def test_gemm_s32_bit_exact_on_oracle_codes(cr, path, M, N, K):
     rng = np.random.default_rng(M + N + K)
     Qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
@@ -220,3 +221,16 @@ def test_every_column_tile_width_is_exact(cr, M, N):
     w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", True, "w")
     A = to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64)
     assert np.array_equal(A, O.int_gemm(Qx, Qw))
+
+
+def test_small_m_multi_equals_separate_calls(cr):
+    """The gated-FFN pair at M = 16 (weight-stream path): one launch for both
+    linears gives exactly what two separate linears give."""
+    wl = WL.ffn_pair()
+    sg = wl.signs.cuda()
+    a = cr.convrot_quantize_act(wl.X.cuda(), wl.group, wl.transform, sg, with_f16=False)
+    ws = [cr.convrot_prepare_weights(W.cuda(), wl.group, wl.transform, sg, with_f16=False) for W in wl.weights]
+    bs = [b.cuda() for b in wl.biases]
+    Ys = cr.convrot_linear_multi(a, ws, bs)
+    for Y, w, b in zip(Ys, ws, bs):
+        assert torch.equal(Y, cr.convrot_linear(a, w, b))
