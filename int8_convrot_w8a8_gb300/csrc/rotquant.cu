@@ -136,14 +136,17 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
 //    registers as 32 fp32 pairs from load to store.
 //  In-lane digits: the radix-4 stages of the three low digits (d0 scalar,
 //    d1 and d2 on packed fp32x2 pairs of adjacent elements).
-//  Cross-lane digits (G = 256: one, G = 1024: two): the lanes that share a
-//    group exchange values with two shuffles per element, u = x + x[a^1],
-//    w = x - x[a^1], y = u + w[a^2], which is the same operation sequence,
-//    bit for bit, as the in-register stage.
+//  Digit 3 (G >= 256): the four lines of a group belong to the four lanes
+//    of a quad; one fp32 transpose through shared memory inside the quad
+//    (swizzled, conflict-free) turns the line index into a register index,
+//    so the stage runs in registers on packed pairs.
+//  Digit 4 (G = 1024): across the quads of a group with two shuffles per
+//    element, u = x + x[a^1], w = x - x[a^1], y = u + w[a^2], which is the
+//    same operation sequence, bit for bit, as the in-register stage.
 //  Row absmax: warp reduction (one instruction when the warp lies in one
 //    row), one shared-memory atomicMax per warp and row, one barrier.
-//  Quantize straight from registers: the 64 int8 codes leave as two 32-byte
-//    stores, the fp16 copies as four, each a whole 32-byte sector.
+//  Quantize straight from registers: codes leave as 32-byte stores (16-byte
+//    after the quad transpose), fp16 copies as 32-byte stores: whole sectors.
 
 template <int G>
 struct LaneCfg {
@@ -172,13 +175,14 @@ template <int G>
 __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CUtensorMap xmap, long long M, int K,
                                                        int R, int NT, int8_t* __restrict__ Q, float* __restrict__ S,
                                                        __half* __restrict__ Q16, float s_div, int stage_bytes,
-                                                       long long spin_limit) {
+                                                       int tbytes, long long spin_limit) {
   using C = LaneCfg<G>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_base = smem_u32(smem);
-  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + 2 * stage_bytes);  // [3][R]
+  const uint32_t tbuf = stage_base + 2 * stage_bytes;  // fp32 quad-transpose buffer (G >= 256)
+  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + 2 * stage_bytes + tbytes);  // [3][R]
   uint64_t* bar = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));         // [2]
 
   const int tid = threadIdx.x, lane = tid & 31;
@@ -191,6 +195,26 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   // whether this warp's active lanes all belong to one row
   const int row_first = __shfl_sync(0xffffffffu, my_row, 0);
   const bool warp_one_row = __all_sync(0xffffffffu, my_row == row_first);
+
+  // Quad transpose (G >= 256): the 4 lanes of a quad own the 4 lines of a
+  // group. Each writes its line (fp32, 16 chunks of 16 bytes) and reads back
+  // the 16-element run at offset 16a (a = lane & 3) of all 4 lines, so the
+  // group's digit 3 (the line) becomes a register index. Chunk c of line l
+  // sits at chunk c ^ (bitrev3(l mod 8) ^ ((c >> 3) << 1)) of its 256-byte
+  // slot: conflict-free for the line writes and for the transposed reads.
+  const int qa = tid & 3;
+  uint32_t t_wr = 0;      // write base, XOR-ed with the compile-time part of the swizzle
+  uint32_t t_rd[4] = {};  // read base of line (tid & ~3) + r, XOR-ed likewise
+  if constexpr (C::NX >= 1) {
+    auto bitrev3 = [](int x) { return ((x & 1) << 2) | (x & 2) | ((x >> 2) & 1); };
+    t_wr = (tbuf + (static_cast<uint32_t>(tid) << 8)) | (static_cast<uint32_t>(bitrev3(tid & 7)) << 4);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int l = (tid & ~3) + r;
+      const int tr = (4 * qa) ^ bitrev3(l & 7) ^ ((qa >> 1) << 1);
+      t_rd[r] = (tbuf + (static_cast<uint32_t>(l) << 8)) | (static_cast<uint32_t>(tr) << 4);
+    }
+  }
 
   if (tid == 0) {
     mbar_init(&bar[0], 1);
@@ -256,11 +280,33 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
 #pragma unroll
       for (int o = 0; o < 8; ++o) h4_stage(v[o], v[o + 8], v[o + 16], v[o + 24]);
     }
-    // ---- cross-lane digits: lane bits 0-1 hold digit 3, bits 2-3 digit 4
+    // ---- digit 3 through the quad transpose, then in registers: after it
+    // v[8r + i] holds elements 16a + 2i, +1 of line (tid & ~3) + r
     if constexpr (C::NX >= 1) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = h4_xlane<0>(v[i]);
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t addr = t_wr ^ (static_cast<uint32_t>(k ^ ((k >> 3) << 1)) << 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(v[2 * k].x), "f"(v[2 * k].y),
+                     "f"(v[2 * k + 1].x), "f"(v[2 * k + 1].y)
+                     : "memory");
+      }
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float4 f;
+          asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                       : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                       : "r"(t_rd[r] ^ (static_cast<uint32_t>(c) << 4))
+                       : "memory");
+          v[8 * r + 2 * c] = make_float2(f.x, f.y);
+          v[8 * r + 2 * c + 1] = make_float2(f.z, f.w);
+        }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h4_stage(v[i], v[8 + i], v[16 + i], v[24 + i]);
     }
+    // ---- digit 4 (G = 1024): across the 4 quads of a group, lane bits 2-3
     if constexpr (C::NX >= 2) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = h4_xlane<2>(v[i]);
@@ -286,36 +332,69 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
       const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
       const float2 inv2 = make_float2(inv, inv);
       const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
-      const long long e0 = (tile * R) * static_cast<long long>(K) + (static_cast<long long>(tid) << 6);
-      if (e0 < total_elems) {
+      const long long tile_e = (tile * R) * static_cast<long long>(K);
+      // 16 values -> 16 codes (one 16-byte store) and 16 fp16 copies (one 32-byte store)
+      auto emit16 = [&](int p0, long long e) {
+        uint32_t words[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t words[8];
+        for (int k = 0; k < 4; ++k) {
+          const float2 t01 = f2_fma(v[p0 + 2 * k], inv2, mg2);
+          const float2 t23 = f2_fma(v[p0 + 2 * k + 1], inv2, mg2);
+          const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
+          const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
+          words[k] = __byte_perm(b01, b23, 0x5410);
+          if (Q16) {  // reuse the rounded values: code = t - magic, exact in fp16
+            v[p0 + 2 * k] = f2_sub(t01, mg2);
+            v[p0 + 2 * k + 1] = f2_sub(t23, mg2);
+          }
+        }
+        stg_128(Q + e, make_uint4(words[0], words[1], words[2], words[3]));
+        if (Q16) {
+          uint32_t hw[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const float2 t01 = f2_fma(v[16 * h + 2 * k], inv2, mg2);
-            const float2 t23 = f2_fma(v[16 * h + 2 * k + 1], inv2, mg2);
-            const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
-            const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
-            words[k] = __byte_perm(b01, b23, 0x5410);
-            if (Q16) {
-              // reuse the rounded values: code = t - magic, exact in fp16
-              v[16 * h + 2 * k] = f2_sub(t01, mg2);
-              v[16 * h + 2 * k + 1] = f2_sub(t23, mg2);
-            }
+            const __half2 p = __floats2half2_rn(v[p0 + k].x, v[p0 + k].y);
+            hw[k] = *reinterpret_cast<const uint32_t*>(&p);
           }
-          stg_256(Q + e0 + 32 * h, words);
+          stg_256(Q16 + e, hw);
         }
-        if (Q16) {
+      };
+      if (tile_e + (static_cast<long long>(tid) << 6) < total_elems) {
+        if constexpr (C::NX >= 1) {
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            uint32_t hw[8];
+          for (int r = 0; r < 4; ++r)
+            emit16(8 * r, tile_e + (static_cast<long long>((tid & ~3) + r) << 6) + 16 * qa);
+        } else {
+          // the whole line: codes as two 32-byte stores, fp16 copies as four
+          const long long e0 = tile_e + (static_cast<long long>(tid) << 6);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t words[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const __half2 p = __floats2half2_rn(v[8 * h + k].x, v[8 * h + k].y);
-              hw[k] = *reinterpret_cast<const uint32_t*>(&p);
+              const float2 t01 = f2_fma(v[16 * h + 2 * k], inv2, mg2);
+              const float2 t23 = f2_fma(v[16 * h + 2 * k + 1], inv2, mg2);
+              const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
+              const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
+              words[k] = __byte_perm(b01, b23, 0x5410);
+              if (Q16) {
+                v[16 * h + 2 * k] = f2_sub(t01, mg2);
+                v[16 * h + 2 * k + 1] = f2_sub(t23, mg2);
+              }
             }
-            stg_256(Q16 + e0 + 16 * h, hw);
+            stg_256(Q + e0 + 32 * h, words);
+          }
+          if (Q16) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              uint32_t hw[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const __half2 p = __floats2half2_rn(v[8 * h + k].x, v[8 * h + k].y);
+                hw[k] = *reinterpret_cast<const uint32_t*>(&p);
+              }
+              stg_256(Q16 + e0 + 16 * h, hw);
+            }
           }
         }
       }
@@ -385,7 +464,9 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
     return cudaSuccess;
   const int threads = (NT + 31) / 32 * 32;
   const int stage_bytes = ((R * K * 2 + 1023) / 1024) * 1024;
-  const int smem = 1024 + 2 * stage_bytes + ((3 * R + 1) & ~1) * 4 + 2 * 8;
+  // the quad transpose needs 256 bytes per thread (one fp32 line)
+  const int tbytes = LaneCfg<G>::NX >= 1 ? threads * 256 : 0;
+  const int smem = 1024 + 2 * stage_bytes + tbytes + ((3 * R + 1) & ~1) * 4 + 2 * 8;
   auto kern = rq_lane_kernel<G>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
@@ -397,7 +478,7 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, Q, S, Q16,
                                                              scale_divisor(CONVROT_T_REGULAR_H4, G), stage_bytes,
-                                                             kDefaultSpinLimit);
+                                                             tbytes, kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
 }
