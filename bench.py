@@ -6,10 +6,12 @@ fused dequant/bias/bf16 epilogue for every linear that shares the packed
 activation. Weights are prepared once before timing (the offline path).
 
 Timing: W warm-up steps, then K timed steps; each step is bracketed by CUDA
-events on the launching stream, and L2 is flushed between steps (a 256 MiB
-write, outside the events). Clocks are sampled with nvidia-smi during the
-timed region. The e2e figure repeats the step through the public API with
-host buffers: pinned X copied in, Y copied back, inside the timed region.
+events on the launching stream, and L2 is flushed between steps, outside
+the events: a 256 MiB write, then a 256 MiB read, so that the flush's own
+dirty lines are written back before the step starts. Clocks are sampled
+with nvidia-smi during the timed region. The e2e figure repeats the step
+through the public API with host buffers: pinned X copied in, Y copied
+back, inside the timed region.
 
 `--impl reference` times the CPU oracle (fp64 numpy) on a bounded row
 sample of the same workload, on the host cores.
@@ -228,6 +230,14 @@ def gpu_main(args, world, rank, local):
     act = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16)
     outs = [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: the written
+        # lines leave L2 (and reach DRAM) here, not inside the next timed step
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_sink)
 
     def step():
         cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16, out=act)
@@ -240,7 +250,7 @@ def gpu_main(args, world, rank, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         e_mid = torch.cuda.Event(enable_timing=True)
         step()
     torch.cuda.synchronize()
@@ -263,7 +273,7 @@ def gpu_main(args, world, rank, local):
     with ClockSampler(local) as clocks:
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
             e0, e_mid, e1 = ev[i]
             h0 = time.perf_counter()
@@ -282,7 +292,7 @@ def gpu_main(args, world, rank, local):
     act8 = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
     q_only_ms = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2()
         torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
@@ -298,7 +308,7 @@ def gpu_main(args, world, rank, local):
             and K // max(wl.group, 64) <= 128:
         hm_ms = []
         for i in range(args.warmup + args.steps):
-            flush.zero_()
+            flush_l2()
             torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
             b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             b0.record(stream)
@@ -332,7 +342,7 @@ def gpu_main(args, world, rank, local):
     else:
         w_bytes = sum(n * K + 4 * n for n in Ns) + M * K + 4 * M + 2 * M * sum(Ns)
         gbs = w_bytes / gemm_s / 1e9
-        dominant = {"kernel": "gemm_mma_kernel", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+        dominant = {"kernel": "gemm_small_kernel", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
                     "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None,
                     "peak_note": f"{pk['source']} HBM copy bandwidth"}
 
@@ -386,186 +396,13 @@ def gpu_main(args, world, rank, local):
 
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]()
-    rows = args.ref_rows
-    res = []
-    for _ in range(args.warmup):
-        oracle_sample(wl, max(8, rows // 8))
-    for s in range(args.steps):
-        res.append(oracle_sample(wl, rows, seed=s))
-    secs = sum(r["seconds"] for r in res)
-    ops = sum(r["ops"] for r in res)
-    value = ops / secs / 1e12
-    cores = blas_threads()
-    sample = f"{rows} seeded rows of {wl.M} per step (full K={wl.K}, all N={sum(wl.Ns)}), fp64 numpy"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "sample": sample},
-            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-
-
-# --------------------------------------------------------------------- GPU ---
-
-def gpu_main(args, world, rank, local):
-    import int8_convrot_w8a8_gb300 as cr
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    wl = WORKLOADS[args.workload]()
-    stream = torch.cuda.current_stream()
-    sg = None if wl.signs is None else wl.signs.to(dev)
-    use_f16 = wl.M > 64
-    ws = [cr.convrot_prepare_weights(W.to(dev), wl.group, wl.transform, sg, with_f16=use_f16) for W in wl.weights]
-    bs = [b.to(dev) for b in wl.biases]
-    X = wl.X.to(dev)
-    M, K, Ns = wl.M, wl.K, wl.Ns
-    act = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16)
-    outs = [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16, out=act)
-        e_mid.record(stream)
-        if len(ws) == 1:
-            cr.convrot_linear(act, ws[0], bs[0], out=outs[0])
-        else:
-            cr.convrot_linear_multi(act, ws, bs, outs=outs)
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for _ in range(args.warmup):
-        flush.zero_()
-        e_mid = torch.cuda.Event(enable_timing=True)
-        step()
-    torch.cuda.synchronize()
-    assert cr.convrot_get_device_status() == 0
-    if args.profile:
-        # a short, fixed launch list for ncu: one more step, then one int8-only
-        # rotate+quantize and (where supported) one matmul-form rotate+quantize
-        e_mid = torch.cuda.Event(enable_timing=True)
-        step()
-        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
-        if wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
-                and K // max(wl.group, 64) <= 128:
-            cr.convrot_quantize_act_hmatmul(X, wl.group, with_f16=False)
-        torch.cuda.synchronize()
-        return
-
-    barrier(world)
-    torch.cuda.synchronize()
-    host_us = []
-    with ClockSampler(local) as clocks:
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
-            e0, e_mid, e1 = ev[i]
-            h0 = time.perf_counter()
-            e0.record(stream)
-            step()
-            e1.record(stream)
-            host_us.append(1e6 * (time.perf_counter() - h0))
-        torch.cuda.synchronize()
-        wall1 = time.perf_counter()
-    barrier(world)
-    status = cr.convrot_get_device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
-    # the rotate+quantize contract alone (bf16 in, int8 codes + fp32 scales out,
-    # no fp16 operand copy), timed on its own for the GB/s figure
-    act8 = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
-    q_only_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False, out=act8)
-        b1.record(stream)
-        if i >= args.warmup:
-            q_only_ms.append((b0, b1))
-    torch.cuda.synchronize()
-    q_only_ms = [b0.elapsed_time(b1) for b0, b1 in q_only_ms]
-    # the same contract with the rotation applied as a dense tensor-core matmul
-    hm_ms = None
-    if wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
-            and K // max(wl.group, 64) <= 128:
-        hm_ms = []
-        for i in range(args.warmup + args.steps):
-            flush.zero_()
-            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
-            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            b0.record(stream)
-            cr.convrot_quantize_act_hmatmul(X, wl.group, with_f16=False)
-            b1.record(stream)
-            if i >= args.warmup:
-                hm_ms.append((b0, b1))
-        torch.cuda.synchronize()
-        hm_ms = [b0.elapsed_time(b1) for b0, b1 in hm_ms]
-    step_ms = [e0.elapsed_time(e1) for e0, _, e1 in ev]
-    quant_ms = [e0.elapsed_time(em) for e0, em, _ in ev]
-    gemm_ms = [em.elapsed_time(e1) for _, em, e1 in ev]
-    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
-
-    ops_step = 2.0 * M * sum(Ns) * K
-    value = world * ops_step * args.steps / total_s / 1e12
-    pk = peaks()
-    gemm_s = statistics.mean(gemm_ms) / 1e3
-    quant_s = statistics.mean(quant_ms) / 1e3
-    gemm_tflops = ops_step / gemm_s / 1e12
-    # algorithmic bytes of rotate+quantize: bf16 in, int8 out, fp32 scales
-    q_bytes = 2 * M * K + M * K + 4 * M
-    q_bytes_f16 = q_bytes + 2 * M * K if use_f16 else q_bytes
-    quant_only_s = statistics.mean(q_only_ms) / 1e3
-    quant_gbs = q_bytes / quant_only_s / 1e9
-    if use_f16:
-        dominant = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": gemm_tflops,
-                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
-                    "traffic": None,
-                    "peak_note": f"{pk['source']} bf16 dense burst; the fp16 tensor rate is the same (nominal ratio 1)"}
-    else:
-        w_bytes = sum(n * K + 4 * n for n in Ns) + M * K + 4 * M + 2 * M * sum(Ns)
-        gbs = w_bytes / gemm_s / 1e9
-        dominant = {"kernel": "gemm_mma_kernel", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None,
-                    "peak_note": f"{pk['source']} HBM copy bandwidth"}
-
-    # ---- end to end through the public API with host buffers
-    Xh = wl.X.pin_memory()
-    Yh = [torch.empty((M, n), dtype=torch.bfloat16).pin_memory() for n in Ns]
-    Xd = torch.empty_like(X)
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        Xd.copy_(Xh, non_blocking=True)
-        cr.convrot_quantize_act(Xd, wl.group, wl.transform, sg, with_f16=use_f16, out=act)
-        if len(ws) == 1:
-            cr.convrot_linear(act, ws[0], bs[0], out=outs[0])
-        else:
-            cr.convrot_linear_multi(act, ws, bs, outs=outs)
-        for y, yh in zip(outs, Yh):
-            yh.copy_(y, non_blocking=True)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(a0.elapsed_time(a1))
-    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world)
-    e2e_value = world * ops_step * args.steps / e2e_s / 1e12
-
-    if rank != 0:
-        return
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": wl.name, "M": M, "K": K, "N": Ns, "group": wl.group, "transform": wl.transform,
-                   "seed": wl.seed, "l2": "flushed between steps (256 MiB write outside the events)",
-                   "inputs": wl.description, "gemm_path": "tcgen05 fp16-exact" if use_f16 else "mma.sync s8"},
+                   "seed": wl.seed, "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
+                   "inputs": wl.description, "gemm_path": "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)"},
         "roofline": dominant,
         "rotate_quant": {"kernel": "rq_fast_kernel" if wl.transform == "h4" else "rq_generic_kernel",
                          "us": quant_only_s * 1e6, "gbs": quant_gbs, "peak_gbs": pk["hbm_gbs"],

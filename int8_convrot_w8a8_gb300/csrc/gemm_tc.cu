@@ -71,8 +71,10 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
   static constexpr int HALF = BN / 2;  // columns per epilogue thread
+  // per epilogue warp: the column scales and biases of its half tile
+  static constexpr int EPI_BYTES = NUM_EPI_WARPS * HALF * 2 * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + EPI_BYTES + 1024;
   static_assert(HALF % 16 == 0, "the drain loads 32 or 16 columns at a time");
   // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16
   // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
@@ -103,6 +105,17 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, lo
     if (i > 128) __nanosleep(32);
   }
   return false;
+}
+
+// 16-byte global -> shared copy that reads `src_bytes` (0..16) bytes and
+// zero-fills the rest; with src_bytes == 0 nothing is read.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void lds_128(uint32_t addr, float* v) {
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
 }
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag) {
@@ -141,6 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   uint64_t* final_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned char* epi_smem = smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / BK;
@@ -293,11 +307,33 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int half = (warp - 2) >> 2;    // which half of the BN columns
     const int row_in_tile = q * 32 + lane;
     const int col0 = half * C::HALF;
+    // this warp's copy of the half tile's column scales, then biases
+    const uint32_t wsw = smem_u32(epi_smem) + static_cast<uint32_t>((warp - 2) * C::HALF * 2 * 4);
+    const uint32_t wbias = wsw + C::HALF * 4;
     int chunk = 0;
     bool ok = true;
     for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
       int m_blk, n_glob, li, n_local;
       decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
+      const GemmOut& o = p.outs.o[li];
+      const long long m = static_cast<long long>(m_blk) * BM + row_in_tile;
+      const int nb = n_local * BN + col0;
+      float srow = 0.0f;
+      if constexpr (!RAW) {
+        __syncwarp();  // every lane has read the previous tile's values
+        // fetched now, used after the last chunk: the loads overlap the MMAs.
+        // Columns past N read as zero (the warp's previous reads of these
+        // buffers finished before its final stores of the previous tile).
+        if (m < p.M) srow = __ldg(p.sx + m);
+        for (int j = 4 * lane; j < C::HALF; j += 128) {
+          const int n = nb + j;
+          const int bytes = n < o.n ? 4 * min(4, o.n - n) : 0;
+          cp_async_16(wsw + 4 * j, bytes ? static_cast<const void*>(o.sw + n) : static_cast<const void*>(o.sw), bytes);
+          const int bb = o.bias ? bytes : 0;
+          cp_async_16(wbias + 4 * j, bb ? static_cast<const void*>(o.bias + n) : static_cast<const void*>(o.sw), bb);
+        }
+        cp_async_commit();
+      }
       int acc[C::HALF];
 #pragma unroll
       for (int j = 0; j < C::HALF; ++j) acc[j] = 0;
@@ -341,9 +377,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       }
       if (!ok) break;
 
-      const GemmOut& o = p.outs.o[li];
-      const long long m = static_cast<long long>(m_blk) * BM + row_in_tile;
-      const int nb = n_local * BN + col0;
+      if constexpr (!RAW) {
+        cp_async_wait_all();
+        __syncwarp();
+      }
       if (m < p.M) {
         if constexpr (RAW) {
           int* yrow = static_cast<int*>(o.y) + m * o.ldy;
@@ -359,23 +396,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             }
           }
         } else {
-          const float srow = p.sx[m];
           __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(o.y) + m * o.ldy;
 #pragma unroll
           for (int j = 0; j < C::HALF; j += 8) {
             const int n = nb + j;
+            // 8 scales and 8 biases, the same address in every lane (broadcast)
+            float swv[8], bv[8];
+            lds_128(wsw + 4 * j, swv);
+            lds_128(wsw + 4 * j + 16, swv + 4);
+            lds_128(wbias + 4 * j, bv);
+            lds_128(wbias + 4 * j + 16, bv + 4);
             if (n + 8 <= o.n) {
-              // 8 scales and 8 biases in 16-byte loads (n is a multiple of 8)
-              float swv[8], bv[8];
-              *reinterpret_cast<float4*>(swv) = __ldg(reinterpret_cast<const float4*>(o.sw + n));
-              *reinterpret_cast<float4*>(swv + 4) = __ldg(reinterpret_cast<const float4*>(o.sw + n + 4));
-              if (o.bias) {
-                *reinterpret_cast<float4*>(bv) = __ldg(reinterpret_cast<const float4*>(o.bias + n));
-                *reinterpret_cast<float4*>(bv + 4) = __ldg(reinterpret_cast<const float4*>(o.bias + n + 4));
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) bv[e] = 0.0f;
-              }
               uint32_t w[4];
 #pragma unroll
               for (int e = 0; e < 8; e += 2) {
@@ -387,12 +418,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
               stg_128(yrow + n, make_uint4(w[0], w[1], w[2], w[3]));
             } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                if (n + e < o.n) {
-                  const float be = o.bias ? __ldg(o.bias + n + e) : 0.0f;
-                  yrow[n + e] = __float2bfloat16_rn(fmaf(static_cast<float>(acc[j + e]), srow * __ldg(o.sw + n + e), be));
-                }
-              }
+              for (int e = 0; e < 8; ++e)
+                if (n + e < o.n) yrow[n + e] = __float2bfloat16_rn(fmaf(static_cast<float>(acc[j + e]), srow * swv[e], bv[e]));
             }
           }
         }
@@ -400,6 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     }
   }
 
+  cp_async_wait_all();  // no copy into shared memory outlives the CTA (abort path)
   tc_fence_before();
   __syncthreads();
   // neither CTA leaves while the other may still write into it

@@ -475,7 +475,11 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaSuccess;
   const long long tiles = (M + R - 1) / R;
-  const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
+  // the fewest CTAs that still take every tile in the same number of rounds:
+  // no partial last round in which most of the GPU would sit idle
+  const long long slots = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
+  const long long rounds = (tiles + slots - 1) / slots;
+  const long long grid = (tiles + rounds - 1) / rounds;
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, Q, S, Q16,
                                                              scale_divisor(CONVROT_T_REGULAR_H4, G), stage_bytes,
                                                              tbytes, kDefaultSpinLimit);
