@@ -56,6 +56,10 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
+// Y leaves through TMA stores of 32 rows x 16 columns (one warp's rows),
+// 32-byte swizzle: the 16-byte half of row r sits at half ^ (r >> 2 & 1).
+constexpr int OUT_COLS = 16;
+constexpr int OUT_PIECE_BYTES = 1024;
 
 // CL = 1: one CTA computes a 128 x BN tile with cta_group::1 MMAs.
 // CL = 2: a cluster pair computes a 256 x BN tile with cta_group::2 MMAs
@@ -72,9 +76,13 @@ struct Cfg {
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int HALF = BN / 2;  // columns per epilogue thread
+  // per epilogue warp: two 32 x 16 bf16 output pieces for the tiled store
+  static constexpr int OUT_BYTES = NUM_EPI_WARPS * 2 * OUT_PIECE_BYTES;
   // per epilogue warp: the column scales and biases of its half tile
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * HALF * 2 * 4;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + EPI_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + EPI_BYTES + 1024;
+  static_assert(STAGE_BYTES % 1024 == 0, "the output pieces stay 1 KB aligned");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(HALF % 16 == 0, "the drain loads 32 or 16 columns at a time");
   // Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = F16
   // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
@@ -85,6 +93,7 @@ struct Cfg {
 struct TcParams {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b[kMaxLinears];
+  CUtensorMap tmap_y[kMaxLinears];  // bf16 Y [M, n] for the tiled stores (when y_tma)
   GemmOutputs outs;
   const float* sx;
   long long M;
@@ -92,6 +101,7 @@ struct TcParams {
   int m_tiles;
   int n_tiles;
   int num_tiles;   // cluster tiles: (m tiles / cluster size, rounded up) x n tiles
+  int y_tma;       // 1: Y through tmap_y; 0: direct stores
   long long spin_limit;
 };
 
@@ -147,14 +157,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   static_assert(CL == 1 || CL == 2, "cluster of 1 or 2 CTAs");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  unsigned char* out_smem = smem + C::STAGES * C::STAGE_BYTES;  // 1 KB aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_smem + C::OUT_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* final_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  unsigned char* epi_smem = smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES;
+  unsigned char* epi_smem = out_smem + C::OUT_BYTES + C::BAR_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / BK;
@@ -310,6 +321,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // this warp's copy of the half tile's column scales, then biases
     const uint32_t wsw = smem_u32(epi_smem) + static_cast<uint32_t>((warp - 2) * C::HALF * 2 * 4);
     const uint32_t wbias = wsw + C::HALF * 4;
+    const uint32_t wout = smem_u32(out_smem) + static_cast<uint32_t>((warp - 2) * 2 * OUT_PIECE_BYTES);
+    // this lane's row in an output piece, with the 32-byte swizzle
+    const uint32_t out_row = static_cast<uint32_t>(lane) * 32;
+    const uint32_t out_sw = static_cast<uint32_t>((lane >> 2) & 1) << 4;
+    int piece = 0;  // output pieces issued by this warp so far
     int chunk = 0;
     bool ok = true;
     for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
@@ -381,7 +397,53 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         cp_async_wait_all();
         __syncwarp();
       }
-      if (m < p.M) {
+      if (!RAW && p.y_tma) {
+        // The warp's 32 rows x HALF columns leave in 32 x 16 pieces through
+        // two buffers; lane 0 issues the stores and, before a buffer is
+        // rewritten, waits until the store issued from it two pieces ago has
+        // read it. Rows past M and columns past n are clipped by the copy.
+        const int row0 = m_blk * BM + q * 32;
+        const bool rows_in = row0 < p.M;
+#pragma unroll
+        for (int j = 0; j < C::HALF; j += OUT_COLS) {
+          if (!rows_in || nb + j >= o.n) continue;  // warp-uniform
+          const uint32_t pb = wout + static_cast<uint32_t>((piece & 1) * OUT_PIECE_BYTES);
+          if (piece >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          uint32_t w[8];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float swv[8], bv[8];
+            lds_128(wsw + 4 * (j + 8 * h), swv);
+            lds_128(wsw + 4 * (j + 8 * h) + 16, swv + 4);
+            lds_128(wbias + 4 * (j + 8 * h), bv);
+            lds_128(wbias + 4 * (j + 8 * h) + 16, bv + 4);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const int c = j + 8 * h + e;
+              const float y0 = fmaf(static_cast<float>(acc[c]), srow * swv[e], bv[e]);
+              const float y1 = fmaf(static_cast<float>(acc[c + 1]), srow * swv[e + 1], bv[e + 1]);
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(y0, y1);
+              w[4 * h + e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + out_row + out_sw), "r"(w[0]), "r"(w[1]),
+                       "r"(w[2]), "r"(w[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + out_row + (16u ^ out_sw)), "r"(w[4]),
+                       "r"(w[5]), "r"(w[6]), "r"(w[7])
+                       : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmap_y[li], pb, nb + j, row0);
+            bulk_commit();
+          }
+          ++piece;
+        }
+      } else if (m < p.M) {
         if constexpr (RAW) {
           int* yrow = static_cast<int*>(o.y) + m * o.ldy;
 #pragma unroll
@@ -428,6 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
 
   cp_async_wait_all();  // no copy into shared memory outlives the CTA (abort path)
+  if (warp >= 2 && (threadIdx.x & 31) == 0) bulk_wait_all();  // the tiled stores are complete
   tc_fence_before();
   __syncthreads();
   // neither CTA leaves while the other may still write into it
@@ -501,6 +564,24 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
     nt += (outs.o[i].n + BN - 1) / BN;
     // in a pair each CTA loads its BN / 2 rows of the B tile
     if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN / CL)) return cudaErrorInvalidValue;
+  }
+  // Y through tiled stores when every output allows it: bf16, 16-byte aligned
+  // base and row pitch, at least one full piece wide
+  p.y_tma = RAW ? 0 : 1;
+  for (int i = 0; i < outs.count && p.y_tma; ++i) {
+    const GemmOut& o = outs.o[i];
+    if (reinterpret_cast<uintptr_t>(o.y) % 16 != 0 || (o.ldy * 2) % 16 != 0 || o.n < OUT_COLS || M < 32) {
+      p.y_tma = 0;
+      break;
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.n), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ldy) * 2};
+    cuuint32_t box[2] = {OUT_COLS, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&p.tmap_y[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.y, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      p.y_tma = 0;
   }
   p.outs = outs;
   p.sx = sx;

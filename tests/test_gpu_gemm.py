@@ -234,3 +234,38 @@ def test_small_m_multi_equals_separate_calls(cr):
     Ys = cr.convrot_linear_multi(a, ws, bs)
     for Y, w, b in zip(Ys, ws, bs):
         assert torch.equal(Y, cr.convrot_linear(a, w, b))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("N,ld", [(1000, None), (24, None), (8, None), (200, 264), (1000, 1008)])
+def test_epilogue_ragged_columns_and_row_pitch(cr, path, N, ld):
+    """Large-M outputs whose width is not a multiple of the tile or of the
+    16-column store piece (or narrower than one piece), written densely or
+    into a wider buffer. Columns past N stay untouched."""
+    M, K = 333, 1024
+    rng = np.random.default_rng(N + (ld or 0))
+    Qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    sx = rng.uniform(0.5, 2.0, M) / 127.0
+    sw = rng.uniform(0.5, 2.0, N) / 127.0
+    bias = rng.normal(0, 0.5, N).astype(np.float32)
+    a = packed_from_codes(cr, Qx, sx, 0, "none", path == "tc", "act")
+    w = packed_from_codes(cr, Qw, sw, 0, "none", path == "tc", "w")
+    A = O.int_gemm(Qx, Qw)
+    if ld is None:
+        Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda())
+    else:
+        big = torch.full((M, ld), 7.0, dtype=torch.bfloat16, device="cuda")
+        Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda(), out=big[:, :N])
+        assert torch.all(big[:, N:] == 7.0)
+    check_y_same_codes(to_np(Y.float()), A, sx.astype(np.float32), sw.astype(np.float32), bias, f"{path}/{N}/{ld}")
+
+
+def test_row_pitch_not_multiple_of_8_is_rejected(cr):
+    M, K, N = 96, 1024, 200
+    a = packed_from_codes(cr, np.ones((M, K), np.int8), np.ones(M), 0, "none", True, "act")
+    w = packed_from_codes(cr, np.ones((N, K), np.int8), np.ones(N), 0, "none", True, "w")
+    big = torch.zeros((M, 203), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cr.ConvRotError, match="ALIGNMENT"):
+        cr.convrot_linear(a, w, out=big[:, :N])
+    assert torch.all(big == 0)
