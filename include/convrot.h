@@ -171,6 +171,34 @@ convrot_status convrot_linear_multi(const convrot_packed_act* a, int32_t n,
 convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w,
                                 int32_t* A, int64_t lda, cudaStream_t stream);
 
+/* GEMM workspace. The pages have no counterpart: this is a scheduling device
+ * of the tensor-core path. When the tiles of the last round would leave at
+ * least half of the GPU idle, the GEMM splits them along K, one piece per
+ * cluster; the pieces add their int32 partial sums into the workspace and
+ * the last one to arrive reads the totals and finishes the tile. Integer
+ * sums are exact, so results are bit-identical with or without a workspace.
+ *   workspace        device memory, 256-byte aligned, ALL ZERO before its
+ *                    first use; every call whose kernels run to completion
+ *                    leaves it all zero again (after a call that recorded
+ *                    CONVROT_ERR_TIMEOUT its content is undefined: clear it).
+ *   workspace_bytes  its size; CONVROT_GEMM_WORKSPACE_BYTES covers every split
+ *                    the library plans on a GPU with up to 160 SMs, a smaller
+ *                    one allows fewer. NULL: no split.
+ * Calls sharing one workspace must not overlap in time (issue them on one
+ * stream). The int8 warp-MMA and small-M paths ignore the workspace.
+ * Errors as for the calls without _ws, plus ALIGNMENT (workspace) and
+ * INVALID_ARG (negative size). */
+#define CONVROT_GEMM_WORKSPACE_BYTES (4096 + 40 * 256 * 1024)
+
+convrot_status convrot_linear_multi_ws(const convrot_packed_act* a, int32_t n,
+                                       const convrot_packed_weight* w, const float* const* bias,
+                                       uint16_t* const* Y, const int64_t* ldy, void* workspace,
+                                       int64_t workspace_bytes, cudaStream_t stream);
+
+convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_packed_weight* w,
+                                   int32_t* A, int64_t lda, void* workspace, int64_t workspace_bytes,
+                                   cudaStream_t stream);
+
 /* Reads and clears the device error word of the current device (synchronizes
  * the device first). CONVROT_OK if no kernel reported a problem, else the
  * first status a kernel recorded (e.g. CONVROT_ERR_TIMEOUT). */

@@ -26,14 +26,17 @@ import torch
 __all__ = [
     "ConvRotError", "PackedAct", "PackedWeight", "ConvRotLinear", "TRANSFORMS",
     "convrot_prepare_weights", "convrot_quantize_act", "convrot_quantize_act_hmatmul",
-    "convrot_linear", "convrot_linear_multi", "convrot_gemm_s32",
-    "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
+    "convrot_linear", "convrot_linear_multi", "convrot_gemm_s32", "gemm_workspace",
+    "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libconvrot.so")
 
 TRANSFORMS = {"h4": 0, "rht": 1, "none": 2}
+# CONVROT_GEMM_WORKSPACE_BYTES: scratch that lets the GEMM split a mostly idle
+# last round of tiles along K
+GEMM_WORKSPACE_BYTES = 4096 + 40 * 256 * 1024
 _DTYPE_F32, _DTYPE_BF16 = 0, 1
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_GROUP", 3: "ALIGNMENT", 4: "CUDA", 5: "TIMEOUT"}
 
@@ -75,7 +78,10 @@ _SIGS = {
     "convrot_linear": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _P, _I64, _P],
     "convrot_linear_multi": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                              ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
+    "convrot_linear_multi_ws": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
+                                ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P],
     "convrot_gemm_s32": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P],
+    "convrot_gemm_s32_ws": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P, _I64, _P],
     "convrot_get_device_status": [],
     "convrot_selftest_wait_timeout": [_I64, _P],
     "convrot_status_str": [_I32],
@@ -206,11 +212,20 @@ def convrot_quantize_act_hmatmul(X: torch.Tensor, group: int, with_f16: bool = T
     return PackedAct(q, s, q16, group, TRANSFORMS["h4"])
 
 
+def gemm_workspace(device=None) -> torch.Tensor:
+    """A zeroed GEMM workspace (caller-owned; calls sharing it must be ordered,
+    e.g. on one stream). Every completed call leaves it zeroed again."""
+    return torch.zeros(GEMM_WORKSPACE_BYTES, dtype=torch.uint8, device=device or "cuda")
+
+
 def convrot_linear(a: PackedAct, w: PackedWeight, bias: Optional[torch.Tensor] = None,
-                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                   out: Optional[torch.Tensor] = None, stream=None,
+                   workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Y = A * s_x * s_w + b (bf16) for one linear."""
     if out is None:
         out = torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q.device)
+    if workspace is not None:
+        return convrot_linear_multi(a, [w], [bias], outs=[out], stream=stream, workspace=workspace)[0]
     ca, cw = a._c(), w._c()
     _check(lib.convrot_linear(ctypes.byref(ca), ctypes.byref(cw), _ptr(bias), out.data_ptr(), out.stride(0),
                               _stream(stream)))
@@ -218,7 +233,8 @@ def convrot_linear(a: PackedAct, w: PackedWeight, bias: Optional[torch.Tensor] =
 
 
 def convrot_linear_multi(a: PackedAct, ws: Sequence[PackedWeight], biases: Optional[Sequence] = None,
-                         outs: Optional[List[torch.Tensor]] = None, stream=None) -> List[torch.Tensor]:
+                         outs: Optional[List[torch.Tensor]] = None, stream=None,
+                         workspace: Optional[torch.Tensor] = None) -> List[torch.Tensor]:
     """Several linears sharing one packed activation, in one launch."""
     n = len(ws)
     if outs is None:
@@ -228,17 +244,27 @@ def convrot_linear_multi(a: PackedAct, ws: Sequence[PackedWeight], biases: Optio
     yarr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
     larr = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
     ca = a._c()
-    _check(lib.convrot_linear_multi(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
+    if workspace is None:
+        _check(lib.convrot_linear_multi(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
+    else:
+        _check(lib.convrot_linear_multi_ws(ctypes.byref(ca), n, warr, barr, yarr, larr, workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
     return outs
 
 
-def convrot_gemm_s32(a: PackedAct, w: PackedWeight, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+def convrot_gemm_s32(a: PackedAct, w: PackedWeight, out: Optional[torch.Tensor] = None, stream=None,
+                     workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Raw int32 accumulators A = Q_x Q_w^T through the linear's GEMM main loop."""
     if out is None:
         out = torch.empty((a.M, w.N), dtype=torch.int32, device=a.q.device)
     ca, cw = a._c(), w._c()
-    _check(lib.convrot_gemm_s32(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
-                                _stream(stream)))
+    if workspace is None:
+        _check(lib.convrot_gemm_s32(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
+                                    _stream(stream)))
+    else:
+        _check(lib.convrot_gemm_s32_ws(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
+                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
     return out
 
 
@@ -258,10 +284,12 @@ class ConvRotLinear:
     runs the int8 GEMM with the fused epilogue, then restores the shape.
     """
 
-    def __init__(self, packed: PackedWeight, bias: Optional[torch.Tensor], signs: Optional[torch.Tensor] = None):
+    def __init__(self, packed: PackedWeight, bias: Optional[torch.Tensor], signs: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None):
         self.weight = packed
         self.bias = None if bias is None else bias.to(device=packed.q.device, dtype=torch.float32).contiguous()
         self.signs = signs
+        self.workspace = workspace  # optional GEMM workspace (see gemm_workspace)
 
     @classmethod
     def from_float(cls, W: torch.Tensor, bias: Optional[torch.Tensor], group: int, transform="h4",
@@ -275,7 +303,7 @@ class ConvRotLinear:
         x2 = x.reshape(-1, shape[-1])
         a = convrot_quantize_act(x2, self.weight.group, self.weight.transform, self.signs,
                                  with_f16=self.weight.q_f16 is not None)
-        y = convrot_linear(a, self.weight, self.bias)
+        y = convrot_linear(a, self.weight, self.bias, workspace=self.workspace)
         return y.reshape(*shape[:-1], y.shape[-1])
 
     __call__ = forward

@@ -21,7 +21,7 @@ bool hmatmul_supported(long long K, long long ldx, int G);
 cudaError_t gemm_mma_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                             bool raw, cudaStream_t st);
 cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
-                           bool raw, cudaStream_t st);
+                           bool raw, void* ws, long long ws_bytes, cudaStream_t st);
 bool gemm_tc_supported(long long M, int K);
 cudaError_t gemm_small_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                               bool raw, cudaStream_t st);
@@ -196,7 +196,8 @@ convrot_status check_pair(const convrot_packed_act* a, const convrot_packed_weig
   return CONVROT_OK;
 }
 
-convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw, cudaStream_t stream) {
+convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw, void* ws, long long ws_bytes,
+                        cudaStream_t stream) {
   if (a->M == 0) return ok();
   bool all_f16 = a->q_f16 != nullptr;
   for (int i = 0; i < outs.count; ++i) all_f16 = all_f16 && outs.o[i].qw16 != nullptr;
@@ -206,7 +207,7 @@ convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw
     e = gemm_small_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
   } else if (all_f16 && gemm_tc_supported(a->M, static_cast<int>(a->K))) {
-    e = gemm_tc_launch(a->q_f16, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    e = gemm_tc_launch(a->q_f16, a->scale, a->M, static_cast<int>(a->K), outs, raw, ws, ws_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
   } else {
     e = gemm_mma_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
@@ -292,6 +293,58 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
   return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+convrot_status check_workspace(const void* ws, int64_t ws_bytes) {
+  if (!ws) return ok();
+  if (!aligned(ws, 256)) return fail(CONVROT_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (ws_bytes < 0) return fail(CONVROT_ERR_INVALID_ARG, "workspace_bytes=%lld < 0", static_cast<long long>(ws_bytes));
+  return ok();
+}
+
+convrot_status linear_multi(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                            const float* const* bias, uint16_t* const* Y, const int64_t* ldy, void* ws,
+                            int64_t ws_bytes, cudaStream_t stream) {
+  if (n < 1 || n > kMaxLinears) return fail(CONVROT_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, kMaxLinears);
+  if (!w || !Y || !ldy) return fail(CONVROT_ERR_INVALID_ARG, "w, Y and ldy arrays must be non-null");
+  convrot_status s = check_workspace(ws, ws_bytes);
+  if (s != CONVROT_OK) return s;
+  GemmOutputs outs{};
+  outs.count = n;
+  for (int i = 0; i < n; ++i) {
+    s = check_pair(a, &w[i]);
+    if (s != CONVROT_OK) return s;
+    const float* b = bias ? bias[i] : nullptr;
+    if (a->M > 0 && !Y[i]) return fail(CONVROT_ERR_INVALID_ARG, "Y[%d] is null", i);
+    if (ldy[i] < w[i].N) return fail(CONVROT_ERR_INVALID_ARG, "ldy[%d] < N", i);
+    if (!aligned(Y[i], 16) || ldy[i] % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y[%d] alignment", i);
+    if (b && !aligned(b, 16)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] must be 16-byte aligned", i);
+    outs.o[i] = GemmOut{w[i].q, w[i].q_f16, w[i].scale, b, Y[i], ldy[i], static_cast<int>(w[i].N), 0};
+  }
+  return run_gemm(a, outs, false, ws, ws_bytes, stream);
+}
+
+convrot_status gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A, int64_t lda,
+                        void* ws, int64_t ws_bytes, cudaStream_t stream) {
+  convrot_status s = check_pair(a, w);
+  if (s != CONVROT_OK) return s;
+  s = check_workspace(ws, ws_bytes);
+  if (s != CONVROT_OK) return s;
+  if (a->M > 0 && !A) return fail(CONVROT_ERR_INVALID_ARG, "A is null");
+  if (lda < w->N) return fail(CONVROT_ERR_INVALID_ARG, "lda < N");
+  if (!aligned(A, 16) || lda % 4) return fail(CONVROT_ERR_ALIGNMENT, "A must be 16-byte aligned and lda a multiple of 4");
+  GemmOutputs outs{};
+  outs.count = 1;
+  outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, nullptr, A, lda, static_cast<int>(w->N), 0};
+  return run_gemm(a, outs, true, ws, ws_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
 convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_weight* w, const float* bias,
                               uint16_t* Y, int64_t ldy, cudaStream_t stream) {
   convrot_status s = check_pair(a, w);
@@ -303,40 +356,29 @@ convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_
   GemmOutputs outs{};
   outs.count = 1;
   outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, bias, Y, ldy, static_cast<int>(w->N), 0};
-  return run_gemm(a, outs, false, stream);
+  return run_gemm(a, outs, false, nullptr, 0, stream);
 }
 
 convrot_status convrot_linear_multi(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
                                     const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
                                     cudaStream_t stream) {
-  if (n < 1 || n > kMaxLinears) return fail(CONVROT_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, kMaxLinears);
-  if (!w || !Y || !ldy) return fail(CONVROT_ERR_INVALID_ARG, "w, Y and ldy arrays must be non-null");
-  GemmOutputs outs{};
-  outs.count = n;
-  for (int i = 0; i < n; ++i) {
-    convrot_status s = check_pair(a, &w[i]);
-    if (s != CONVROT_OK) return s;
-    const float* b = bias ? bias[i] : nullptr;
-    if (a->M > 0 && !Y[i]) return fail(CONVROT_ERR_INVALID_ARG, "Y[%d] is null", i);
-    if (ldy[i] < w[i].N) return fail(CONVROT_ERR_INVALID_ARG, "ldy[%d] < N", i);
-    if (!aligned(Y[i], 16) || ldy[i] % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y[%d] alignment", i);
-    if (b && !aligned(b, 16)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] must be 16-byte aligned", i);
-    outs.o[i] = GemmOut{w[i].q, w[i].q_f16, w[i].scale, b, Y[i], ldy[i], static_cast<int>(w[i].N), 0};
-  }
-  return run_gemm(a, outs, false, stream);
+  return linear_multi(a, n, w, bias, Y, ldy, nullptr, 0, stream);
+}
+
+convrot_status convrot_linear_multi_ws(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                                       const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
+                                       void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
+  return linear_multi(a, n, w, bias, Y, ldy, workspace, workspace_bytes, stream);
 }
 
 convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
                                 int64_t lda, cudaStream_t stream) {
-  convrot_status s = check_pair(a, w);
-  if (s != CONVROT_OK) return s;
-  if (a->M > 0 && !A) return fail(CONVROT_ERR_INVALID_ARG, "A is null");
-  if (lda < w->N) return fail(CONVROT_ERR_INVALID_ARG, "lda < N");
-  if (!aligned(A, 16) || lda % 4) return fail(CONVROT_ERR_ALIGNMENT, "A must be 16-byte aligned and lda a multiple of 4");
-  GemmOutputs outs{};
-  outs.count = 1;
-  outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, nullptr, A, lda, static_cast<int>(w->N), 0};
-  return run_gemm(a, outs, true, stream);
+  return gemm_s32(a, w, A, lda, nullptr, 0, stream);
+}
+
+convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
+                                   int64_t lda, void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
+  return gemm_s32(a, w, A, lda, workspace, workspace_bytes, stream);
 }
 
 convrot_status convrot_get_device_status(void) {

@@ -24,9 +24,15 @@
 //   warps 2..9  epilogue: TMEM -> registers (tcgen05.ld 32x32b), int32
 //               accumulation, then scaling, bias, bf16 and the store.
 // Tiles are handed out statically (tile = blockIdx.x + i * gridDim.x) in a
-// grouped order for L2 reuse; the schedule is data-parallel (no split-K), so
-// every output is computed by exactly one CTA in a fixed order and results
-// do not depend on how the rows are partitioned.
+// grouped order for L2 reuse. When the last round would leave most of the
+// GPU idle and the caller gave a workspace, the tiles of that round are
+// split along K instead, one piece per cluster: each piece adds its int32
+// partial sums into the tile's workspace slot with bulk reductions (TMA,
+// performed in L2), and the warp that brings the last piece of its 32-row
+// slab reads the totals back, clears them and runs the epilogue. Integer
+// addition is exact and associative, so the result is bit-identical to the
+// unsplit schedule and does not depend on how the rows are partitioned.
+// Nothing waits on another CTA.
 //
 // Every mbarrier wait is bounded. A wait that gives up records
 // CONVROT_ERR_TIMEOUT in the device error word and raises a CTA-wide abort
@@ -102,6 +108,11 @@ struct TcParams {
   int n_tiles;
   int num_tiles;   // cluster tiles: (m tiles / cluster size, rounded up) x n tiles
   int y_tma;       // 1: Y through tmap_y; 0: direct stores
+  int dp_tiles;    // tiles computed whole, round-robin over the clusters
+  int sk_tiles;    // the tiles after those, each split along K ...
+  int sk_pieces;   // ... into this many pieces, one per cluster
+  int* ws_cnt;     // split tiles: arrival counter per 32-row slab
+  int* ws_acc;     // split tiles: int32 sums, [tile][rank][warp][8-column chunk][lane][8]
   long long spin_limit;
 };
 
@@ -151,6 +162,29 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int rank, 
   n_local = n_glob - p.outs.o[li].tile_begin;
 }
 
+// Work item i of cluster c (of nc): tile t over k blocks [kb0, kb1); piece
+// is -1 for a whole tile, else the index of the K piece of a split tile.
+// Returns false past the cluster's last item.
+__device__ __forceinline__ bool work_item(const TcParams& p, int c, int nc, int i, int nk, int& t, int& kb0, int& kb1,
+                                         int& piece) {
+  const int td = c + i * nc;
+  if (td < p.dp_tiles) {
+    t = td;
+    kb0 = 0;
+    kb1 = nk;
+    piece = -1;
+    return true;
+  }
+  // with a split, dp_tiles is a multiple of nc: every cluster has dp_tiles / nc
+  // whole tiles, then at most one piece
+  if (p.sk_tiles == 0 || i != p.dp_tiles / nc || c >= p.sk_tiles * p.sk_pieces) return false;
+  t = p.dp_tiles + c / p.sk_pieces;
+  piece = c % p.sk_pieces;
+  kb0 = piece * nk / p.sk_pieces;
+  kb1 = (piece + 1) * nk / p.sk_pieces;
+  return true;
+}
+
 template <int BN, bool RAW, int CL>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<BN, CL>;
@@ -169,7 +203,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / BK;
-  const int nch = (nk + KITER_PER_CHUNK - 1) / KITER_PER_CHUNK;
   const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
   const int cluster_id = blockIdx.x / CL, nclusters = gridDim.x / CL;
 
@@ -214,10 +247,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       for (int s = 0; s < C::STAGES; ++s) armed_round[s] = -1;
       int it = 0;
       bool ok = true;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
+      int t, kb0, kb1, pc;
+      for (int i = 0; ok && work_item(p, cluster_id, nclusters, i, nk, t, kb0, kb1, pc); ++i) {
         int m_blk, n_glob, li, n_local;
         decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES, round = it / C::STAGES;
           if (!wait_or_abort(&empty[s], (round & 1) ^ 1, p.spin_limit, abort_flag)) {
             raise_abort(abort_flag);
@@ -257,8 +291,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     } else if (lane == 0) {
       int it = 0, chunk = 0;
       bool ok = true;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
-        for (int kb = 0; kb < nk && ok;) {
+      int t, kb0, kb1, pc;
+      for (int i = 0; ok && work_item(p, cluster_id, nclusters, i, nk, t, kb0, kb1, pc); ++i) {
+        for (int kb = kb0; kb < kb1 && ok;) {
           const int b = chunk & 1, u = chunk >> 1;
           if (!wait_or_abort(&acc_empty[b], (u & 1) ^ 1, p.spin_limit, abort_flag)) {
             raise_abort(abort_flag);
@@ -267,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-          const int kend = min(kb + KITER_PER_CHUNK, nk);
+          const int kend = min(kb + KITER_PER_CHUNK, kb1);
           const int kstart = kb;
           for (; kb < kend; ++kb, ++it) {
             const int s = it % C::STAGES, round = it / C::STAGES;
@@ -325,12 +360,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // this lane's row in an output piece, with the 32-byte swizzle
     const uint32_t out_row = static_cast<uint32_t>(lane) * 32;
     const uint32_t out_sw = static_cast<uint32_t>((lane >> 2) & 1) << 4;
-    int piece = 0;  // output pieces issued by this warp so far
+    int ob = 0;  // output-buffer uses (tiled stores, bulk reductions) by this warp so far
     int chunk = 0;
     bool ok = true;
-    for (int t = cluster_id; t < p.num_tiles && ok; t += nclusters) {
+    int t, kb0, kb1, pc;
+    for (int i = 0; ok && work_item(p, cluster_id, nclusters, i, nk, t, kb0, kb1, pc); ++i) {
       int m_blk, n_glob, li, n_local;
       decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
+      const int nch = (kb1 - kb0 + KITER_PER_CHUNK - 1) / KITER_PER_CHUNK;
       const GemmOut& o = p.outs.o[li];
       const long long m = static_cast<long long>(m_blk) * BM + row_in_tile;
       const int nb = n_local * BN + col0;
@@ -397,18 +434,73 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         cp_async_wait_all();
         __syncwarp();
       }
+      if (pc >= 0) {
+        // a piece of a split tile: add this warp's 32-row slab of partial sums
+        // into the tile's workspace slot by bulk reductions in L2 (8 columns
+        // = 1 KB at a time, staged in the output buffers). The warp whose
+        // piece arrives last for the slab reads the totals, clears the slot
+        // and the counter for the next call, and finishes the slab; the
+        // others move on.
+        const int slab = ((t - p.dp_tiles) * CL + rank) * NUM_EPI_WARPS + (warp - 2);
+        int* wslab = p.ws_acc + static_cast<long long>(slab) * (C::HALF * 32);  // [8-column chunk][lane][8]
+#pragma unroll
+        for (int j = 0; j < C::HALF; j += 8) {
+          const uint32_t pb = wout + static_cast<uint32_t>((ob & 1) * OUT_PIECE_BYTES);
+          if (ob >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + lane * 32), "r"(acc[j]), "r"(acc[j + 1]),
+                       "r"(acc[j + 2]), "r"(acc[j + 3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + lane * 32 + 16), "r"(acc[j + 4]),
+                       "r"(acc[j + 5]), "r"(acc[j + 6]), "r"(acc[j + 7])
+                       : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            bulk_reduce_add_s32(wslab + j * 32, pb, OUT_PIECE_BYTES);
+            bulk_commit();
+          }
+          ++ob;
+        }
+        int prev = 0;
+        if (lane == 0) {
+          bulk_wait_all();  // the additions are complete ...
+          fence_proxy_async_global();
+          __threadfence();  // ... and visible before the arrival is counted
+          prev = atomicAdd(p.ws_cnt + slab, 1);
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != p.sk_pieces - 1) continue;
+        __threadfence();
+        fence_proxy_async_global();
+#pragma unroll
+        for (int j = 0; j < C::HALF; j += 8) {
+          const int4 lo = __ldcg(reinterpret_cast<const int4*>(wslab + j * 32 + lane * 8));
+          const int4 hi = __ldcg(reinterpret_cast<const int4*>(wslab + j * 32 + lane * 8 + 4));
+          acc[j] = lo.x; acc[j + 1] = lo.y; acc[j + 2] = lo.z; acc[j + 3] = lo.w;
+          acc[j + 4] = hi.x; acc[j + 5] = hi.y; acc[j + 6] = hi.z; acc[j + 7] = hi.w;
+        }
+#pragma unroll
+        for (int j = 0; j < C::HALF; j += 8) {
+          __stcg(reinterpret_cast<int4*>(wslab + j * 32 + lane * 8), make_int4(0, 0, 0, 0));
+          __stcg(reinterpret_cast<int4*>(wslab + j * 32 + lane * 8 + 4), make_int4(0, 0, 0, 0));
+        }
+        if (lane == 0) atomicExch(p.ws_cnt + slab, 0);
+      }
       if (!RAW && p.y_tma) {
         // The warp's 32 rows x HALF columns leave in 32 x 16 pieces through
         // two buffers; lane 0 issues the stores and, before a buffer is
-        // rewritten, waits until the store issued from it two pieces ago has
+        // rewritten, waits until the copy issued from it two uses ago has
         // read it. Rows past M and columns past n are clipped by the copy.
         const int row0 = m_blk * BM + q * 32;
         const bool rows_in = row0 < p.M;
 #pragma unroll
         for (int j = 0; j < C::HALF; j += OUT_COLS) {
           if (!rows_in || nb + j >= o.n) continue;  // warp-uniform
-          const uint32_t pb = wout + static_cast<uint32_t>((piece & 1) * OUT_PIECE_BYTES);
-          if (piece >= 2) {
+          const uint32_t pb = wout + static_cast<uint32_t>((ob & 1) * OUT_PIECE_BYTES);
+          if (ob >= 2) {
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
           }
@@ -441,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             tma_store_2d(&p.tmap_y[li], pb, nb + j, row0);
             bulk_commit();
           }
-          ++piece;
+          ++ob;
         }
       } else if (m < p.M) {
         if constexpr (RAW) {
@@ -525,24 +617,61 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long r
 // peak (measured on GB300, 2-SM MMA: N = 256 / 192 / 128 reach 0.85 / 0.71 /
 // 0.50 of the bf16 peak on the same shapes; 128 is therefore not offered).
 // The choice minimizes
-// waves x (time of one tile), a wave being one tile per resident cluster.
+// rounds x (time of one tile), a round being one tile per resident cluster;
+// a last round split along K costs 1 / pieces of a round plus a fixed time
+// for the partial sums' trip through L2 and the exposed final epilogue
+// (about 10 us measured on GB300; in the model's cycles, with the tensor
+// pipes at the ~72 % they sustain here, some 15000).
 double mma_cycles_per_column(int bn) {
   const double compute = bn / 2.0;
   const double operands = (4096.0 + 16.0 * bn) / 64.0;
   return std::max(compute, operands) / bn;
 }
 
-int choose_bn(long long M, const GemmOutputs& outs, int sms, int cl) {
+// Workspace layout: arrival counters in the first 4 KB, then the partial sums.
+constexpr long long kWsCounterBytes = 4096;
+
+struct SplitPlan {
+  int dp_tiles;  // whole tiles
+  int sk_tiles;  // split tiles (0: no split)
+  int pieces;    // K pieces per split tile
+};
+
+// Split the last round along K when it would leave at least half of the
+// clusters idle and the workspace has a slot for every split tile; each
+// piece keeps at least two k blocks.
+SplitPlan plan_split(long long tiles, int clusters, int nk, int bn, int cl, long long ws_bytes) {
+  SplitPlan sp{static_cast<int>(tiles), 0, 1};
+  if (ws_bytes <= kWsCounterBytes || clusters < 2) return sp;
+  // one slot of sums per split tile, one counter per 32-row slab
+  const long long slot_bytes = static_cast<long long>(cl) * BM * bn * 4;
+  const long long slots = (ws_bytes - kWsCounterBytes) / slot_bytes;
+  const long long tail = tiles % clusters;
+  if (tail == 0 || tail > slots || tail * cl * NUM_EPI_WARPS * 4 > kWsCounterBytes) return sp;
+  const long long pieces = std::min<long long>(clusters / tail, nk / 2);
+  if (pieces < 2) return sp;
+  sp.dp_tiles = static_cast<int>(tiles - tail);
+  sp.sk_tiles = static_cast<int>(tail);
+  sp.pieces = static_cast<int>(pieces);
+  return sp;
+}
+
+constexpr double kSplitOverheadCycles = 15000.0;
+
+int choose_bn(long long M, int K, const GemmOutputs& outs, int sms, int cl, long long ws_bytes) {
   const long long mt = ((M + BM - 1) / BM + cl - 1) / cl;
-  const long long slots = std::max(1, sms / cl);
+  const int clusters = std::max(1, sms / cl);
   int best = 256;
   double best_cost = -1.0;
   for (int bn : {256, 224, 192}) {
     long long nt = 0;
     for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + bn - 1) / bn;
     const long long tiles = mt * nt;
-    const long long waves = (tiles + slots - 1) / slots;
-    const double cost = static_cast<double>(waves) * bn * mma_cycles_per_column(bn);
+    const SplitPlan sp = plan_split(tiles, clusters, K / BK, bn, cl, ws_bytes);
+    // cycles of one tile: k blocks x MMAs per block x their cycles
+    const double tile = static_cast<double>(K / BK) * (BK / 16) * bn * mma_cycles_per_column(bn);
+    const double cost = sp.sk_tiles ? (sp.dp_tiles / clusters + 1.0 / sp.pieces) * tile + kSplitOverheadCycles
+                                    : static_cast<double>((tiles + clusters - 1) / clusters) * tile;
     if (best_cost < 0 || cost < best_cost * 0.999) {
       best_cost = cost;
       best = bn;
@@ -553,7 +682,7 @@ int choose_bn(long long M, const GemmOutputs& outs, int sms, int cl) {
 
 template <int BN, bool RAW, int CL>
 cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K, GemmOutputs outs,
-                      cudaStream_t st, int sms) {
+                      void* ws, long long ws_bytes, cudaStream_t st, int sms) {
   using C = Cfg<BN, CL>;
   TcParams p;
   memset(&p, 0, sizeof(p));
@@ -596,16 +725,26 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   auto kern = gemm_tc_kernel<BN, RAW, CL>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
-  if constexpr (CL == 1) {
-    const int grid = static_cast<int>(std::min<long long>(tiles, sms));
-    kern<<<grid, THREADS, C::SMEM, st>>>(p);
-    return cudaGetLastError();
-  } else {
-    int clusters = 0;
+  // clusters that are resident together: the split plan needs the real count
+  int clusters = sms;
+  if constexpr (CL > 1) {
     e = max_active_clusters(reinterpret_cast<const void*>(kern), THREADS, C::SMEM, CL, &clusters);
     if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    const int grid = CL * static_cast<int>(std::min<long long>(tiles, clusters));
+  }
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const SplitPlan sp = plan_split(tiles, clusters, K / BK, BN, CL, ws ? ws_bytes : 0);
+  p.dp_tiles = sp.dp_tiles;
+  p.sk_tiles = sp.sk_tiles;
+  p.sk_pieces = sp.pieces;
+  p.ws_cnt = static_cast<int*>(ws);
+  p.ws_acc = ws ? reinterpret_cast<int*>(static_cast<char*>(ws) + kWsCounterBytes) : nullptr;
+  // a split runs on every cluster (its whole tiles are a multiple of them)
+  const int nc = sp.sk_tiles ? clusters : static_cast<int>(std::min<long long>(tiles, clusters));
+  if constexpr (CL == 1) {
+    kern<<<nc, THREADS, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+  } else {
+    const int grid = CL * nc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
@@ -624,11 +763,11 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
 
 template <bool RAW, int CL>
 cudaError_t launch_cl(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K,
-                      const GemmOutputs& outs, cudaStream_t st, int sms) {
-  switch (choose_bn(M, outs, sms, CL)) {
-    case 256: return launch_bn<256, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
-    case 224: return launch_bn<224, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
-    default: return launch_bn<192, RAW, CL>(enc, Qx16, sx, M, K, outs, st, sms);
+                      const GemmOutputs& outs, void* ws, long long ws_bytes, cudaStream_t st, int sms) {
+  switch (choose_bn(M, K, outs, sms, CL, ws ? ws_bytes : 0)) {
+    case 256: return launch_bn<256, RAW, CL>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+    case 224: return launch_bn<224, RAW, CL>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+    default: return launch_bn<192, RAW, CL>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
   }
 }
 
@@ -637,18 +776,18 @@ cudaError_t launch_cl(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
 bool gemm_tc_supported(long long M, int K) { return M > 64 && K % BK == 0 && K >= BK; }
 
 cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
-                           bool raw, cudaStream_t st) {
+                           bool raw, void* ws, long long ws_bytes, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const int sms = device_sm_count();
   // CTA pairs run the 2-SM MMA when there are at least two row blocks
   if (M > BM) {
-    return raw ? launch_cl<true, 2>(enc, Qx16, sx, M, K, outs, st, sms)
-               : launch_cl<false, 2>(enc, Qx16, sx, M, K, outs, st, sms);
+    return raw ? launch_cl<true, 2>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
+               : launch_cl<false, 2>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
   }
-  return raw ? launch_cl<true, 1>(enc, Qx16, sx, M, K, outs, st, sms)
-             : launch_cl<false, 1>(enc, Qx16, sx, M, K, outs, st, sms);
+  return raw ? launch_cl<true, 1>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
+             : launch_cl<false, 1>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
 }
 
 }  // namespace convrot

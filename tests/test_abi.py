@@ -90,3 +90,23 @@ def test_linear_validation(cr):
 
 def test_selftest_argument_check(cr):
     assert cr.lib.convrot_selftest_wait_timeout(0, None) == 1
+
+
+def test_workspace_constant_matches_header(cr):
+    text = open(HEADER).read()
+    m = re.search(r"#define CONVROT_GEMM_WORKSPACE_BYTES \(([0-9 +*]+)\)", text)
+    assert m, "CONVROT_GEMM_WORKSPACE_BYTES not found"
+    assert eval(m.group(1), {"__builtins__": {}}) == cr.GEMM_WORKSPACE_BYTES
+
+
+def test_workspace_validation(cr):
+    act = cr._Act(0x1000, 0x2000, None, 4, 256, 256, 0)
+    w = (cr._Weight * 1)(cr._Weight(0x4000, 0x5000, None, 16, 256, 256, 0))
+    bias = (ctypes.c_void_p * 1)(None)
+    ys = (ctypes.c_void_p * 1)(0x6000)
+    ld = (ctypes.c_int64 * 1)(16)
+    f = cr.lib.convrot_linear_multi_ws
+    assert f(ctypes.byref(act), 1, w, bias, ys, ld, 0x7010, cr.GEMM_WORKSPACE_BYTES, None) == 3  # misaligned
+    assert b"256-byte" in cr.lib.convrot_last_error()
+    assert f(ctypes.byref(act), 1, w, bias, ys, ld, 0x7000, -1, None) == 1  # negative size
+    assert f(ctypes.byref(act), 0, w, bias, ys, ld, None, 0, None) == 1     # n out of range

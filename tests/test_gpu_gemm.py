@@ -269,3 +269,76 @@ def test_row_pitch_not_multiple_of_8_is_rejected(cr):
     with pytest.raises(cr.ConvRotError, match="ALIGNMENT"):
         cr.convrot_linear(a, w, out=big[:, :N])
     assert torch.all(big == 0)
+
+
+@pytest.mark.parametrize("M,N", [(300, 1000), (1024, 5120), (129, 1000), (100, 1000)])
+def test_split_last_round_is_bit_exact(cr, M, N):
+    """With a workspace the tensor-core GEMM splits a mostly idle last round
+    of tiles along K (on these shapes for every column width it may pick, on
+    the pair path and, for M = 100, the single-CTA path). The accumulators
+    must equal the oracle's and the unsplit run's, twice in a row on the same
+    workspace, and the workspace must be left all zero."""
+    K = 1024
+    rng = np.random.default_rng(7 * M + N)
+    Qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", True, "act")
+    w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", True, "w")
+    ws = cr.gemm_workspace()
+    A1 = cr.convrot_gemm_s32(a, w, workspace=ws)
+    A2 = cr.convrot_gemm_s32(a, w, workspace=ws)
+    A0 = cr.convrot_gemm_s32(a, w)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    assert torch.equal(A1, A0) and torch.equal(A2, A0)
+    assert np.array_equal(to_np(A1).astype(np.int64), O.int_gemm(Qx, Qw))
+
+
+def test_split_adversarial_magnitudes(cr):
+    """All-127 codes with K = 6144 (the largest partial sums) through split
+    pieces: still exact."""
+    M, N, K = 300, 1000, 6144
+    Qx = np.full((M, K), 127, np.int8)
+    Qw = np.full((N, K), 127, np.int8)
+    Qw[::2] = -127
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", True, "act")
+    w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", True, "w")
+    ws = cr.gemm_workspace()
+    A = to_np(cr.convrot_gemm_s32(a, w, workspace=ws)).astype(np.int64)
+    assert np.array_equal(A, O.int_gemm(Qx, Qw))
+    assert int(ws.count_nonzero()) == 0
+
+
+def test_split_linear_multi_matches_unsplit(cr):
+    """The bf16 linear through split tiles (three linears sharing one packed
+    activation, ragged M): bit-identical to the unsplit run and within one
+    bf16 ulp of the oracle's reconstruction."""
+    wl = WL.qkv32700(M=129)
+    a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4")
+    wts = [cr.convrot_prepare_weights(W.cuda(), 256, "h4") for W in wl.weights]
+    bs = [b.cuda() for b in wl.biases]
+    ws = cr.gemm_workspace()
+    Y1 = cr.convrot_linear_multi(a, wts, bs, workspace=ws)
+    Y0 = cr.convrot_linear_multi(a, wts, bs)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    qx, sx = to_np(a.q).astype(np.int8), to_np(a.scale)
+    for y1, y0, w, b in zip(Y1, Y0, wts, wl.biases):
+        assert torch.equal(y1, y0)
+        A = O.int_gemm(qx, to_np(w.q).astype(np.int8))
+        check_y_same_codes(to_np(y1.float()), A, sx, to_np(w.scale), b.numpy(), "split multi")
+
+
+def test_split_full_size_dit_matches_unsplit(cr):
+    """The DiT linear at full size (4096 x 6144 x 6144), as the bench runs it
+    with a workspace: bit-identical to the unsplit launch."""
+    wl = WL.dit6144()
+    a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4")
+    w = cr.convrot_prepare_weights(wl.weights[0].cuda(), 256, "h4")
+    b = wl.biases[0].cuda()
+    ws = cr.gemm_workspace()
+    Y1 = cr.convrot_linear(a, w, b, workspace=ws)
+    Y0 = cr.convrot_linear(a, w, b)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    assert torch.equal(Y1, Y0)
