@@ -199,6 +199,26 @@ convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_pa
                                    int32_t* A, int64_t lda, void* workspace, int64_t workspace_bytes,
                                    cudaStream_t stream);
 
+/* convrot_linear_multi with the GEMM workspace held by the library instead of
+ * the caller: ALLOCATES NOTHING. The pages have no counterpart; this is a
+ * deployment convenience of this library.
+ * The scratch is a static device array of CONVROT_GEMM_WORKSPACE_BYTES, one
+ * per device, located with cudaGetSymbolAddress and cleared (synchronously)
+ * on the first call on each device; every call whose kernels complete leaves
+ * it clear again, and convrot_get_device_status() clears it after reporting
+ * CONVROT_ERR_TIMEOUT. A split is planned only within that size (a launch
+ * that would need more is rejected before it starts).
+ * RACES: every caller on a device shares the one scratch. Calls that may
+ * overlap in time on the GPU (different streams, different host threads)
+ * race on it and can produce wrong results: serialize them, e.g. on one
+ * stream, or give concurrent calls their own workspaces through
+ * convrot_linear_multi_ws.
+ * Errors: as convrot_linear_multi, plus CUDA if the scratch cannot be
+ * located or cleared. */
+convrot_status convrot_linear_multi_static(const convrot_packed_act* a, int32_t n,
+                                           const convrot_packed_weight* w, const float* const* bias,
+                                           uint16_t* const* Y, const int64_t* ldy, cudaStream_t stream);
+
 /* Reads and clears the device error word of the current device (synchronizes
  * the device first). CONVROT_OK if no kernel reported a problem, else the
  * first status a kernel recorded (e.g. CONVROT_ERR_TIMEOUT). */

@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "ConvRotError", "PackedAct", "PackedWeight", "ConvRotLinear", "TRANSFORMS",
     "convrot_prepare_weights", "convrot_quantize_act", "convrot_quantize_act_hmatmul",
-    "convrot_linear", "convrot_linear_multi", "convrot_gemm_s32", "gemm_workspace",
+    "convrot_linear", "convrot_linear_multi", "convrot_linear_multi_static", "convrot_gemm_s32", "gemm_workspace",
     "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
 ]
 
@@ -82,6 +82,8 @@ _SIGS = {
                                 ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P],
     "convrot_gemm_s32": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P],
     "convrot_gemm_s32_ws": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P, _I64, _P],
+    "convrot_linear_multi_static": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
+                                    ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
     "convrot_get_device_status": [],
     "convrot_selftest_wait_timeout": [_I64, _P],
     "convrot_status_str": [_I32],
@@ -249,6 +251,23 @@ def convrot_linear_multi(a: PackedAct, ws: Sequence[PackedWeight], biases: Optio
     else:
         _check(lib.convrot_linear_multi_ws(ctypes.byref(ca), n, warr, barr, yarr, larr, workspace.data_ptr(),
                                            workspace.numel() * workspace.element_size(), _stream(stream)))
+    return outs
+
+
+def convrot_linear_multi_static(a: PackedAct, ws: Sequence[PackedWeight], biases: Optional[Sequence] = None,
+                                outs: Optional[List[torch.Tensor]] = None, stream=None) -> List[torch.Tensor]:
+    """convrot_linear_multi with the library's static per-device GEMM scratch
+    (the library allocates nothing). Calls that may overlap on the GPU race
+    on that scratch: keep them on one stream."""
+    n = len(ws)
+    if outs is None:
+        outs = [torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q.device) for w in ws]
+    warr = (_Weight * n)(*[w._c() for w in ws])
+    barr = (ctypes.c_void_p * n)(*[(_ptr(b) if b is not None else None) for b in (biases or [None] * n)])
+    yarr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    larr = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
+    ca = a._c()
+    _check(lib.convrot_linear_multi_static(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
     return outs
 
 

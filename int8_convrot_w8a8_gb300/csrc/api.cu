@@ -30,12 +30,18 @@ cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st);
 
 CONVROT_DEFINE_STATUS_WORD(status_word_api)
 
+// Scratch of convrot_linear_multi_static: the GEMM workspace as a static
+// device array (one copy per device, zero when the module loads), so that
+// entry point allocates nothing.
+static __device__ __align__(256) unsigned char g_static_gemm_scratch[CONVROT_GEMM_WORKSPACE_BYTES];
+
 namespace {
 std::mutex g_cache_mu;
 std::map<std::pair<const void*, int>, int> g_smem_set;                 // (kernel, device) -> bytes
 std::map<std::tuple<const void*, int, int, int>, int> g_occupancy;     // (kernel, device, threads, smem)
 std::map<int, int> g_sms;                                              // device -> SM count
 std::map<std::tuple<const void*, int, int, int>, int> g_clusters;      // (kernel, device, smem, cluster)
+std::map<int, void*> g_static_scratch;                                 // device -> scratch address
 }  // namespace
 
 cudaError_t set_smem_limit(const void* kernel, int bytes) {
@@ -297,6 +303,33 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
 
 namespace {
 
+// Locates this device's static scratch on first use (cudaGetSymbolAddress)
+// and clears it once; later calls reuse the address.
+convrot_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto it = g_static_scratch.find(dev);
+  if (it != g_static_scratch.end()) {
+    *out = it->second;
+    return ok();
+  }
+  void* p = nullptr;
+  size_t bytes = 0;
+  e = cudaGetSymbolAddress(&p, g_static_gemm_scratch);
+  if (e == cudaSuccess) e = cudaGetSymbolSize(&bytes, g_static_gemm_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "locating the static GEMM scratch");
+  if (bytes < static_cast<size_t>(CONVROT_GEMM_WORKSPACE_BYTES))
+    return fail(CONVROT_ERR_INVALID_ARG, "static GEMM scratch is %zu bytes, below the workspace size", bytes);
+  e = cudaMemset(p, 0, bytes);  // what the split kernels expect to find zero
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static GEMM scratch");
+  g_static_scratch[dev] = p;
+  *out = p;
+  return ok();
+}
+
 convrot_status check_workspace(const void* ws, int64_t ws_bytes) {
   if (!ws) return ok();
   if (!aligned(ws, 256)) return fail(CONVROT_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
@@ -371,6 +404,15 @@ convrot_status convrot_linear_multi_ws(const convrot_packed_act* a, int32_t n, c
   return linear_multi(a, n, w, bias, Y, ldy, workspace, workspace_bytes, stream);
 }
 
+convrot_status convrot_linear_multi_static(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                                           const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
+                                           cudaStream_t stream) {
+  void* ws = nullptr;
+  convrot_status s = static_scratch(&ws);
+  if (s != CONVROT_OK) return s;
+  return linear_multi(a, n, w, bias, Y, ldy, ws, CONVROT_GEMM_WORKSPACE_BYTES, stream);
+}
+
 convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
                                 int64_t lda, cudaStream_t stream) {
   return gemm_s32(a, w, A, lda, nullptr, 0, stream);
@@ -388,6 +430,18 @@ convrot_status convrot_get_device_status(void) {
                   status_word_gemm_small(), status_word_hmatmul(), status_word_api()};
   for (int w : words) {
     if (w != 0) {
+      if (w == CONVROT_ERR_TIMEOUT) {
+        // an aborted split may have left partial sums in the static scratch
+        int dev = 0;
+        void* p = nullptr;
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+          std::lock_guard<std::mutex> lock(g_cache_mu);
+          auto it = g_static_scratch.find(dev);
+          if (it != g_static_scratch.end()) p = it->second;
+        }
+        if (p && (cudaMemset(p, 0, CONVROT_GEMM_WORKSPACE_BYTES) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
+          return cuda_fail(cudaGetLastError(), "clearing the static GEMM scratch");
+      }
       return fail(static_cast<convrot_status>(w), "a kernel recorded status %d (%s)", w,
                   convrot_status_str(static_cast<convrot_status>(w)));
     }

@@ -733,6 +733,9 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const SplitPlan sp = plan_split(tiles, clusters, K / BK, BN, CL, ws ? ws_bytes : 0);
+  // oversize guard: the split's counters and sums must fit the workspace
+  if (sp.sk_tiles && kWsCounterBytes + static_cast<long long>(sp.sk_tiles) * CL * BM * BN * 4 > ws_bytes)
+    return cudaErrorInvalidValue;
   p.dp_tiles = sp.dp_tiles;
   p.sk_tiles = sp.sk_tiles;
   p.sk_pieces = sp.pieces;
