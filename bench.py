@@ -42,6 +42,31 @@ L2_FLUSH_BYTES = 256 << 20
 # kernels, not the host's launch latency.
 PRE_STEP_SLEEP_CYCLES = 300_000
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the step's dominant kernel, from one ncu capture of `bench.py --profile` on
+# GB300 (summaries in profiles/), keyed by kernel and workload, with the
+# SHA-256 of the kernel's source file at capture time: once the source has
+# changed the figure no longer applies and the line reports null.
+NCU_TRAFFIC = {
+    ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
+        "bytes": 253_280_000 + 42_949_376,
+        "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
+        "sha256": "23ddf7973a17f4856e4a2c95047db887fd188e7032c39409961ab57592f72c95",
+    },
+}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    import hashlib
+    rec = NCU_TRAFFIC.get((kernel, workload))
+    if rec is None:
+        return None
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+            return None
+    return rec["bytes"]
+
+
 WORKLOADS = {
     "dit6144": lambda: WL.dit6144(),
     "qkv32700": lambda: WL.qkv32700(),
@@ -338,7 +363,7 @@ def gpu_main(args, world, rank, local):
     if use_f16:
         dominant = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": gemm_tflops,
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
-                    "traffic": None,
+                    "traffic": ncu_traffic("gemm_tc_kernel", wl.name),
                     "peak_note": f"{pk['source']} bf16 dense burst; the fp16 tensor rate is the same (nominal ratio 1)"}
     else:
         w_bytes = sum(n * K + 4 * n for n in Ns) + M * K + 4 * M + 2 * M * sum(Ns)
@@ -406,7 +431,7 @@ def gpu_main(args, world, rank, local):
                    "seed": wl.seed, "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
                    "inputs": wl.description, "gemm_path": "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)"},
         "roofline": dominant,
-        "rotate_quant": {"kernel": "rq_fast_kernel" if wl.transform == "h4" else "rq_generic_kernel",
+        "rotate_quant": {"kernel": "rq_lane_kernel" if wl.transform == "h4" else "rq_generic_kernel",
                          "us": quant_only_s * 1e6, "gbs": quant_gbs, "peak_gbs": pk["hbm_gbs"],
                          "frac": quant_gbs / pk["hbm_gbs"], "algorithmic_bytes": q_bytes,
                          "note": "int8 codes + scales only; in the step the kernel also writes the fp16 operand copy",
