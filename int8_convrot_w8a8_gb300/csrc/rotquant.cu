@@ -148,13 +148,36 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
 //  Quantize straight from registers: codes leave as 32-byte stores (16-byte
 //    after the quad transpose), fp16 copies as 32-byte stores: whole sectors.
 
-template <int G>
+// T: the transform; G: the group (regular Hadamard) or block (randomized
+// Hadamard) size; the naive variant takes G = 1.
+template <int T, int G>
 struct LaneCfg {
-  static constexpr int N = ilog4_c(G);
-  static constexpr int NIN = N < 3 ? N : 3;  // digits inside a 64-element line
-  static constexpr int NX = N - NIN;         // digits across lanes
-  static_assert(NX <= 2, "G <= 1024");
+  static constexpr bool H4 = T == CONVROT_T_REGULAR_H4;
+  static constexpr bool RHT = T == CONVROT_T_RHT;
+  // regular Hadamard: radix-4 digits inside a 64-element line, then across lanes
+  static constexpr int N = H4 ? ilog4_c(G) : 0;
+  static constexpr int NIN = N < 3 ? N : 3;
+  static constexpr int NX = N - NIN;
+  // randomized Hadamard: radix-2 stages inside a line, then across lanes
+  static constexpr int NB = RHT ? ilog2_c(G) : 0;
+  static constexpr int NBIN = NB < 6 ? NB : 6;
+  static constexpr int NBX = NB - NBIN;
+  // line positions with distinct sign patterns (randomized Hadamard)
+  static constexpr int NPOS = RHT && G > 64 ? G / 64 : 1;
+  static_assert(NX <= 2 && NBX <= 2, "G <= 1024 (regular) or B <= 256 (randomized)");
 };
+
+// One radix-2 Walsh-Hadamard stage across lanes (partner lane ^ MASK): the
+// lower lane of the pair gets a + b, the upper one a - b (a the lower value),
+// the same single roundings as the stage done in one place.
+template <int MASK>
+__device__ __forceinline__ float2 wht_xlane(float2 x, int lane) {
+  float2 t;
+  t.x = __shfl_xor_sync(0xffffffffu, x.x, MASK);
+  t.y = __shfl_xor_sync(0xffffffffu, x.y, MASK);
+  const float sg = (lane & MASK) ? -1.0f : 1.0f;
+  return make_float2(fmaf(sg, x.x, t.x), fmaf(sg, x.y, t.y));
+}
 
 // One radix-4 stage, unnormalized, on lanes: this lane holds digit value
 // a = (lane >> shift) & 3 of the quad it exchanges with.
@@ -171,12 +194,13 @@ __device__ __forceinline__ float2 h4_xlane(float2 x) {
   return f2_add(u, w);
 }
 
-template <int G>
+template <int T, int G>
 __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CUtensorMap xmap, long long M, int K,
-                                                       int R, int NT, int8_t* __restrict__ Q, float* __restrict__ S,
+                                                       int R, int NT, const int8_t* __restrict__ signs,
+                                                       int8_t* __restrict__ Q, float* __restrict__ S,
                                                        __half* __restrict__ Q16, float s_div, int stage_bytes,
                                                        int tbytes, long long spin_limit) {
-  using C = LaneCfg<G>;
+  using C = LaneCfg<T, G>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,6 +208,10 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   const uint32_t tbuf = stage_base + 2 * stage_bytes;  // fp32 quad-transpose buffer (G >= 256)
   unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(smem + 2 * stage_bytes + tbytes);  // [3][R]
   uint64_t* bar = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));         // [2]
+  // randomized Hadamard: per line position, 32 words that flip the sign bits
+  // of the packed bf16 pairs (bit 15: element 2k, bit 31: element 2k + 1)
+  uint32_t* sign_tab =
+      reinterpret_cast<uint32_t*>((reinterpret_cast<uintptr_t>(bar + 2) + 15) & ~uintptr_t(15));  // [NPOS][32]
 
   const int tid = threadIdx.x, lane = tid & 31;
   const bool active = tid < NT;
@@ -226,7 +254,15 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   // thread has passed the barrier of iteration it - 1, so every thread has
   // finished reading it.
   for (int i = tid; i < 3 * R; i += blockDim.x) rowmax_buf[i] = 0u;
+  if constexpr (C::RHT) {
+    for (int i = tid; i < C::NPOS * 32; i += blockDim.x) {
+      const int e = ((i >> 5) * 64 + 2 * (i & 31)) & (G - 1);  // element of the block
+      sign_tab[i] = (signs[e] < 0 ? 0x8000u : 0u) | (signs[(e + 1) & (G - 1)] < 0 ? 0x80000000u : 0u);
+    }
+  }
   __syncthreads();
+  // the line position of this thread in its block (its lines are fixed)
+  const uint32_t my_signs = smem_u32(sign_tab) + static_cast<uint32_t>(((tid % lines_per_row) % C::NPOS) * 128);
 
   long long tile = blockIdx.x;
   if (tid == 0 && tile < ntiles) {
@@ -257,6 +293,16 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
         if (active) {
           const uint32_t addr = lb + ((k ^ (tid & 7)) << 4);
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
+          if constexpr (C::RHT) {
+            uint32_t m0, m1, m2, m3;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
+                         : "r"(my_signs + 16 * k));
+            w0 ^= m0;
+            w1 ^= m1;
+            w2 ^= m2;
+            w3 ^= m3;
+          }
         }
         v[4 * k + 0] = make_float2(bf16lo_f32(w0), bf16hi_f32(w0));
         v[4 * k + 1] = make_float2(bf16lo_f32(w1), bf16hi_f32(w1));
@@ -310,6 +356,38 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
     if constexpr (C::NX >= 2) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = h4_xlane<2>(v[i]);
+    }
+
+    // ---- randomized Hadamard: radix-2 stages, stride 1 first (in the pair),
+    // strides 2..32 across pairs (packed), 64 and 128 across lanes
+    if constexpr (C::NBIN >= 1) {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const float a = v[q].x, b = v[q].y;
+        v[q] = make_float2(a + b, a - b);
+      }
+    }
+#pragma unroll
+    for (int st = 1; st < 6; ++st) {
+      if (st < C::NBIN) {
+        const int d = 1 << (st - 1);  // pair distance
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          if ((q & d) == 0) {
+            const float2 a = v[q], b = v[q + d];
+            v[q] = f2_add(a, b);
+            v[q + d] = f2_sub(a, b);
+          }
+        }
+      }
+    }
+    if constexpr (C::NBX >= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = wht_xlane<1>(v[i], lane);
+    }
+    if constexpr (C::NBX >= 2) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = wht_xlane<2>(v[i], lane);
     }
 
     // ---- row absmax
@@ -443,9 +521,9 @@ static bool choose_rows(int K, int ept, bool phase_c, int* R_out, int* NT_out) {
   return true;
 }
 
-template <int G>
-static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
-                               __half* Q16, cudaStream_t st, bool* launched) {
+template <int T, int G>
+static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, const int8_t* signs,
+                               int8_t* Q, float* S, __half* Q16, cudaStream_t st, bool* launched) {
   *launched = false;
   if (K % 64 != 0 || K / 64 > 256 || M > 0x7fffffffLL) return cudaSuccess;
   int R = 0, NT = 0;
@@ -465,9 +543,9 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   const int threads = (NT + 31) / 32 * 32;
   const int stage_bytes = ((R * K * 2 + 1023) / 1024) * 1024;
   // the quad transpose needs 256 bytes per thread (one fp32 line)
-  const int tbytes = LaneCfg<G>::NX >= 1 ? threads * 256 : 0;
-  const int smem = 1024 + 2 * stage_bytes + tbytes + ((3 * R + 1) & ~1) * 4 + 2 * 8;
-  auto kern = rq_lane_kernel<G>;
+  const int tbytes = LaneCfg<T, G>::NX >= 1 ? threads * 256 : 0;
+  const int smem = 1024 + 2 * stage_bytes + tbytes + ((3 * R + 1) & ~1) * 4 + 2 * 8 + 16 + LaneCfg<T, G>::NPOS * 128;
+  auto kern = rq_lane_kernel<T, G>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -480,9 +558,9 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   const long long slots = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
   const long long rounds = (tiles + slots - 1) / slots;
   const long long grid = (tiles + rounds - 1) / rounds;
-  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, Q, S, Q16,
-                                                             scale_divisor(CONVROT_T_REGULAR_H4, G), stage_bytes,
-                                                             tbytes, kDefaultSpinLimit);
+  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, signs, Q, S, Q16,
+                                                             scale_divisor(T, G), stage_bytes, tbytes,
+                                                             kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
 }
@@ -500,18 +578,34 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
   const bool aligned32 = (reinterpret_cast<uintptr_t>(X) % 16 == 0) && (ldx % 8 == 0) &&
                          (reinterpret_cast<uintptr_t>(Q) % 32 == 0) &&
                          (Q16 == nullptr || reinterpret_cast<uintptr_t>(Q16) % 32 == 0);
-  if (!force_generic && in_dtype == CONVROT_DTYPE_BF16 && transform == CONVROT_T_REGULAR_H4 && aligned32 &&
-      K % 16 == 0) {
+  if (!force_generic && in_dtype == CONVROT_DTYPE_BF16 && aligned32 && K % 16 == 0) {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
     bool launched = false;
     cudaError_t e = cudaSuccess;
-    switch (G) {
-      case 4: e = launch_lane<4>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 16: e = launch_lane<16>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 64: e = launch_lane<64>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 256: e = launch_lane<256>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 1024: e = launch_lane<1024>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      default: break;
+    constexpr int H4 = CONVROT_T_REGULAR_H4, RHT = CONVROT_T_RHT;
+    if (transform == H4) {
+      switch (G) {
+        case 4: e = launch_lane<H4, 4>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 16: e = launch_lane<H4, 16>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 64: e = launch_lane<H4, 64>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 256: e = launch_lane<H4, 256>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 1024: e = launch_lane<H4, 1024>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        default: break;
+      }
+    } else if (transform == RHT) {
+      switch (G) {
+        case 2: e = launch_lane<RHT, 2>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 4: e = launch_lane<RHT, 4>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 8: e = launch_lane<RHT, 8>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 16: e = launch_lane<RHT, 16>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 32: e = launch_lane<RHT, 32>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 64: e = launch_lane<RHT, 64>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 128: e = launch_lane<RHT, 128>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        case 256: e = launch_lane<RHT, 256>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
+        default: break;
+      }
+    } else {
+      e = launch_lane<CONVROT_T_NONE, 1>(xb, M, K, ldx, signs, Q, S, q16, st, &launched);
     }
     if (e != cudaSuccess) return e;
     if (launched) {

@@ -123,6 +123,50 @@ def test_quantize_act_rht_matches_oracle(cr, M, K, B):
     check_scales(to_np(a.scale), s, f"rht B{B}")
 
 
+def _fast_and_generic(cr, X, G, transform, signs=None):
+    """The same call twice: outputs 32-byte aligned (register kernel) and at a
+    16- but not 32-byte aligned address (generic kernel)."""
+    M, K = X.shape
+    fast = cr.convrot_quantize_act(X, G, transform, signs)
+    qbuf = torch.empty(M * K + 16, dtype=torch.int8, device="cuda")
+    hbuf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
+    q_un, h_un = qbuf[16:].view(M, K), hbuf[8:].view(M, K)
+    assert q_un.data_ptr() % 32 == 16 and h_un.data_ptr() % 32 == 16
+    out = cr.PackedAct(q_un, torch.empty(M, dtype=torch.float32, device="cuda"), h_un, G, cr.TRANSFORMS[transform])
+    gen = cr.convrot_quantize_act(X, G, transform, signs, out=out)
+    torch.cuda.synchronize()
+    return fast, gen
+
+
+@pytest.mark.parametrize("M,K,B", [(37, 1152, 2), (37, 1152, 8), (37, 1152, 32), (37, 1152, 64),
+                                   (37, 1152, 128), (37, 2048, 256), (300, 4096, 256), (1, 256, 256)])
+def test_quantize_act_rht_register_kernel(cr, M, K, B):
+    """Block randomized Hadamard on the register kernel (signs applied to the
+    bf16 bits, radix-2 stages in registers and across lanes): codes and
+    scales against the oracle, and bit-identical to the generic kernel."""
+    wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.002, outlier_scale=40.0, group=B,
+                      transform="rht", seed=3 * B + M)
+    X, sg = wl.X.cuda(), wl.signs.cuda()
+    fast, gen = _fast_and_generic(cr, X, B, "rht", sg)
+    Q, s, v = _oracle_act(wl.X, B, "rht", wl.signs)
+    check_codes(to_np(fast.q), Q, v, f"rht B{B}")
+    check_scales(to_np(fast.scale), s, f"rht B{B}")
+    assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
+    assert torch.equal(fast.q_f16.float(), fast.q.float())
+
+
+@pytest.mark.parametrize("M,K", [(21, 1152), (300, 6144), (5, 64)])
+def test_quantize_act_none_register_kernel(cr, M, K):
+    """The naive variant (no rotation) on the register kernel: against the
+    oracle and bit-identical to the generic kernel."""
+    wl = WL.make_case(M, K, [], seed=M + K)
+    fast, gen = _fast_and_generic(cr, wl.X.cuda(), 0, "none")
+    Q, s, v = _oracle_act(wl.X, 0, "none")
+    check_codes(to_np(fast.q), Q, v, "none")
+    check_scales(to_np(fast.scale), s, "none")
+    assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
+
+
 def test_quantize_act_none_matches_oracle(cr):
     wl = WL.make_case(21, 1152, [], seed=14)
     a = _run_act(cr, wl.X, 0, "none")
