@@ -69,6 +69,9 @@ def ncu_traffic(kernel: str, workload: str):
 
 WORKLOADS = {
     "dit6144": lambda: WL.dit6144(),
+    "dit6144_rht128": lambda: WL.dit6144_variant("rht", 128),
+    "dit6144_rht256": lambda: WL.dit6144_variant("rht", 256),
+    "dit6144_none": lambda: WL.dit6144_variant("none", 0),
     "qkv32700": lambda: WL.qkv32700(),
     "qkv32700_cat": lambda: _concat(WL.qkv32700()),
     "ffn_pair": lambda: WL.ffn_pair(),
@@ -79,6 +82,18 @@ WORKLOADS = {
     "k2688": lambda: WL.k2688(),
     "tiny": lambda: WL.tiny(),
 }
+
+
+def rq_kernel_name(wl) -> str:
+    """The rotate+quantize kernel the library picks for this workload (bf16,
+    aligned torch buffers, K a multiple of 64)."""
+    lane = (wl.K % 64 == 0 and K_LANE_MAX >= wl.K and
+            ((wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)) or
+             (wl.transform == "rht" and 2 <= wl.group <= 256) or wl.transform == "none"))
+    return "rq_lane_kernel" if lane else "rq_generic_kernel"
+
+
+K_LANE_MAX = 64 * 256  # the register kernel takes rows of up to 256 lines
 
 
 def _concat(wl):
@@ -431,7 +446,7 @@ def gpu_main(args, world, rank, local):
                    "seed": wl.seed, "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
                    "inputs": wl.description, "gemm_path": "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)"},
         "roofline": dominant,
-        "rotate_quant": {"kernel": "rq_lane_kernel" if wl.transform == "h4" else "rq_generic_kernel",
+        "rotate_quant": {"kernel": rq_kernel_name(wl),
                          "us": quant_only_s * 1e6, "gbs": quant_gbs, "peak_gbs": pk["hbm_gbs"],
                          "frac": quant_gbs / pk["hbm_gbs"], "algorithmic_bytes": q_bytes,
                          "note": "int8 codes + scales only; in the step the kernel also writes the fp16 operand copy",

@@ -140,6 +140,17 @@ def dit6144(seed: int = 1, M: int = 4096) -> Workload:
     return w
 
 
+def dit6144_variant(transform: str, group: int, seed: int = 1, M: int = 4096) -> Workload:
+    """The DiT linear's inputs (same seed, so the same X, W and bias) under
+    another rotation: the block randomized Hadamard or none (naive W8A8)."""
+    w = make_case(M, 6144, [6144], dist="t3", outlier_frac=0.001,
+                  outlier_scale=50.0, group=group, transform=transform, seed=seed,
+                  name=f"dit_linear_{M}x6144x6144_{transform.upper()}{group if transform != 'none' else ''}")
+    w.description = ("X bf16 [M,6144] Student-t(3), 0.1% channels x50; "
+                     f"W [6144,6144] ~N(0,0.02^2); bias ~N(0,0.01^2); {transform} {group}")
+    return w
+
+
 def qkv32700(seed: int = 2, M: int = 32700) -> Workload:
     w = make_case(M, 3072, [3072, 3072, 3072], dist="t3", outlier_frac=0.001,
                   outlier_scale=50.0, group=256, seed=seed,
