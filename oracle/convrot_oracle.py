@@ -31,6 +31,13 @@ Readings where the pages are silent (each is also listed in the design notes):
 * The Walsh-Hadamard matrix is in natural (Sylvester) order.
 * Y is reconstructed in fp64 from the stored fp32 scales and rounded once to
   bf16, round-to-nearest-even.
+* 4-bit ConvRot ("feat: load ConvRot int4 and per-channel int8 safetensors",
+  sections "Solution" and "The rotation"): codes in [-7, 7] with one fp32
+  scale per output channel, adjacent pairs packed in a byte. The pages do not
+  say which nibble holds the first element nor how the 4-bit activations are
+  scaled: element 2j goes to the low nibble as a two's-complement nibble, and
+  activations use the int8 recipe with 7 in place of 127 (s = max|x_rot|/7,
+  q = clamp(round(x_rot/s), -7, 7)).
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against what the
 pages and the mathematics fix: the printed H4, closed forms of R, basis
@@ -46,7 +53,7 @@ __all__ = [
     "sylvester_hadamard", "rht_block", "row_operator", "rotate_rows",
     "quantize_rows", "prepare_weights", "quantize_act", "int_gemm",
     "reconstruct", "round_to_bf16", "linear", "float_linear",
-    "boundary_distance",
+    "boundary_distance", "QMAX4", "pack_int4", "unpack_int4",
 ]
 
 # "INT8 Convrot Safetensors", "How INT8 convrot works": the printed matrix,
@@ -59,6 +66,7 @@ H4 = np.array([[1.0, 1.0, 1.0, -1.0],
 TRANSFORMS = ("h4", "rht", "none")
 
 QMAX = 127  # "clamp(round(...), -127, 127)" in both quantization sections
+QMAX4 = 7   # 4-bit ConvRot: "int4 values occupy [-7,7]"
 
 
 def log4(G: int) -> int:
@@ -159,43 +167,67 @@ def rotate_rows(X, G: int, transform: str = "h4", signs=None) -> np.ndarray:
     return (X.reshape(rows, K // G, G) @ T).reshape(rows, K)
 
 
-def quantize_rows(Xrot):
-    """Per-row symmetric int8 quantization of an already rotated matrix.
+def quantize_rows(Xrot, qmax: int = QMAX):
+    """Per-row symmetric quantization of an already rotated matrix.
 
     "Weight quantization" / "Runtime activation quantization":
         s[r]    = max_i |X_rot[r, i]| / 127
         Q[r, i] = clamp(round(X_rot[r, i] / s[r]), -127, 127)
+    and the same with 7 for the 4-bit codes (qmax = QMAX4).
 
     Returns (Q int8, s float32 as stored, v = X_rot / s in fp64 before
     rounding, s in fp64). A zero row gets s = 0 and Q = 0.
     """
     Xrot = np.asarray(Xrot, dtype=np.float64)
     amax = np.abs(Xrot).max(axis=1) if Xrot.shape[1] else np.zeros(Xrot.shape[0])
-    s64 = amax / QMAX
+    s64 = amax / qmax
     safe = np.where(s64 > 0, s64, 1.0)
     v = np.where(s64[:, None] > 0, Xrot / safe[:, None], 0.0)
-    Q = np.clip(np.rint(v), -QMAX, QMAX).astype(np.int8)
+    Q = np.clip(np.rint(v), -qmax, qmax).astype(np.int8)
     return Q, s64.astype(np.float32), v, s64
 
 
-def prepare_weights(W, G: int, transform: str = "h4", signs=None):
-    """Offline weight path: W_rot = W R per K-group, then per-output-row int8.
+def prepare_weights(W, G: int, transform: str = "h4", signs=None, qmax: int = QMAX):
+    """Offline weight path: W_rot = W R per K-group, then per-output-row codes.
 
     "How INT8 convrot works" (W_rot = W R) and "Weight quantization".
     Returns (Q_w int8 [N,K], s_w float32 [N], v fp64 [N,K]).
     """
-    Q, s, v, _ = quantize_rows(rotate_rows(W, G, transform, signs))
+    Q, s, v, _ = quantize_rows(rotate_rows(W, G, transform, signs), qmax)
     return Q, s, v
 
 
-def quantize_act(X, G: int, transform: str = "h4", signs=None):
+def quantize_act(X, G: int, transform: str = "h4", signs=None, qmax: int = QMAX):
     """Runtime activation path: X_rot = X R, then one dynamic scale per row.
 
     "Runtime activation quantization". The packed activation is the pair
     (Q_x, s_x). Returns (Q_x int8 [M,K], s_x float32 [M], v fp64 [M,K]).
     """
-    Q, s, v, _ = quantize_rows(rotate_rows(X, G, transform, signs))
+    Q, s, v, _ = quantize_rows(rotate_rows(X, G, transform, signs), qmax)
     return Q, s, v
+
+
+def pack_int4(Q) -> np.ndarray:
+    """4-bit codes in [-7, 7], two per byte: element 2j in the low nibble,
+    2j + 1 in the high nibble, each as a two's-complement nibble."""
+    Q = np.asarray(Q)
+    if Q.shape[-1] % 2 or np.abs(Q.astype(np.int64)).max(initial=0) > QMAX4:
+        raise ValueError("need an even row length and codes in [-7, 7]")
+    lo = Q[..., 0::2].astype(np.int64) & 0xF
+    hi = Q[..., 1::2].astype(np.int64) & 0xF
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def unpack_int4(P) -> np.ndarray:
+    """Inverse of pack_int4: bytes -> int8 codes, sign-extended nibbles."""
+    P = np.asarray(P, dtype=np.uint8).astype(np.int64)
+    lo, hi = P & 0xF, (P >> 4) & 0xF
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    out = np.empty(P.shape[:-1] + (2 * P.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
 
 
 def int_gemm(Qx, Qw) -> np.ndarray:
@@ -240,13 +272,13 @@ def round_to_bf16(Y) -> np.ndarray:
     return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
-def linear(X, Qw, sw, bias, G: int, transform: str = "h4", signs=None):
+def linear(X, Qw, sw, bias, G: int, transform: str = "h4", signs=None, qmax: int = QMAX):
     """The whole runtime path for one linear: rotate, quantize, GEMM, reconstruct.
 
     Returns a dict with Qx, sx, v (pre-rounding activation codes), A (int64),
     Y64 (fp64) and Y (bf16 values as fp64).
     """
-    Qx, sx, v = quantize_act(X, G, transform, signs)
+    Qx, sx, v = quantize_act(X, G, transform, signs, qmax)
     A = int_gemm(Qx, Qw)
     Y64 = reconstruct(A, sx, sw, bias)
     return {"Qx": Qx, "sx": sx, "v": v, "A": A, "Y64": Y64, "Y": round_to_bf16(Y64)}

@@ -43,6 +43,8 @@ def load_quantizer_rows():
             if not line or line.startswith("#"):
                 continue
             tag, *vals = line.split()
+            if tag == "row4":  # a 4-bit row: codes in [-7, 7]
+                tag, cur["qmax"] = "row", 7
             cur[tag] = [float(v) for v in vals]
             if tag == "s":
                 cases.append(cur)
@@ -77,7 +79,10 @@ def pin_orthogonal_symmetric(R, tol=1e-12):
 
 def pin_quantizer_rows(quantize_rows):
     for case in load_quantizer_rows():
-        Q, s, v, _ = quantize_rows(np.array([case["row"]]))
+        if "qmax" in case:
+            Q, s, v, _ = quantize_rows(np.array([case["row"]]), case["qmax"])
+        else:
+            Q, s, v, _ = quantize_rows(np.array([case["row"]]))
         if not (np.array_equal(Q[0].astype(np.int64), np.array(case["q"], dtype=np.int64))
                 and float(s[0]) == case["s"][0]):
             return False
@@ -388,3 +393,60 @@ def test_planted_dropped_term_in_gemm_is_caught():
     brute = np.array([[sum(int(Qx[r, i]) * int(Qw[o, i]) for i in range(40)) for o in range(2)]
                       for r in range(3)])
     assert np.array_equal(good, brute) and not np.array_equal(bad, brute)
+
+
+# ------------------------------------------------------------ 4-bit codes --
+# "feat: load ConvRot int4 and per-channel int8 safetensors", "Solution":
+# int4 values occupy [-7, 7], adjacent pairs packed in a byte (nibble order
+# and two's-complement nibbles are this build's reading, pinned here).
+
+def pin_int4_bytes(pack):
+    # codes (1, -1) -> low nibble 0x1, high nibble 0xF; (7, -7) -> 0x7, 0x9;
+    # (0, 3) -> 0x0, 0x3; (-4, 5) -> 0xC, 0x5
+    got = pack(np.array([[1, -1, 7, -7, 0, 3, -4, 5]], dtype=np.int8))
+    return np.array_equal(got, np.array([[0xF1, 0x97, 0x30, 0x5C]], dtype=np.uint8))
+
+
+def test_int4_packing_hand_bytes():
+    assert pin_int4_bytes(O.pack_int4)
+
+
+def test_int4_pack_round_trip_and_range():
+    rng = np.random.default_rng(4)
+    Q = rng.integers(-7, 8, size=(5, 64)).astype(np.int8)
+    P = O.pack_int4(Q)
+    assert P.shape == (5, 32) and P.dtype == np.uint8
+    assert np.array_equal(O.unpack_int4(P), Q)
+    with pytest.raises(ValueError):
+        O.pack_int4(np.array([[8, 0]], dtype=np.int8))
+    with pytest.raises(ValueError):
+        O.pack_int4(np.array([[1, 2, 3]], dtype=np.int8))
+
+
+def test_4bit_quantizer_range_and_scale():
+    """Every 4-bit code is within [-7, 7]; the largest |x_rot| of a row maps to
+    exactly +-7; a basis vector in a G = 256 group maps to +-7 everywhere."""
+    rng = np.random.default_rng(5)
+    X = rng.standard_t(3, size=(9, 1024))
+    Q, s, v = O.quantize_act(X, 256, "h4", qmax=O.QMAX4)
+    assert np.abs(Q).max() == 7 and np.all(np.abs(Q).max(axis=1) == 7)
+    Xr = O.rotate_rows(X, 256, "h4")
+    assert np.allclose(s, np.abs(Xr).max(axis=1) / 7, rtol=1e-7)
+    e = np.zeros((1, 256))
+    e[0, 17] = 3.0
+    Qe, _, _ = O.quantize_act(e, 256, "h4", qmax=O.QMAX4)
+    assert np.all(np.abs(Qe) == 7)
+
+
+def test_planted_int4_nibble_swap_is_caught():
+    def swapped(Q):
+        Q = np.asarray(Q)
+        return ((Q[..., 1::2].astype(np.int64) & 0xF) | ((Q[..., 0::2].astype(np.int64) & 0xF) << 4)).astype(np.uint8)
+    assert not pin_int4_bytes(swapped)
+
+
+def test_planted_int4_offset_binary_is_caught():
+    def biased(Q):  # +8 offset nibbles instead of two's complement
+        Q = np.asarray(Q).astype(np.int64) + 8
+        return (Q[..., 0::2] | (Q[..., 1::2] << 4)).astype(np.uint8)
+    assert not pin_int4_bytes(biased)
