@@ -72,6 +72,9 @@ WORKLOADS = {
     "dit6144_rht128": lambda: WL.dit6144_variant("rht", 128),
     "dit6144_rht256": lambda: WL.dit6144_variant("rht", 256),
     "dit6144_none": lambda: WL.dit6144_variant("none", 0),
+    "dit6144_w4": lambda: _w4(WL.dit6144()),
+    "qkv32700_w4": lambda: _w4(WL.qkv32700()),
+    "gsweep256_w4": lambda: _w4(WL.gsweep(256)),
     "qkv32700": lambda: WL.qkv32700(),
     "qkv32700_cat": lambda: _concat(WL.qkv32700()),
     "ffn_pair": lambda: WL.ffn_pair(),
@@ -94,6 +97,13 @@ def rq_kernel_name(wl) -> str:
 
 
 K_LANE_MAX = 64 * 256  # the register kernel takes rows of up to 256 lines
+
+
+def _w4(wl):
+    """The same inputs through the 4-bit ConvRot path (codes in [-7, 7])."""
+    wl.bits = 4
+    wl.name = wl.name + "_W4A4"
+    return wl
 
 
 def _concat(wl):
@@ -214,12 +224,13 @@ def oracle_sample(wl, rows: int, seed: int = 0):
     """Times the CPU oracle on a seeded sample of `rows` rows (full K, all N)."""
     import oracle as O
     sg = None if wl.signs is None else wl.signs.numpy()
-    Ws = [O.prepare_weights(W.numpy().astype(np.float64), wl.group, wl.transform, sg) for W in wl.weights]
+    qmax = O.QMAX4 if getattr(wl, "bits", 8) == 4 else O.QMAX
+    Ws = [O.prepare_weights(W.numpy().astype(np.float64), wl.group, wl.transform, sg, qmax) for W in wl.weights]
     rng = np.random.default_rng(seed)
     idx = np.sort(rng.choice(wl.M, size=min(rows, wl.M), replace=False))
     X64 = wl.X[torch.from_numpy(idx)].float().numpy().astype(np.float64)
     t0 = time.perf_counter()
-    Qx, sx, _ = O.quantize_act(X64, wl.group, wl.transform, sg)
+    Qx, sx, _ = O.quantize_act(X64, wl.group, wl.transform, sg, qmax)
     t1 = time.perf_counter()
     for (Qw, sw, _), b in zip(Ws, wl.biases):
         O.round_to_bf16(O.reconstruct(O.int_gemm(Qx, Qw), sx, sw, b.numpy()))
@@ -262,12 +273,33 @@ def gpu_main(args, world, rank, local):
     wl = WORKLOADS[args.workload]()
     stream = torch.cuda.current_stream()
     sg = None if wl.signs is None else wl.signs.to(dev)
-    use_f16 = wl.M > 64
-    ws = [cr.convrot_prepare_weights(W.to(dev), wl.group, wl.transform, sg, with_f16=use_f16) for W in wl.weights]
+    bits = getattr(wl, "bits", 8)
+    # the tensor-core operand copies: fp16 (8-bit codes, M > 64) or e4m3 (4-bit codes, always)
+    use_f16 = wl.M > 64 or bits == 4
+    if bits == 4:
+        def quant(Xq, with_f16, out=None, stream=None):
+            return cr.convrot_quantize_act4(Xq, wl.group, wl.transform, sg, with_f8=with_f16, out=out, stream=stream)
+
+        def lin(a, outs_, workspace, stream=None):
+            cr.convrot_linear4_multi(a, ws, bs, outs=outs_, stream=stream, workspace=workspace)
+
+        ws = [cr.convrot_prepare_weights4(W.to(dev), wl.group, wl.transform, sg) for W in wl.weights]
+    else:
+        def quant(Xq, with_f16, out=None, stream=None):
+            return cr.convrot_quantize_act(Xq, wl.group, wl.transform, sg, with_f16=with_f16, out=out, stream=stream)
+
+        def lin(a, outs_, workspace, stream=None):
+            if len(ws) == 1:
+                cr.convrot_linear(a, ws[0], bs[0], out=outs_[0], stream=stream, workspace=workspace)
+            else:
+                cr.convrot_linear_multi(a, ws, bs, outs=outs_, stream=stream, workspace=workspace)
+
+        ws = [cr.convrot_prepare_weights(W.to(dev), wl.group, wl.transform, sg, with_f16=use_f16)
+              for W in wl.weights]
     bs = [b.to(dev) for b in wl.biases]
     X = wl.X.to(dev)
     M, K, Ns = wl.M, wl.K, wl.Ns
-    act = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16)
+    act = quant(X, use_f16)
     outs = [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
     gws = cr.gemm_workspace(dev)  # lets the GEMM split a mostly idle last round of tiles
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -281,12 +313,9 @@ def gpu_main(args, world, rank, local):
         torch.sum(flush_rd, dim=0, out=flush_sink)
 
     def step():
-        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16, out=act)
+        quant(X, use_f16, out=act)
         e_mid.record(stream)
-        if len(ws) == 1:
-            cr.convrot_linear(act, ws[0], bs[0], out=outs[0], workspace=gws)
-        else:
-            cr.convrot_linear_multi(act, ws, bs, outs=outs, workspace=gws)
+        lin(act, outs, gws)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -301,8 +330,8 @@ def gpu_main(args, world, rank, local):
         # rotate+quantize and (where supported) one matmul-form rotate+quantize
         e_mid = torch.cuda.Event(enable_timing=True)
         step()
-        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
-        if wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
+        quant(X, False)
+        if bits == 8 and wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
                 and K // max(wl.group, 64) <= 128:
             cr.convrot_quantize_act_hmatmul(X, wl.group, with_f16=False)
         torch.cuda.synchronize()
@@ -330,14 +359,14 @@ def gpu_main(args, world, rank, local):
         raise RuntimeError(f"device status {status} after the timed region")
     # the rotate+quantize contract alone (bf16 in, int8 codes + fp32 scales out,
     # no fp16 operand copy), timed on its own for the GB/s figure
-    act8 = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
+    act8 = quant(X, False)
     q_only_ms = []
     for i in range(args.warmup + args.steps):
         flush_l2()
         torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
-        cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False, out=act8)
+        quant(X, False, out=act8)
         b1.record(stream)
         if i >= args.warmup:
             q_only_ms.append((b0, b1))
@@ -345,7 +374,7 @@ def gpu_main(args, world, rank, local):
     q_only_ms = [b0.elapsed_time(b1) for b0, b1 in q_only_ms]
     # the same contract with the rotation applied as a dense tensor-core matmul
     hm_ms = None
-    if wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
+    if bits == 8 and wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
             and K // max(wl.group, 64) <= 128:
         hm_ms = []
         for i in range(args.warmup + args.steps):
@@ -371,11 +400,19 @@ def gpu_main(args, world, rank, local):
     quant_s = statistics.mean(quant_ms) / 1e3
     gemm_tflops = ops_step / gemm_s / 1e12
     # algorithmic bytes of rotate+quantize: bf16 in, int8 out, fp32 scales
-    q_bytes = 2 * M * K + M * K + 4 * M
-    q_bytes_f16 = q_bytes + 2 * M * K if use_f16 else q_bytes
+    # 4-bit codes are packed two per byte; their e4m3 copy is one byte per code
+    q_bytes = 2 * M * K + (M * K if bits == 8 else M * K // 2) + 4 * M
+    q_bytes_f16 = q_bytes + (2 if bits == 8 else 1) * M * K if use_f16 else q_bytes
     quant_only_s = statistics.mean(q_only_ms) / 1e3
     quant_gbs = q_bytes / quant_only_s / 1e9
-    if use_f16:
+    if bits == 4:
+        # e4m3 dense rate: the measured bf16 burst x the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        peak8 = 2.0 * pk["bf16_tflops"]
+        dominant = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": gemm_tflops,
+                    "peak": peak8, "unit": "TFLOP/s", "frac": gemm_tflops / peak8,
+                    "traffic": ncu_traffic("gemm_tc_kernel", wl.name),
+                    "peak_note": f"{pk['source']} bf16 dense burst x 2 (nominal fp8/bf16 ratio 4.5/2.25)"}
+    elif use_f16:
         dominant = {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": gemm_tflops,
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
                     "traffic": ncu_traffic("gemm_tc_kernel", wl.name),
@@ -399,7 +436,7 @@ def gpu_main(args, world, rank, local):
     for _ in range(nbuf):
         Xd = torch.empty_like(X)
         bufs.append({"X": Xd,
-                     "act": cr.convrot_quantize_act(Xd.zero_(), wl.group, wl.transform, sg, with_f16=use_f16),
+                     "act": quant(Xd.zero_(), use_f16),
                      "Y": [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns],
                      "ws": cr.gemm_workspace(dev),
                      "Yh": [torch.empty((M, n), dtype=torch.bfloat16).pin_memory() for n in Ns]})
@@ -408,11 +445,8 @@ def gpu_main(args, world, rank, local):
         b, s = bufs[i % nbuf], e2e_streams[i % nbuf]
         with torch.cuda.stream(s):
             b["X"].copy_(Xh, non_blocking=True)
-            cr.convrot_quantize_act(b["X"], wl.group, wl.transform, sg, with_f16=use_f16, out=b["act"], stream=s)
-            if len(ws) == 1:
-                cr.convrot_linear(b["act"], ws[0], bs[0], out=b["Y"][0], stream=s, workspace=b["ws"])
-            else:
-                cr.convrot_linear_multi(b["act"], ws, bs, outs=b["Y"], stream=s, workspace=b["ws"])
+            quant(b["X"], use_f16, out=b["act"], stream=s)
+            lin(b["act"], b["Y"], b["ws"], stream=s)
             for y, yh in zip(b["Y"], b["Yh"]):
                 yh.copy_(y, non_blocking=True)
 
@@ -441,15 +475,19 @@ def gpu_main(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if bits == 8 else "int4", "data": "synthetic",
         "config": {"workload": wl.name, "M": M, "K": K, "N": Ns, "group": wl.group, "transform": wl.transform,
                    "seed": wl.seed, "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
-                   "inputs": wl.description, "gemm_path": "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)"},
+                   "inputs": wl.description,
+                   "gemm_path": ("tcgen05 e4m3-exact (kind::f8f6f4)" if bits == 4 else
+                                 "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)")},
         "roofline": dominant,
         "rotate_quant": {"kernel": rq_kernel_name(wl),
                          "us": quant_only_s * 1e6, "gbs": quant_gbs, "peak_gbs": pk["hbm_gbs"],
                          "frac": quant_gbs / pk["hbm_gbs"], "algorithmic_bytes": q_bytes,
-                         "note": "int8 codes + scales only; in the step the kernel also writes the fp16 operand copy",
+                         "note": ("packed 4-bit codes + scales only; in the step the kernel also writes the e4m3 copy"
+                                  if bits == 4 else
+                                  "int8 codes + scales only; in the step the kernel also writes the fp16 operand copy"),
                          "in_step_us": quant_s * 1e6, "in_step_bytes": q_bytes_f16,
                          "in_step_gbs": q_bytes_f16 / quant_s / 1e9},
         "rotate_quant_hmatmul": None if hm_ms is None else {

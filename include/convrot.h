@@ -219,6 +219,67 @@ convrot_status convrot_linear_multi_static(const convrot_packed_act* a, int32_t 
                                            const convrot_packed_weight* w, const float* const* bias,
                                            uint16_t* const* Y, const int64_t* ldy, cudaStream_t stream);
 
+/* ---- 4-bit ConvRot (W4A4) -------------------------------------------------
+ * "feat: load ConvRot int4 and per-channel int8 safetensors", section
+ * "Solution": codes in [-7, 7], one fp32 scale per output channel, adjacent
+ * pairs packed in a byte; the rotation is the same as for int8 ("The
+ * rotation"). Readings where the page is silent: element 2j sits in the low
+ * nibble of byte j, as a two's-complement nibble; activations are quantized
+ * per row like the int8 ones with 7 in place of 127 (s = max|x_rot| / 7).
+ * The tensor cores read e4m3 copies of the codes (every integer in [-7, 7]
+ * is exact in e4m3) through tcgen05 kind::f8f6f4, at twice the fp16 rate;
+ * the int32 accumulators stay exact. K must be a multiple of 128.
+ *   q4    packed codes [rows, K / 2] bytes (storage format; the GEMM reads q_f8)
+ *   scale fp32 [rows]
+ *   q_f8  e4m3 copy [rows, K] bytes (required by the GEMM), 16-byte aligned */
+typedef struct {
+  const uint8_t* q4;
+  const float* scale;
+  const uint8_t* q_f8;
+  int64_t M;
+  int64_t K;
+  int32_t group;
+  int32_t transform;
+} convrot_packed_act4;
+
+typedef struct {
+  const uint8_t* q4;
+  const float* scale;
+  const uint8_t* q_f8;
+  int64_t N;
+  int64_t K;
+  int32_t group;
+  int32_t transform;
+} convrot_packed_weight4;
+
+/* convrot_prepare_weights with 4-bit codes: Qw4 [N, K / 2] bytes, sw fp32
+ * [N], Qw_f8 e4m3 [N, K] or NULL. Errors as convrot_prepare_weights, plus
+ * ALIGNMENT when K is not a multiple of 128. */
+convrot_status convrot_prepare_weights4(const void* W, int32_t w_dtype, int64_t N, int64_t K,
+                                        int32_t group, int32_t transform, const int8_t* signs,
+                                        uint8_t* Qw4, float* sw, uint8_t* Qw_f8, cudaStream_t stream);
+
+/* convrot_quantize_act with 4-bit codes: Qx4 [M, K / 2] bytes, sx fp32 [M],
+ * Qx_f8 e4m3 [M, K] or NULL. The fastest path wants X 16-byte and Qx4,
+ * Qx_f8 32-byte aligned. */
+convrot_status convrot_quantize_act4(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                     int32_t group, int32_t transform, const int8_t* signs,
+                                     uint8_t* Qx4, float* sx, uint8_t* Qx_f8, cudaStream_t stream);
+
+/* Y = A * s_x * s_w + b (bf16) for n = 1..8 linears sharing one 4-bit
+ * packed activation, on the e4m3 tensor-core path (any M >= 0). Workspace as
+ * for convrot_linear_multi_ws (may be NULL). */
+convrot_status convrot_linear4_multi(const convrot_packed_act4* a, int32_t n,
+                                     const convrot_packed_weight4* w, const float* const* bias,
+                                     uint16_t* const* Y, const int64_t* ldy, void* workspace,
+                                     int64_t workspace_bytes, cudaStream_t stream);
+
+/* Raw int32 accumulators of the 4-bit GEMM (tests). A int32 [M, N], lda >= N,
+ * a multiple of 4. */
+convrot_status convrot_gemm4_s32(const convrot_packed_act4* a, const convrot_packed_weight4* w,
+                                 int32_t* A, int64_t lda, void* workspace, int64_t workspace_bytes,
+                                 cudaStream_t stream);
+
 /* Reads and clears the device error word of the current device (synchronizes
  * the device first). CONVROT_OK if no kernel reported a problem, else the
  * first status a kernel recorded (e.g. CONVROT_ERR_TIMEOUT). */

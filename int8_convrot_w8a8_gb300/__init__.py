@@ -28,6 +28,8 @@ __all__ = [
     "convrot_prepare_weights", "convrot_quantize_act", "convrot_quantize_act_hmatmul",
     "convrot_linear", "convrot_linear_multi", "convrot_linear_multi_static", "convrot_gemm_s32", "gemm_workspace",
     "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
+    "PackedAct4", "PackedWeight4", "convrot_prepare_weights4", "convrot_quantize_act4", "convrot_linear4",
+    "convrot_linear4_multi", "convrot_gemm4_s32",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +72,18 @@ class _Weight(ctypes.Structure):
                 ("transform", ctypes.c_int32)]
 
 
+class _Act4(ctypes.Structure):
+    _fields_ = [("q4", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("q_f8", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("group", ctypes.c_int32),
+                ("transform", ctypes.c_int32)]
+
+
+class _Weight4(ctypes.Structure):
+    _fields_ = [("q4", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("q_f8", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("group", ctypes.c_int32),
+                ("transform", ctypes.c_int32)]
+
+
 _P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
 _SIGS = {
     "convrot_prepare_weights": [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
@@ -84,6 +98,11 @@ _SIGS = {
     "convrot_gemm_s32_ws": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P, _I64, _P],
     "convrot_linear_multi_static": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                                     ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
+    "convrot_prepare_weights4": [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
+    "convrot_quantize_act4": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
+    "convrot_linear4_multi": [ctypes.POINTER(_Act4), _I32, ctypes.POINTER(_Weight4), ctypes.POINTER(_P),
+                              ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P],
+    "convrot_gemm4_s32": [ctypes.POINTER(_Act4), ctypes.POINTER(_Weight4), _P, _I64, _P, _I64, _P],
     "convrot_get_device_status": [],
     "convrot_selftest_wait_timeout": [_I64, _P],
     "convrot_status_str": [_I32],
@@ -284,6 +303,127 @@ def convrot_gemm_s32(a: PackedAct, w: PackedWeight, out: Optional[torch.Tensor] 
         _check(lib.convrot_gemm_s32_ws(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- 4-bit ---
+# "feat: load ConvRot int4 and per-channel int8 safetensors", "Solution":
+# codes in [-7, 7], adjacent pairs in a byte (element 2j in the low nibble),
+# one fp32 scale per row; the GEMM reads the e4m3 copies.
+
+@dataclasses.dataclass
+class PackedAct4:
+    q4: torch.Tensor                # uint8 [M, K/2]
+    scale: torch.Tensor             # fp32 [M]
+    q_f8: Optional[torch.Tensor]    # uint8 (e4m3 bits) [M, K]
+    group: int
+    transform: int
+
+    @property
+    def M(self) -> int:
+        return self.q4.shape[0]
+
+    @property
+    def K(self) -> int:
+        return 2 * self.q4.shape[1]
+
+    def _c(self) -> _Act4:
+        return _Act4(self.q4.data_ptr(), self.scale.data_ptr(), _ptr(self.q_f8), self.M, self.K, self.group,
+                     self.transform)
+
+
+@dataclasses.dataclass
+class PackedWeight4:
+    q4: torch.Tensor
+    scale: torch.Tensor
+    q_f8: Optional[torch.Tensor]
+    group: int
+    transform: int
+
+    @property
+    def N(self) -> int:
+        return self.q4.shape[0]
+
+    @property
+    def K(self) -> int:
+        return 2 * self.q4.shape[1]
+
+    def _c(self) -> _Weight4:
+        return _Weight4(self.q4.data_ptr(), self.scale.data_ptr(), _ptr(self.q_f8), self.N, self.K, self.group,
+                        self.transform)
+
+
+def convrot_prepare_weights4(W: torch.Tensor, group: int, transform="h4", signs: Optional[torch.Tensor] = None,
+                             with_f8: bool = True, stream=None) -> PackedWeight4:
+    """Offline 4-bit weight path: W_rot = W R, per-output-row codes in [-7, 7]."""
+    if W.dtype not in (torch.float32, torch.bfloat16) or W.dim() != 2:
+        raise TypeError("W must be a 2-D fp32 or bf16 tensor")
+    W = W.contiguous()
+    N, K = W.shape
+    t = _transform_id(transform)
+    q4 = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    s = torch.empty((N,), dtype=torch.float32, device=W.device)
+    f8 = torch.empty((N, K), dtype=torch.uint8, device=W.device) if with_f8 else None
+    _check(lib.convrot_prepare_weights4(W.data_ptr(), _DTYPE_F32 if W.dtype == torch.float32 else _DTYPE_BF16, N, K,
+                                        group, t, _ptr(signs), q4.data_ptr(), s.data_ptr(), _ptr(f8),
+                                        _stream(stream)))
+    return PackedWeight4(q4, s, f8, group, t)
+
+
+def convrot_quantize_act4(X: torch.Tensor, group: int, transform="h4", signs: Optional[torch.Tensor] = None,
+                          with_f8: bool = True, out: Optional[PackedAct4] = None, stream=None) -> PackedAct4:
+    """Runtime 4-bit path: X_rot = X R, per-row scale max/7, codes in [-7, 7]."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2:
+        raise TypeError("X must be a 2-D bf16 tensor")
+    if X.stride(1) != 1:
+        X = X.contiguous()
+    M, K = X.shape
+    t = _transform_id(transform)
+    if out is None:
+        q4 = torch.empty((M, K // 2), dtype=torch.uint8, device=X.device)
+        s = torch.empty((M,), dtype=torch.float32, device=X.device)
+        f8 = torch.empty((M, K), dtype=torch.uint8, device=X.device) if with_f8 else None
+        out = PackedAct4(q4, s, f8, group, t)
+    _check(lib.convrot_quantize_act4(X.data_ptr(), M, K, X.stride(0), group, t, _ptr(signs), out.q4.data_ptr(),
+                                     out.scale.data_ptr(), _ptr(out.q_f8), _stream(stream)))
+    return out
+
+
+def convrot_linear4_multi(a: PackedAct4, ws: Sequence[PackedWeight4], biases: Optional[Sequence] = None,
+                          outs: Optional[List[torch.Tensor]] = None, stream=None,
+                          workspace: Optional[torch.Tensor] = None) -> List[torch.Tensor]:
+    """4-bit linears sharing one packed activation, in one launch (e4m3 tensor cores)."""
+    n = len(ws)
+    if outs is None:
+        outs = [torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q4.device) for w in ws]
+    warr = (_Weight4 * n)(*[w._c() for w in ws])
+    barr = (ctypes.c_void_p * n)(*[(_ptr(b) if b is not None else None) for b in (biases or [None] * n)])
+    yarr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    larr = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
+    ca = a._c()
+    wsp = None if workspace is None else workspace.data_ptr()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.convrot_linear4_multi(ctypes.byref(ca), n, warr, barr, yarr, larr, wsp, wsb, _stream(stream)))
+    return outs
+
+
+def convrot_linear4(a: PackedAct4, w: PackedWeight4, bias: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, stream=None,
+                    workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    return convrot_linear4_multi(a, [w], [bias], outs=None if out is None else [out], stream=stream,
+                                 workspace=workspace)[0]
+
+
+def convrot_gemm4_s32(a: PackedAct4, w: PackedWeight4, out: Optional[torch.Tensor] = None, stream=None,
+                      workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Raw int32 accumulators of the 4-bit GEMM."""
+    if out is None:
+        out = torch.empty((a.M, w.N), dtype=torch.int32, device=a.q4.device)
+    ca, cw = a._c(), w._c()
+    wsp = None if workspace is None else workspace.data_ptr()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.convrot_gemm4_s32(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0), wsp, wsb,
+                                 _stream(stream)))
     return out
 
 

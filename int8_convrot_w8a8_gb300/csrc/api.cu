@@ -13,15 +13,15 @@
 namespace convrot {
 
 cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, long long ldx, int G, int transform,
-                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic,
+                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic, int qm,
                             cudaStream_t st, int* path);
 cudaError_t hmatmul_launch(const void* X, long long M, int K, long long ldx, int G, int8_t* Q, float* S,
                            uint16_t* Q16, cudaStream_t st);
 bool hmatmul_supported(long long K, long long ldx, int G);
 cudaError_t gemm_mma_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                             bool raw, cudaStream_t st);
-cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
-                           bool raw, void* ws, long long ws_bytes, cudaStream_t st);
+cudaError_t gemm_tc_launch(const void* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs, bool raw,
+                           bool f8, void* ws, long long ws_bytes, cudaStream_t st);
 bool gemm_tc_supported(long long M, int K);
 cudaError_t gemm_small_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                               bool raw, cudaStream_t st);
@@ -213,7 +213,7 @@ convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw
     e = gemm_small_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
   } else if (all_f16 && gemm_tc_supported(a->M, static_cast<int>(a->K))) {
-    e = gemm_tc_launch(a->q_f16, a->scale, a->M, static_cast<int>(a->K), outs, raw, ws, ws_bytes, stream);
+    e = gemm_tc_launch(a->q_f16, a->scale, a->M, static_cast<int>(a->K), outs, raw, false, ws, ws_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
   } else {
     e = gemm_mma_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
@@ -226,7 +226,7 @@ convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw
 
 extern "C" {
 
-int32_t convrot_version(void) { return 100; }
+int32_t convrot_version(void) { return 101; }
 
 const char* convrot_status_str(convrot_status s) {
   switch (s) {
@@ -256,7 +256,7 @@ convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N
     return fail(CONVROT_ERR_ALIGNMENT, "pointers must be 16-byte aligned (scales 4-byte)");
   int path = 0;
   cudaError_t e = rotquant_launch(W, w_dtype, N, static_cast<int>(K), K, group, transform, signs, Qw, sw, Qw_f16,
-                                  w_dtype == CONVROT_DTYPE_F32, stream, &path);
+                                  w_dtype == CONVROT_DTYPE_F32, 127, stream, &path);
   if (e != cudaSuccess) return cuda_fail(e, "weight rotate/quantize launch");
   return ok();
 }
@@ -275,7 +275,7 @@ convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t
     return fail(CONVROT_ERR_ALIGNMENT, "X, Qx, Qx_f16 must be 16-byte aligned and ldx a multiple of 8");
   int path = 0;
   cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs, Qx,
-                                  sx, Qx_f16, 0, stream, &path);
+                                  sx, Qx_f16, 0, 127, stream, &path);
   if (e != cudaSuccess) return cuda_fail(e, "activation rotate/quantize launch");
   return ok();
 }
@@ -359,6 +359,55 @@ convrot_status linear_multi(const convrot_packed_act* a, int32_t n, const convro
   return run_gemm(a, outs, false, ws, ws_bytes, stream);
 }
 
+// ---- 4-bit variant
+convrot_status check_pair4(const convrot_packed_act4* a, const convrot_packed_weight4* w) {
+  if (!a || !w) return fail(CONVROT_ERR_INVALID_ARG, "null descriptor");
+  if (a->M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(a->M));
+  if (w->N <= 0) return fail(CONVROT_ERR_INVALID_ARG, "N=%lld must be >= 1", static_cast<long long>(w->N));
+  if ((a->M > 0 && (!a->q_f8 || !a->scale)) || !w->q_f8 || !w->scale)
+    return fail(CONVROT_ERR_INVALID_ARG, "the 4-bit GEMM needs the e4m3 copies and the scales of both operands");
+  if (a->K != w->K)
+    return fail(CONVROT_ERR_INVALID_ARG, "K mismatch: activation %lld, weight %lld", static_cast<long long>(a->K),
+                static_cast<long long>(w->K));
+  if (a->transform != w->transform || (a->transform != CONVROT_T_NONE && a->group != w->group))
+    return fail(CONVROT_ERR_INVALID_ARG, "activation and weight were rotated differently");
+  convrot_status s = check_shape(a->K, a->group, a->transform);
+  if (s != CONVROT_OK) return s;
+  if (a->K % 128) return fail(CONVROT_ERR_ALIGNMENT, "the 4-bit path needs K a multiple of 128, got %lld",
+                              static_cast<long long>(a->K));
+  if ((a->M > 0 && !aligned(a->q_f8, 16)) || !aligned(w->q_f8, 16) || !aligned(w->scale, 16) ||
+      (a->M > 0 && !aligned(a->scale, 4)))
+    return fail(CONVROT_ERR_ALIGNMENT, "e4m3 copies and weight scales must be 16-byte aligned");
+  return ok();
+}
+
+convrot_status gemm4(const convrot_packed_act4* a, int32_t n, const convrot_packed_weight4* w,
+                     const float* const* bias, void* const* Y, const int64_t* ldy, bool raw, void* ws,
+                     int64_t ws_bytes, cudaStream_t stream) {
+  if (n < 1 || n > kMaxLinears) return fail(CONVROT_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, kMaxLinears);
+  if (!w || !Y || !ldy) return fail(CONVROT_ERR_INVALID_ARG, "w, Y and ldy arrays must be non-null");
+  convrot_status s = check_workspace(ws, ws_bytes);
+  if (s != CONVROT_OK) return s;
+  GemmOutputs outs{};
+  outs.count = n;
+  for (int i = 0; i < n; ++i) {
+    s = check_pair4(a, &w[i]);
+    if (s != CONVROT_OK) return s;
+    const float* b = bias ? bias[i] : nullptr;
+    if (a->M > 0 && !Y[i]) return fail(CONVROT_ERR_INVALID_ARG, "Y[%d] is null", i);
+    if (ldy[i] < w[i].N) return fail(CONVROT_ERR_INVALID_ARG, "ldy[%d] < N", i);
+    if (!aligned(Y[i], 16) || ldy[i] % (raw ? 4 : 8)) return fail(CONVROT_ERR_ALIGNMENT, "Y[%d] alignment", i);
+    if (b && !aligned(b, 16)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] must be 16-byte aligned", i);
+    outs.o[i] = GemmOut{nullptr, reinterpret_cast<const uint16_t*>(w[i].q_f8), w[i].scale, b, Y[i], ldy[i],
+                        static_cast<int>(w[i].N), 0};
+  }
+  if (a->M == 0) return ok();
+  cudaError_t e = gemm_tc_launch(a->q_f8, a->scale, a->M, static_cast<int>(a->K), outs, raw, true, ws, ws_bytes,
+                                 stream);
+  if (e != cudaSuccess) return cuda_fail(e, "4-bit tensor-core GEMM launch");
+  return ok();
+}
+
 convrot_status gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A, int64_t lda,
                         void* ws, int64_t ws_bytes, cudaStream_t stream) {
   convrot_status s = check_pair(a, w);
@@ -402,6 +451,60 @@ convrot_status convrot_linear_multi_ws(const convrot_packed_act* a, int32_t n, c
                                        const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
                                        void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
   return linear_multi(a, n, w, bias, Y, ldy, workspace, workspace_bytes, stream);
+}
+
+convrot_status convrot_prepare_weights4(const void* W, int32_t w_dtype, int64_t N, int64_t K, int32_t group,
+                                        int32_t transform, const int8_t* signs, uint8_t* Qw4, float* sw,
+                                        uint8_t* Qw_f8, cudaStream_t stream) {
+  if (!W || !Qw4 || !sw) return fail(CONVROT_ERR_INVALID_ARG, "W, Qw4 and sw must be non-null");
+  if (w_dtype != CONVROT_DTYPE_F32 && w_dtype != CONVROT_DTYPE_BF16)
+    return fail(CONVROT_ERR_INVALID_ARG, "w_dtype %d is neither fp32 nor bf16", w_dtype);
+  if (N <= 0) return fail(CONVROT_ERR_INVALID_ARG, "N=%lld must be >= 1", static_cast<long long>(N));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (K % 128) return fail(CONVROT_ERR_ALIGNMENT, "the 4-bit path needs K a multiple of 128");
+  if (transform == CONVROT_T_RHT && !signs) return fail(CONVROT_ERR_INVALID_ARG, "RHT needs the sign vector");
+  if (!aligned(W, 16) || !aligned(Qw4, 16) || !aligned(sw, 4) || (Qw_f8 && !aligned(Qw_f8, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "pointers must be 16-byte aligned (scales 4-byte)");
+  int path = 0;
+  cudaError_t e = rotquant_launch(W, w_dtype, N, static_cast<int>(K), K, group, transform, signs,
+                                  reinterpret_cast<int8_t*>(Qw4), sw, reinterpret_cast<uint16_t*>(Qw_f8),
+                                  w_dtype == CONVROT_DTYPE_F32, 7, stream, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "4-bit weight rotate/quantize launch");
+  return ok();
+}
+
+convrot_status convrot_quantize_act4(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                     int32_t transform, const int8_t* signs, uint8_t* Qx4, float* sx, uint8_t* Qx_f8,
+                                     cudaStream_t stream) {
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (K % 128) return fail(CONVROT_ERR_ALIGNMENT, "the 4-bit path needs K a multiple of 128");
+  if (M == 0) return ok();
+  if (!X || !Qx4 || !sx) return fail(CONVROT_ERR_INVALID_ARG, "X, Qx4 and sx must be non-null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (transform == CONVROT_T_RHT && !signs) return fail(CONVROT_ERR_INVALID_ARG, "RHT needs the sign vector");
+  if (!aligned(X, 16) || ldx % 8 || !aligned(Qx4, 16) || !aligned(sx, 4) || (Qx_f8 && !aligned(Qx_f8, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "X, Qx4, Qx_f8 must be 16-byte aligned and ldx a multiple of 8");
+  int path = 0;
+  cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs,
+                                  reinterpret_cast<int8_t*>(Qx4), sx, reinterpret_cast<uint16_t*>(Qx_f8), 0, 7, stream,
+                                  &path);
+  if (e != cudaSuccess) return cuda_fail(e, "4-bit activation rotate/quantize launch");
+  return ok();
+}
+
+convrot_status convrot_linear4_multi(const convrot_packed_act4* a, int32_t n, const convrot_packed_weight4* w,
+                                     const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
+                                     void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
+  return gemm4(a, n, w, bias, reinterpret_cast<void* const*>(Y), ldy, false, workspace, workspace_bytes, stream);
+}
+
+convrot_status convrot_gemm4_s32(const convrot_packed_act4* a, const convrot_packed_weight4* w, int32_t* A,
+                                 int64_t lda, void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
+  void* y = A;
+  return gemm4(a, 1, w, nullptr, &y, &lda, true, workspace, workspace_bytes, stream);
 }
 
 convrot_status convrot_linear_multi_static(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,

@@ -8,7 +8,11 @@
 //
 // sm_103a has no integer tcgen05 MMA, so the int8 codes enter the tensor
 // cores as fp16 values (every integer in [-127, 127] is exact in fp16) with
-// an fp32 accumulator in tensor memory. Products are exact (|q*q| <= 16129)
+// an fp32 accumulator in tensor memory. The 4-bit codes of the W4A4 variant
+// ("feat: load ConvRot int4 and per-channel int8 safetensors", "Solution":
+// values in [-7, 7]) enter as e4m3 (exact) through kind::f8f6f4, at twice
+// the fp16 rate; a 128-byte stage row then holds 128 K values instead of 64
+// and |q*q| <= 49 keeps every partial sum of a 2048-long chunk exact. Products are exact (|q*q| <= 16129)
 // and so is every partial sum while it stays below 2^24 in magnitude:
 // 127 * 127 * 1024 = 16 516 096 < 2^24 = 16 777 216. The K loop therefore
 // runs in chunks of at most 1024; each chunk accumulates into a fresh TMEM
@@ -56,6 +60,7 @@ using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;           // fp16 elements per stage row = 128 bytes = one swizzle atom
+constexpr int BK8 = 128;         // e4m3 elements per stage row (4-bit variant)
 constexpr int KCHUNK = 1024;     // exact fp32 accumulation span (see above)
 constexpr int KITER_PER_CHUNK = KCHUNK / BK;
 constexpr int NUM_EPI_WARPS = 8;
@@ -185,7 +190,7 @@ __device__ __forceinline__ bool work_item(const TcParams& p, int c, int nc, int 
   return true;
 }
 
-template <int BN, bool RAW, int CL>
+template <int BN, bool RAW, int CL, bool F8>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<BN, CL>;
   static_assert(CL == 1 || CL == 2, "cluster of 1 or 2 CTAs");
@@ -202,7 +207,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   unsigned char* epi_smem = out_smem + C::OUT_BYTES + C::BAR_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = p.K / BK;
+  constexpr int BKE = F8 ? BK8 : BK;  // K values per 128-byte stage row
+  const int nk = p.K / BKE;
   const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
   const int cluster_id = blockIdx.x / CL, nclusters = gridDim.x / CL;
 
@@ -261,15 +267,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           const uint32_t sa = smem_base + s * C::STAGE_BYTES;
           if constexpr (CL == 1) {
             mbar_expect_tx(&full[s], C::STAGE_BYTES);
-            tma_load_2d(sa, &p.tmap_a, kb * BK, m_blk * BM, &full[s]);
-            tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN, &full[s]);
+            tma_load_2d(sa, &p.tmap_a, kb * BKE, m_blk * BM, &full[s]);
+            tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BKE, n_local * BN, &full[s]);
           } else {
             // both CTAs' bytes complete on the leader's barrier, which the
             // leader arms for the pair
             if (rank == 0) mbar_expect_tx(&full[s], CL * C::STAGE_BYTES);
             const uint32_t lb = mapa_shared(&full[s], 0);
-            tma_load_2d_pair(sa, &p.tmap_a, kb * BK, m_blk * BM, lb);
-            tma_load_2d_pair(sa + C::A_BYTES, &p.tmap_b[li], kb * BK, n_local * BN + rank * C::B_ROWS, lb);
+            tma_load_2d_pair(sa, &p.tmap_a, kb * BKE, m_blk * BM, lb);
+            tma_load_2d_pair(sa + C::A_BYTES, &p.tmap_b[li], kb * BKE, n_local * BN + rank * C::B_ROWS, lb);
           }
           armed_round[s] = round;
         }
@@ -314,14 +320,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             tc_fence_after();
             const uint32_t sa = smem_base + s * C::STAGE_BYTES;
             const uint32_t sb = sa + C::A_BYTES;
+            // four MMAs per 128-byte row: K = 16 (fp16) or 32 (e4m3) each
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              if constexpr (CL == 1) {
-                tc_mma_f16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
-                           (kb != kstart || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t acc = (kb != kstart || k > 0) ? 1u : 0u;
+              if constexpr (CL == 1 && !F8) {
+                tc_mma_f16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC, acc);
+              } else if constexpr (CL == 1) {
+                tc_mma_f8(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC, acc);
+              } else if constexpr (!F8) {
+                tc_mma_f16_pair(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC, acc);
               } else {
-                tc_mma_f16_pair(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC,
-                                (kb != kstart || k > 0) ? 1u : 0u);
+                tc_mma_f8_pair(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), C::IDESC, acc);
               }
             }
             if constexpr (CL == 1) {
@@ -599,12 +609,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 
 // ---- host -------------------------------------------------------------------
 
-bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long rows, int K, int box_rows) {
+// Operand map: [rows][K] fp16 (or e4m3 bytes), boxes of 128 bytes x box_rows.
+bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long rows, int K, int box_rows, bool f8) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * (f8 ? 1 : 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(f8 ? BK8 : BK), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -658,7 +670,7 @@ SplitPlan plan_split(long long tiles, int clusters, int nk, int bn, int cl, long
 
 constexpr double kSplitOverheadCycles = 15000.0;
 
-int choose_bn(long long M, int K, const GemmOutputs& outs, int sms, int cl, long long ws_bytes) {
+int choose_bn(long long M, int K, int bke, const GemmOutputs& outs, int sms, int cl, long long ws_bytes) {
   const long long mt = ((M + BM - 1) / BM + cl - 1) / cl;
   const int clusters = std::max(1, sms / cl);
   int best = 256;
@@ -667,9 +679,9 @@ int choose_bn(long long M, int K, const GemmOutputs& outs, int sms, int cl, long
     long long nt = 0;
     for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + bn - 1) / bn;
     const long long tiles = mt * nt;
-    const SplitPlan sp = plan_split(tiles, clusters, K / BK, bn, cl, ws_bytes);
+    const SplitPlan sp = plan_split(tiles, clusters, K / bke, bn, cl, ws_bytes);
     // cycles of one tile: k blocks x MMAs per block x their cycles
-    const double tile = static_cast<double>(K / BK) * (BK / 16) * bn * mma_cycles_per_column(bn);
+    const double tile = static_cast<double>(K / bke) * 4 * bn * mma_cycles_per_column(bn);
     const double cost = sp.sk_tiles ? (sp.dp_tiles / clusters + 1.0 / sp.pieces) * tile + kSplitOverheadCycles
                                     : static_cast<double>((tiles + clusters - 1) / clusters) * tile;
     if (best_cost < 0 || cost < best_cost * 0.999) {
@@ -680,19 +692,20 @@ int choose_bn(long long M, int K, const GemmOutputs& outs, int sms, int cl, long
   return best;
 }
 
-template <int BN, bool RAW, int CL>
-cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K, GemmOutputs outs,
+template <int BN, bool RAW, int CL, bool F8>
+cudaError_t launch_bn(EncodeTiledFn enc, const void* Qx16, const float* sx, long long M, int K, GemmOutputs outs,
                       void* ws, long long ws_bytes, cudaStream_t st, int sms) {
   using C = Cfg<BN, CL>;
+  constexpr int BKE = F8 ? BK8 : BK;
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_map(enc, &p.tmap_a, Qx16, M, K, BM)) return cudaErrorInvalidValue;
+  if (!make_map(enc, &p.tmap_a, Qx16, M, K, BM, F8)) return cudaErrorInvalidValue;
   int nt = 0;
   for (int i = 0; i < outs.count; ++i) {
     outs.o[i].tile_begin = nt;
     nt += (outs.o[i].n + BN - 1) / BN;
     // in a pair each CTA loads its BN / 2 rows of the B tile
-    if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN / CL)) return cudaErrorInvalidValue;
+    if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN / CL, F8)) return cudaErrorInvalidValue;
   }
   // Y through tiled stores when every output allows it: bf16, 16-byte aligned
   // base and row pitch, at least one full piece wide
@@ -722,7 +735,7 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.num_tiles = static_cast<int>(tiles);
   p.spin_limit = kDefaultSpinLimit;
-  auto kern = gemm_tc_kernel<BN, RAW, CL>;
+  auto kern = gemm_tc_kernel<BN, RAW, CL, F8>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   // clusters that are resident together: the split plan needs the real count
@@ -732,7 +745,7 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
     if (e != cudaSuccess) return e;
   }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  const SplitPlan sp = plan_split(tiles, clusters, K / BK, BN, CL, ws ? ws_bytes : 0);
+  const SplitPlan sp = plan_split(tiles, clusters, K / BKE, BN, CL, ws ? ws_bytes : 0);
   // oversize guard: the split's counters and sums must fit the workspace
   if (sp.sk_tiles && kWsCounterBytes + static_cast<long long>(sp.sk_tiles) * CL * BM * BN * 4 > ws_bytes)
     return cudaErrorInvalidValue;
@@ -764,13 +777,13 @@ cudaError_t launch_bn(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
   }
 }
 
-template <bool RAW, int CL>
-cudaError_t launch_cl(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, long long M, int K,
+template <bool RAW, int CL, bool F8>
+cudaError_t launch_cl(EncodeTiledFn enc, const void* Qx16, const float* sx, long long M, int K,
                       const GemmOutputs& outs, void* ws, long long ws_bytes, cudaStream_t st, int sms) {
-  switch (choose_bn(M, K, outs, sms, CL, ws ? ws_bytes : 0)) {
-    case 256: return launch_bn<256, RAW, CL>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
-    case 224: return launch_bn<224, RAW, CL>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
-    default: return launch_bn<192, RAW, CL>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+  switch (choose_bn(M, K, F8 ? BK8 : BK, outs, sms, CL, ws ? ws_bytes : 0)) {
+    case 256: return launch_bn<256, RAW, CL, F8>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+    case 224: return launch_bn<224, RAW, CL, F8>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+    default: return launch_bn<192, RAW, CL, F8>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
   }
 }
 
@@ -778,19 +791,28 @@ cudaError_t launch_cl(EncodeTiledFn enc, const uint16_t* Qx16, const float* sx, 
 
 bool gemm_tc_supported(long long M, int K) { return M > 64 && K % BK == 0 && K >= BK; }
 
-cudaError_t gemm_tc_launch(const uint16_t* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs,
-                           bool raw, void* ws, long long ws_bytes, cudaStream_t st) {
+// Qx16: fp16 codes, or with f8 the e4m3 codes of the 4-bit variant (any M;
+// K a multiple of 128; the outputs' qw16 point at e4m3 weights).
+cudaError_t gemm_tc_launch(const void* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs, bool raw,
+                           bool f8, void* ws, long long ws_bytes, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
+  if (K % (f8 ? BK8 : BK) != 0) return cudaErrorInvalidValue;
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const int sms = device_sm_count();
   // CTA pairs run the 2-SM MMA when there are at least two row blocks
-  if (M > BM) {
-    return raw ? launch_cl<true, 2>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
-               : launch_cl<false, 2>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+  if (f8) {
+    if (M > BM)
+      return raw ? launch_cl<true, 2, true>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
+                 : launch_cl<false, 2, true>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+    return raw ? launch_cl<true, 1, true>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
+               : launch_cl<false, 1, true>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
   }
-  return raw ? launch_cl<true, 1>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
-             : launch_cl<false, 1>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+  if (M > BM)
+    return raw ? launch_cl<true, 2, false>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
+               : launch_cl<false, 2, false>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
+  return raw ? launch_cl<true, 1, false>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms)
+             : launch_cl<false, 1, false>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
 }
 
 }  // namespace convrot

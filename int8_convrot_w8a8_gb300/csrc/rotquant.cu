@@ -21,6 +21,11 @@
 //    one rounding (see kRoundMagic). |y| <= amax, so |y * inv| < 127.5 and
 //    the clamp to [-127, 127] can never bite; a zero row gets inv = 0,
 //    codes 0 and scale 0.
+//  * 4-bit codes ("feat: load ConvRot int4 and per-channel int8
+//    safetensors", "Solution": values in [-7, 7], adjacent pairs in a byte)
+//    use 7 in place of 127; they leave as two's-complement nibbles, element
+//    2j in the low nibble of byte j, plus an e4m3 copy (every integer in
+//    [-7, 7] is exact in e4m3) that the tensor cores read.
 #include <algorithm>
 #include <cstdio>
 
@@ -29,6 +34,21 @@
 namespace convrot {
 
 CONVROT_DEFINE_STATUS_WORD(status_word_rotquant)
+
+// Eight magic-rounded values -> eight two's-complement nibbles, value i in
+// bits 4i..4i+3 (the low bits of the rounded value are the code).
+__device__ __forceinline__ uint32_t nibbles8(float t0, float t1, float t2, float t3, float t4, float t5, float t6,
+                                             float t7) {
+  const float t[8] = {t0, t1, t2, t3, t4, t5, t6, t7};
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w |= (__float_as_uint(t[i]) & 0xFu) << (4 * i);
+  return w;
+}
+// Two integer-valued floats -> two e4m3 bytes, the first in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
 
 __device__ __forceinline__ void h4_stage(float& x0, float& x1, float& x2, float& x3) {
   const float u01 = x0 + x1, w0 = x0 - x1, u23 = x2 + x3, w2 = x2 - x3;
@@ -58,11 +78,13 @@ __device__ __forceinline__ float load_in<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float load_in<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// qm = 127: Q int8 [M, K], Q16 fp16 copy; qm = 7: Q packed nibbles
+// [M, K / 2], Q16 reinterpreted as the e4m3 copy [M, K] (bytes).
 template <typename Tin>
 __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__ X, long long M, int K, long long ldx,
                                                          int transform, int G, const int8_t* __restrict__ signs,
                                                          int8_t* __restrict__ Q, float* __restrict__ S,
-                                                         __half* __restrict__ Q16, float s_div) {
+                                                         __half* __restrict__ Q16, float s_div, int qm) {
   extern __shared__ float buf[];
   __shared__ float red[32];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -112,12 +134,27 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
     }
     __syncthreads();
     const float amax = red[0];
-    const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
-    int8_t* q = Q + row * (long long)K;
-    for (int i = tid; i < K; i += nt) {
-      const int c = code_from_magic(fmaf(buf[i], inv, kRoundMagic));
-      q[i] = static_cast<int8_t>(c);
-      if (Q16) Q16[row * (long long)K + i] = __int2half_rn(c);
+    const float inv = amax > 0.0f ? static_cast<float>(qm) / amax : 0.0f;
+    if (qm == 127) {
+      int8_t* q = Q + row * (long long)K;
+      for (int i = tid; i < K; i += nt) {
+        const int c = code_from_magic(fmaf(buf[i], inv, kRoundMagic));
+        q[i] = static_cast<int8_t>(c);
+        if (Q16) Q16[row * (long long)K + i] = __int2half_rn(c);
+      }
+    } else {
+      uint8_t* q4 = reinterpret_cast<uint8_t*>(Q) + row * (long long)(K / 2);
+      uint8_t* f8 = Q16 ? reinterpret_cast<uint8_t*>(Q16) + row * (long long)K : nullptr;
+      for (int j = tid; j < K / 2; j += nt) {
+        const int c0 = code_from_magic(fmaf(buf[2 * j], inv, kRoundMagic));
+        const int c1 = code_from_magic(fmaf(buf[2 * j + 1], inv, kRoundMagic));
+        q4[j] = static_cast<uint8_t>((c0 & 0xF) | ((c1 & 0xF) << 4));
+        if (f8) {
+          const uint32_t b = e4m3x2(static_cast<float>(c0), static_cast<float>(c1));
+          f8[2 * j] = static_cast<uint8_t>(b & 0xFF);
+          f8[2 * j + 1] = static_cast<uint8_t>(b >> 8);
+        }
+      }
     }
     if (tid == 0) S[row] = amax / s_div;
     __syncthreads();
@@ -194,7 +231,7 @@ __device__ __forceinline__ float2 h4_xlane(float2 x) {
   return f2_add(u, w);
 }
 
-template <int T, int G>
+template <int T, int G, int QM>
 __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CUtensorMap xmap, long long M, int K,
                                                        int R, int NT, const int8_t* __restrict__ signs,
                                                        int8_t* __restrict__ Q, float* __restrict__ S,
@@ -405,7 +442,44 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
     __syncthreads();
 
     // ---- quantize and store
-    if (active) {
+    if (active && QM == 7) {
+      // 4-bit: 16 values -> 8 bytes of nibbles and 16 e4m3 bytes
+      const float amax = __uint_as_float(rowmax[my_row]);
+      const float inv = amax > 0.0f ? 7.0f / amax : 0.0f;
+      const float2 inv2 = make_float2(inv, inv);
+      const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+      const long long tile_e = (tile * R) * static_cast<long long>(K);
+      uint8_t* q4 = reinterpret_cast<uint8_t*>(Q);
+      uint8_t* f8 = reinterpret_cast<uint8_t*>(Q16);
+      auto emit16_w4 = [&](int p0, long long e) {
+        float2 t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = f2_fma(v[p0 + k], inv2, mg2);
+        const uint32_t n0 = nibbles8(t[0].x, t[0].y, t[1].x, t[1].y, t[2].x, t[2].y, t[3].x, t[3].y);
+        const uint32_t n1 = nibbles8(t[4].x, t[4].y, t[5].x, t[5].y, t[6].x, t[6].y, t[7].x, t[7].y);
+        asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(q4 + (e >> 1)), "r"(n0), "r"(n1) : "memory");
+        if (f8) {
+          uint32_t fw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 ca = f2_sub(t[2 * k], mg2), cb = f2_sub(t[2 * k + 1], mg2);
+            fw[k] = e4m3x2(ca.x, ca.y) | (e4m3x2(cb.x, cb.y) << 16);
+          }
+          stg_128(f8 + e, make_uint4(fw[0], fw[1], fw[2], fw[3]));
+        }
+      };
+      if (tile_e + (static_cast<long long>(tid) << 6) < total_elems) {
+        if constexpr (C::NX >= 1) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            emit16_w4(8 * r, tile_e + (static_cast<long long>((tid & ~3) + r) << 6) + 16 * qa);
+        } else {
+          const long long e0 = tile_e + (static_cast<long long>(tid) << 6);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) emit16_w4(8 * h, e0 + 16 * h);
+        }
+      }
+    } else if (active) {
       const float amax = __uint_as_float(rowmax[my_row]);
       const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
       const float2 inv2 = make_float2(inv, inv);
@@ -484,10 +558,10 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
 
 // ================================================================ host =====
 
-static float scale_divisor(int transform, int G) {
-  if (transform == CONVROT_T_REGULAR_H4) return 127.0f * static_cast<float>(1 << (ilog2_c(G) / 2));
-  if (transform == CONVROT_T_RHT) return static_cast<float>(127.0 * std::sqrt(static_cast<double>(G)));
-  return 127.0f;
+static float scale_divisor(int transform, int G, int qm) {
+  if (transform == CONVROT_T_REGULAR_H4) return static_cast<float>(qm) * static_cast<float>(1 << (ilog2_c(G) / 2));
+  if (transform == CONVROT_T_RHT) return static_cast<float>(qm * std::sqrt(static_cast<double>(G)));
+  return static_cast<float>(qm);
 }
 
 
@@ -521,7 +595,7 @@ static bool choose_rows(int K, int ept, bool phase_c, int* R_out, int* NT_out) {
   return true;
 }
 
-template <int T, int G>
+template <int T, int G, int QM>
 static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, const int8_t* signs,
                                int8_t* Q, float* S, __half* Q16, cudaStream_t st, bool* launched) {
   *launched = false;
@@ -545,7 +619,7 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   // the quad transpose needs 256 bytes per thread (one fp32 line)
   const int tbytes = LaneCfg<T, G>::NX >= 1 ? threads * 256 : 0;
   const int smem = 1024 + 2 * stage_bytes + tbytes + ((3 * R + 1) & ~1) * 4 + 2 * 8 + 16 + LaneCfg<T, G>::NPOS * 128;
-  auto kern = rq_lane_kernel<T, G>;
+  auto kern = rq_lane_kernel<T, G, QM>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -559,7 +633,7 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   const long long rounds = (tiles + slots - 1) / slots;
   const long long grid = (tiles + rounds - 1) / rounds;
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, signs, Q, S, Q16,
-                                                             scale_divisor(T, G), stage_bytes, tbytes,
+                                                             scale_divisor(T, G, QM), stage_bytes, tbytes,
                                                              kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
@@ -567,8 +641,42 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
 
 // Entry used by the ABI layer. Returns a cudaError_t; *path tells which
 // kernel ran (0 = generic, 1 = fast).
+template <int QM>
+static cudaError_t launch_lane_any(const __nv_bfloat16* xb, long long M, int K, long long ldx, int G, int transform,
+                                  const int8_t* signs, int8_t* Q, float* S, __half* q16, cudaStream_t st,
+                                  bool* launched) {
+  constexpr int H4 = CONVROT_T_REGULAR_H4, RHT = CONVROT_T_RHT;
+  *launched = false;
+  if (transform == H4) {
+    switch (G) {
+      case 4: return launch_lane<H4, 4, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 16: return launch_lane<H4, 16, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 64: return launch_lane<H4, 64, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 256: return launch_lane<H4, 256, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 1024: return launch_lane<H4, 1024, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      default: return cudaSuccess;
+    }
+  }
+  if (transform == RHT) {
+    switch (G) {
+      case 2: return launch_lane<RHT, 2, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 4: return launch_lane<RHT, 4, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 8: return launch_lane<RHT, 8, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 16: return launch_lane<RHT, 16, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 32: return launch_lane<RHT, 32, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 64: return launch_lane<RHT, 64, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 128: return launch_lane<RHT, 128, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      case 256: return launch_lane<RHT, 256, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+      default: return cudaSuccess;
+    }
+  }
+  return launch_lane<CONVROT_T_NONE, 1, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
+}
+
+// qm = 127: int8 codes (Q) and fp16 copy (Q16); qm = 7: packed 4-bit codes
+// (Q, K / 2 bytes per row) and e4m3 copy (Q16 as bytes).
 cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, long long ldx, int G, int transform,
-                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic,
+                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic, int qm,
                             cudaStream_t st, int* path) {
   *path = 0;
   if (M <= 0) return cudaSuccess;
@@ -581,32 +689,8 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
   if (!force_generic && in_dtype == CONVROT_DTYPE_BF16 && aligned32 && K % 16 == 0) {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
     bool launched = false;
-    cudaError_t e = cudaSuccess;
-    constexpr int H4 = CONVROT_T_REGULAR_H4, RHT = CONVROT_T_RHT;
-    if (transform == H4) {
-      switch (G) {
-        case 4: e = launch_lane<H4, 4>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 16: e = launch_lane<H4, 16>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 64: e = launch_lane<H4, 64>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 256: e = launch_lane<H4, 256>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 1024: e = launch_lane<H4, 1024>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        default: break;
-      }
-    } else if (transform == RHT) {
-      switch (G) {
-        case 2: e = launch_lane<RHT, 2>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 4: e = launch_lane<RHT, 4>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 8: e = launch_lane<RHT, 8>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 16: e = launch_lane<RHT, 16>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 32: e = launch_lane<RHT, 32>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 64: e = launch_lane<RHT, 64>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 128: e = launch_lane<RHT, 128>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        case 256: e = launch_lane<RHT, 256>(xb, M, K, ldx, signs, Q, S, q16, st, &launched); break;
-        default: break;
-      }
-    } else {
-      e = launch_lane<CONVROT_T_NONE, 1>(xb, M, K, ldx, signs, Q, S, q16, st, &launched);
-    }
+    cudaError_t e = qm == 7 ? launch_lane_any<7>(xb, M, K, ldx, G, transform, signs, Q, S, q16, st, &launched)
+                            : launch_lane_any<127>(xb, M, K, ldx, G, transform, signs, Q, S, q16, st, &launched);
     if (e != cudaSuccess) return e;
     if (launched) {
       *path = 1;
@@ -616,19 +700,19 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
   const int threads = 256;
   const size_t smem = static_cast<size_t>(K) * sizeof(float);
   const long long grid = std::min<long long>(M, 64LL * device_sm_count());
-  const float sdiv = scale_divisor(transform, G);
+  const float sdiv = scale_divisor(transform, G, qm);
   if (in_dtype == CONVROT_DTYPE_BF16) {
     auto kern = rq_generic_kernel<__nv_bfloat16>;
     cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(static_cast<const __nv_bfloat16*>(X), M, K, ldx,
-                                                             transform, G, signs, Q, S, q16, sdiv);
+                                                             transform, G, signs, Q, S, q16, sdiv, qm);
   } else {
     auto kern = rq_generic_kernel<float>;
     cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(static_cast<const float*>(X), M, K, ldx, transform, G,
-                                                             signs, Q, S, q16, sdiv);
+                                                             signs, Q, S, q16, sdiv, qm);
   }
   return cudaGetLastError();
 }

@@ -53,7 +53,7 @@ __all__ = [
     "sylvester_hadamard", "rht_block", "row_operator", "rotate_rows",
     "quantize_rows", "prepare_weights", "quantize_act", "int_gemm",
     "reconstruct", "round_to_bf16", "linear", "float_linear",
-    "boundary_distance", "QMAX4", "pack_int4", "unpack_int4",
+    "boundary_distance", "QMAX", "QMAX4", "pack_int4", "unpack_int4",
 ]
 
 # "INT8 Convrot Safetensors", "How INT8 convrot works": the printed matrix,
