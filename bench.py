@@ -49,9 +49,14 @@ PRE_STEP_SLEEP_CYCLES = 300_000
 # changed the figure no longer applies and the line reports null.
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
-        "bytes": 253_280_000 + 42_949_376,
+        "bytes": 264_964_864 + 44_137_984,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "23ddf7973a17f4856e4a2c95047db887fd188e7032c39409961ab57592f72c95",
+        "sha256": "6d6c40045e5bf6f21c2b66e4717e9476ac37e4cba2d9cf397e60ec63a4f3f0a0",
+    },
+    ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256_W4A4"): {
+        "bytes": 63_656_704 + 24_993_024,
+        "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
+        "sha256": "6d6c40045e5bf6f21c2b66e4717e9476ac37e4cba2d9cf397e60ec63a4f3f0a0",
     },
 }
 
