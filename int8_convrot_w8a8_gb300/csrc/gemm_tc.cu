@@ -8,25 +8,30 @@
 //
 // sm_103a has no integer tcgen05 MMA, so the int8 codes enter the tensor
 // cores as fp16 values (every integer in [-127, 127] is exact in fp16) with
-// an fp32 accumulator in tensor memory. The 4-bit codes of the W4A4 variant
-// ("feat: load ConvRot int4 and per-channel int8 safetensors", "Solution":
-// values in [-7, 7]) enter as e4m3 (exact) through kind::f8f6f4, at twice
-// the fp16 rate; a 128-byte stage row then holds 128 K values instead of 64
-// and |q*q| <= 49 keeps every partial sum of a 2048-long chunk exact. Products are exact (|q*q| <= 16129)
+// an fp32 accumulator in tensor memory. Products are exact (|q*q| <= 16129)
 // and so is every partial sum while it stays below 2^24 in magnitude:
 // 127 * 127 * 1024 = 16 516 096 < 2^24 = 16 777 216. The K loop therefore
-// runs in chunks of at most 1024; each chunk accumulates into a fresh TMEM
-// buffer, and the epilogue warps convert the chunk (an exact integer in
-// fp32) to int32 and add it into int32 registers. Two TMEM buffers
-// alternate, so the tensor cores fill chunk c+1 while chunk c drains.
+// runs in chunks of 16 stage rows (1024 fp16 K values); each chunk
+// accumulates into a fresh TMEM buffer, and the epilogue warps convert the
+// chunk (an exact integer in fp32) to int32 and add it into int32 registers.
+// Two TMEM buffers alternate, so the tensor cores fill chunk c+1 while chunk
+// c drains. The 4-bit codes of the W4A4 variant ("feat: load ConvRot int4
+// and per-channel int8 safetensors", "Solution": values in [-7, 7]) enter as
+// e4m3 (exact) through kind::f8f6f4 at twice the fp16 rate; a 128-byte stage
+// row then holds 128 K values, and |q*q| <= 49 keeps every partial sum of a
+// 2048-long chunk exact.
 //
-// Structure (one persistent CTA per SM, 320 threads):
-//   warp 0      TMA producer: 128 x 64 A tiles and BN x 64 B tiles, 128-byte
-//               swizzle, into a STAGES-deep shared-memory ring.
-//   warp 1      TMEM allocation and the MMA issuer: tcgen05.mma kind::f16,
-//               M = 128, N = BN, K = 16, cta_group::1.
+// Structure (one persistent CTA per SM, 320 threads; CTA pairs when M > 128):
+//   warp 0      TMA producer: 128 A rows and BN / CL B rows per stage (128
+//               bytes of K each, 128-byte swizzle) into a STAGES-deep ring;
+//               in a pair both CTAs' copies complete on the leader's barrier.
+//   warp 1      TMEM allocation and the MMA issuer: tcgen05.mma, M = 128 * CL,
+//               N = BN, four MMAs per stage row, cta_group::CL; in a pair only
+//               the leader issues, and its commits are multicast to both.
 //   warps 2..9  epilogue: TMEM -> registers (tcgen05.ld 32x32b), int32
-//               accumulation, then scaling, bias, bf16 and the store.
+//               accumulation; column scales and biases copied to shared
+//               memory (cp.async) while the MMAs run; then scaling, bias,
+//               bf16, and 32 x 16 TMA tiled stores of Y.
 // Tiles are handed out statically (tile = blockIdx.x + i * gridDim.x) in a
 // grouped order for L2 reuse. When the last round would leave most of the
 // GPU idle and the caller gave a workspace, the tiles of that round are
