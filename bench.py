@@ -45,30 +45,43 @@ PRE_STEP_SLEEP_CYCLES = 300_000
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the step's dominant kernel, from one ncu capture of `bench.py --profile` on
 # GB300 (summaries in profiles/), keyed by kernel and workload, with the
-# SHA-256 of the kernel's source file at capture time: once the source has
-# changed the figure no longer applies and the line reports null.
+# SHA-256 of the kernel's source code (comments aside, see code_sha256) at
+# capture time: once the code has changed the figure no longer applies and
+# the line reports null.
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
         "bytes": 264_964_864 + 44_137_984,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "6d6c40045e5bf6f21c2b66e4717e9476ac37e4cba2d9cf397e60ec63a4f3f0a0",
+        "sha256": "821cc009360d5a9fd0c9e632c2257e340d9d68b7ab5c2eee8c4450fdd59a19ee",
     },
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256_W4A4"): {
         "bytes": 63_656_704 + 24_993_024,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "6d6c40045e5bf6f21c2b66e4717e9476ac37e4cba2d9cf397e60ec63a4f3f0a0",
+        "sha256": "821cc009360d5a9fd0c9e632c2257e340d9d68b7ab5c2eee8c4450fdd59a19ee",
     },
 }
 
 
-def ncu_traffic(kernel: str, workload: str):
+def code_sha256(path: str) -> str:
+    """SHA-256 of a C++/CUDA source with its // comments and blank lines
+    removed, so that only code changes change it."""
     import hashlib
+    import re
+    lines = []
+    with open(path) as f:
+        for line in f:
+            line = re.sub(r"//.*", "", line).strip()
+            if line:
+                lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
+def ncu_traffic(kernel: str, workload: str):
     rec = NCU_TRAFFIC.get((kernel, workload))
     if rec is None:
         return None
-    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
-            return None
+    if code_sha256(os.path.join(ROOT, rec["source"])) != rec["sha256"]:
+        return None
     return rec["bytes"]
 
 
