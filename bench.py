@@ -93,6 +93,7 @@ WORKLOADS = {
     "dit6144_w4": lambda: _w4(WL.dit6144()),
     "qkv32700_w4": lambda: _w4(WL.qkv32700()),
     "gsweep256_w4": lambda: _w4(WL.gsweep(256)),
+    "k2688_w4": lambda: _w4(WL.k2688()),
     "qkv32700": lambda: WL.qkv32700(),
     "qkv32700_cat": lambda: _concat(WL.qkv32700()),
     "ffn_pair": lambda: WL.ffn_pair(),
