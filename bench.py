@@ -6,7 +6,10 @@ fused dequant/bias/bf16 epilogue for every linear that shares the packed
 activation. Weights are prepared once before timing (the offline path).
 
 Timing: W warm-up steps, then K timed steps; each step is bracketed by CUDA
-events on the launching stream, and L2 is flushed between steps, outside
+events on the launching stream (the GEMM is a programmatic dependent launch
+of the rotate+quantize, so nothing is recorded between them; each of the two
+kernels is then timed alone the same way for the per-kernel figures), and L2
+is flushed between steps, outside
 the events: a 256 MiB write, then a 256 MiB read, so that the flush's own
 dirty lines are written back before the step starts. Clocks are sampled
 with nvidia-smi during the timed region. The e2e figure repeats the step
@@ -332,22 +335,20 @@ def gpu_main(args, world, rank, local):
         torch.sum(flush_rd, dim=0, out=flush_sink)
 
     def step():
+        # nothing between the two launches: the GEMM is a programmatic
+        # dependent of the rotate+quantize and may start while it finishes
         quant(X, use_f16, out=act)
-        e_mid.record(stream)
         lin(act, outs, gws)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for _ in range(args.warmup):
         flush_l2()
-        e_mid = torch.cuda.Event(enable_timing=True)
         step()
     torch.cuda.synchronize()
     assert cr.convrot_get_device_status() == 0
     if args.profile:
         # a short, fixed launch list for ncu: one more step, then one int8-only
         # rotate+quantize and (where supported) one matmul-form rotate+quantize
-        e_mid = torch.cuda.Event(enable_timing=True)
         step()
         quant(X, False)
         if bits == 8 and wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
@@ -364,7 +365,7 @@ def gpu_main(args, world, rank, local):
         for i in range(args.steps):
             flush_l2()
             torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
-            e0, e_mid, e1 = ev[i]
+            e0, e1 = ev[i]
             h0 = time.perf_counter()
             e0.record(stream)
             step()
@@ -376,21 +377,29 @@ def gpu_main(args, world, rank, local):
     status = cr.convrot_get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    # the rotate+quantize contract alone (bf16 in, int8 codes + fp32 scales out,
-    # no fp16 operand copy), timed on its own for the GB/s figure
+    def timed(fn):
+        """Per-launch times (ms) of fn alone, same flush and pause as a step."""
+        marks = []
+        for i in range(args.warmup + args.steps):
+            flush_l2()
+            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            fn()
+            b1.record(stream)
+            if i >= args.warmup:
+                marks.append((b0, b1))
+        torch.cuda.synchronize()
+        return [b0.elapsed_time(b1) for b0, b1 in marks]
+
+    # the step's two kernels timed alone: the GEMM (the roofline kernel) and
+    # the rotate+quantize with its operand copy
+    gemm_ms = timed(lambda: lin(act, outs, gws))
+    quant_ms = timed(lambda: quant(X, use_f16, out=act))
+    # the rotate+quantize contract alone (bf16 in, codes + fp32 scales out, no
+    # operand copy), for the GB/s figure
     act8 = quant(X, False)
-    q_only_ms = []
-    for i in range(args.warmup + args.steps):
-        flush_l2()
-        torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        quant(X, False, out=act8)
-        b1.record(stream)
-        if i >= args.warmup:
-            q_only_ms.append((b0, b1))
-    torch.cuda.synchronize()
-    q_only_ms = [b0.elapsed_time(b1) for b0, b1 in q_only_ms]
+    q_only_ms = timed(lambda: quant(X, False, out=act8))
     # the same contract with the rotation applied as a dense tensor-core matmul
     hm_ms = None
     if bits == 8 and wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
@@ -407,9 +416,7 @@ def gpu_main(args, world, rank, local):
                 hm_ms.append((b0, b1))
         torch.cuda.synchronize()
         hm_ms = [b0.elapsed_time(b1) for b0, b1 in hm_ms]
-    step_ms = [e0.elapsed_time(e1) for e0, _, e1 in ev]
-    quant_ms = [e0.elapsed_time(em) for e0, em, _ in ev]
-    gemm_ms = [em.elapsed_time(e1) for _, em, e1 in ev]
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
 
     ops_step = 2.0 * M * sum(Ns) * K

@@ -249,6 +249,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if constexpr (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent of the previous kernel in the stream
+  // (the rotate+quantize that writes A and s_x): the set-up above overlaps
+  // its last CTAs; nothing below reads memory the previous grid writes
+  // before that grid has completed and flushed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -761,25 +766,23 @@ cudaError_t launch_bn(EncodeTiledFn enc, const void* Qx16, const float* sx, long
   p.ws_acc = ws ? reinterpret_cast<int*>(static_cast<char*>(ws) + kWsCounterBytes) : nullptr;
   // a split runs on every cluster (its whole tiles are a multiple of them)
   const int nc = sp.sk_tiles ? clusters : static_cast<int>(std::min<long long>(tiles, clusters));
-  if constexpr (CL == 1) {
-    kern<<<nc, THREADS, C::SMEM, st>>>(p);
-    return cudaGetLastError();
-  } else {
-    const int grid = CL * nc;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * nc);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  // may start while the previous kernel of the stream finishes (the kernel
+  // waits for it with griddepcontrol.wait before touching its outputs)
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <bool RAW, int CL, bool F8>

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
                                                          int transform, int G, const int8_t* __restrict__ signs,
                                                          int8_t* __restrict__ Q, float* __restrict__ S,
                                                          __half* __restrict__ Q16, float s_div, int qm) {
+  asm volatile("griddepcontrol.launch_dependents;");  // see rq_lane_kernel
   extern __shared__ float buf[];
   __shared__ float red[32];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -238,6 +239,9 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
                                                        __half* __restrict__ Q16, float s_div, int stage_bytes,
                                                        int tbytes, long long spin_limit) {
   using C = LaneCfg<T, G>;
+  // a programmatic dependent launch (the GEMM) may be scheduled now; it
+  // waits for this grid to complete before it reads the codes
+  asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
