@@ -53,14 +53,15 @@ PRE_STEP_SLEEP_CYCLES = 300_000
 # the line reports null.
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
-        "bytes": 264_964_864 + 44_137_984,
+        "bytes": 253_060_352 + 43_163_648,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "821cc009360d5a9fd0c9e632c2257e340d9d68b7ab5c2eee8c4450fdd59a19ee",
+        "sha256": "d50e73af4e86f3f0cbaba15df3aae89be51da25259a98a684b1b8eee59840b49",
     },
+    # dram__bytes.sum (read + write) = dram__bytes.sum.per_second x duration
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256_W4A4"): {
-        "bytes": 63_656_704 + 24_993_024,
+        "bytes": 88_587_000,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "821cc009360d5a9fd0c9e632c2257e340d9d68b7ab5c2eee8c4450fdd59a19ee",
+        "sha256": "d50e73af4e86f3f0cbaba15df3aae89be51da25259a98a684b1b8eee59840b49",
     },
 }
 
