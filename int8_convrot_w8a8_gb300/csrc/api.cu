@@ -26,6 +26,10 @@ bool gemm_tc_supported(long long M, int K);
 cudaError_t gemm_small_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                               bool raw, cudaStream_t st);
 bool gemm_small_supported(long long M, int K);
+cudaError_t gemm_small_tc_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
+                                 bool raw, cudaStream_t st);
+bool gemm_small_tc_supported(long long M, int K);
+int status_word_gemm_small_tc();
 cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st);
 
 CONVROT_DEFINE_STATUS_WORD(status_word_api)
@@ -208,7 +212,12 @@ convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw
   bool all_f16 = a->q_f16 != nullptr;
   for (int i = 0; i < outs.count; ++i) all_f16 = all_f16 && outs.o[i].qw16 != nullptr;
   cudaError_t e;
-  if (gemm_small_supported(a->M, static_cast<int>(a->K))) {
+  if (gemm_small_tc_supported(a->M, static_cast<int>(a->K))) {
+    // a handful of rows, K a multiple of 128: the int8 weight stream widened
+    // to fp16 on chip for the tcgen05 tensor cores
+    e = gemm_small_tc_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "small-M tensor-core GEMM launch");
+  } else if (gemm_small_supported(a->M, static_cast<int>(a->K))) {
     // a handful of rows: the int8 weight stream, no fp16 copies needed
     e = gemm_small_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
@@ -529,8 +538,8 @@ convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_pa
 convrot_status convrot_get_device_status(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  int words[6] = {status_word_rotquant(), status_word_gemm_mma(), status_word_gemm_tc(),
-                  status_word_gemm_small(), status_word_hmatmul(), status_word_api()};
+  int words[7] = {status_word_rotquant(), status_word_gemm_mma(),   status_word_gemm_tc(), status_word_gemm_small(),
+                  status_word_gemm_small_tc(), status_word_hmatmul(), status_word_api()};
   for (int w : words) {
     if (w != 0) {
       if (w == CONVROT_ERR_TIMEOUT) {

@@ -342,3 +342,41 @@ def test_split_full_size_dit_matches_unsplit(cr):
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0
     assert torch.equal(Y1, Y0)
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 296, 128), (24, 1000, 1152), (32, 13824, 1152), (33, 264, 4096),
+                                   (48, 136, 2048), (64, 4096, 4096)])
+def test_small_m_tensor_core_path_bit_exact(cr, M, N, K):
+    """17..64 rows with K a multiple of 128 take the small-M tensor-core
+    kernel (int8 tiles widened to fp16 on chip, swapped operands, one TMEM
+    region per exact 1024-long chunk): accumulators bit-exact, and Y within
+    one bf16 ulp of the oracle's reconstruction from the same codes."""
+    rng = np.random.default_rng(3 * M + N + K)
+    Qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    Qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    sx = (rng.uniform(0.5, 2.0, M) / 127.0).astype(np.float32)
+    sw = (rng.uniform(0.5, 2.0, N) / 127.0).astype(np.float32)
+    bias = rng.normal(0, 0.5, N).astype(np.float32)
+    a = packed_from_codes(cr, Qx, sx, 0, "none", False, "act")
+    w = packed_from_codes(cr, Qw, sw, 0, "none", False, "w")
+    A = O.int_gemm(Qx, Qw)
+    assert np.array_equal(to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64), A)
+    Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda())
+    check_y_same_codes(to_np(Y.float()), A, sx, sw, bias, f"small tc {M}x{N}x{K}")
+
+
+def test_small_m_tensor_core_adversarial_and_multi(cr):
+    """All +-127 codes at K = 4096 (four exact chunks summed in int32), and two
+    linears in one launch equal to two launches."""
+    M, K = 40, 4096
+    Qx = np.full((M, K), 127, np.int8)
+    Qw = np.full((200, K), 127, np.int8)
+    Qw[::3] = -127
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", False, "act")
+    w = packed_from_codes(cr, Qw, np.ones(200), 0, "none", False, "w")
+    assert np.array_equal(to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64), O.int_gemm(Qx, Qw))
+    rng = np.random.default_rng(9)
+    Qw2 = rng.integers(-127, 128, size=(296, K)).astype(np.int8)
+    w2 = packed_from_codes(cr, Qw2, np.ones(296) / 127.0, 0, "none", False, "w")
+    ys = cr.convrot_linear_multi(a, [w, w2], [None, None])
+    assert torch.equal(ys[0], cr.convrot_linear(a, w)) and torch.equal(ys[1], cr.convrot_linear(a, w2))
