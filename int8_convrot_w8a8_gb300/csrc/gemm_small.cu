@@ -102,16 +102,29 @@ __global__ void __launch_bounds__(THREADS_S) gemm_small_kernel(const __grid_cons
   if (warp == CONSUMERS) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // The weights do not depend on the previous kernel of the stream (a
+      // programmatic dependent launch: the rotate+quantize that writes the
+      // codes): the first ring's weight tiles are requested before waiting
+      // for it, the activation tiles after.
+      const int first = p.ktiles < p.stages ? p.ktiles : p.stages;
+      for (int kt = 0; kt < first; ++kt) {
+        const uint32_t sa = sbase + kt * STAGE_BYTES;
+        mbar_expect_tx(&full[kt], STAGE_BYTES);
+        tma_load_2d(sa + A_BYTES, &p.tmap_b[li], kt * SK, n0, &full[kt]);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int kt = 0; kt < p.ktiles; ++kt) {
         const int s = kt % p.stages, round = kt / p.stages;
-        if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1, p.spin_limit)) {
-          record_status(CONVROT_ERR_TIMEOUT);
-          break;
-        }
         const uint32_t sa = sbase + s * STAGE_BYTES;
-        mbar_expect_tx(&full[s], STAGE_BYTES);
+        if (round > 0) {
+          if (!mbar_wait_bounded(&empty[s], (round - 1) & 1, p.spin_limit)) {
+            record_status(CONVROT_ERR_TIMEOUT);
+            break;
+          }
+          mbar_expect_tx(&full[s], STAGE_BYTES);
+          tma_load_2d(sa + A_BYTES, &p.tmap_b[li], kt * SK, n0, &full[s]);
+        }
         tma_load_2d(sa, &p.tmap_a, kt * SK, 0, &full[s]);
-        tma_load_2d(sa + A_BYTES, &p.tmap_b[li], kt * SK, n0, &full[s]);
       }
     }
   } else {
@@ -156,7 +169,9 @@ __global__ void __launch_bounds__(THREADS_S) gemm_small_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     // ---- epilogue: fragment (g = lane/4, t = lane%4) holds rows g, g+8 and
-    // columns 2t, 2t+1 of each 16x8 tile
+    // columns 2t, 2t+1 of each 16x8 tile; the row scales come from the
+    // previous kernel of the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = lane >> 2, t = lane & 3;
     const int c = n0 + warp * 8 + 2 * t;
     const int N = out.n;
@@ -227,8 +242,17 @@ cudaError_t launch_small(EncodeTiledFn enc, const int8_t* Qx, const float* sx, l
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   if (nt > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  kern<<<nt, THREADS_S, smem, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nt);
+  cfg.blockDim = dim3(THREADS_S);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
