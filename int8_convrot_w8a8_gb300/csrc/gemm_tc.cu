@@ -250,10 +250,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Launched as a programmatic dependent of the previous kernel in the stream
-  // (the rotate+quantize that writes A and s_x): the set-up above overlaps
-  // its last CTAs; nothing below reads memory the previous grid writes
-  // before that grid has completed and flushed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // (the rotate+quantize that writes A and s_x): the set-up above and the
+  // first round of weight tiles overlap its last CTAs. The producer (before
+  // its first A tile) and the epilogue (before s_x) wait for that grid to
+  // complete and flush (griddepcontrol.wait); the MMA issuer reads only
+  // shared memory.
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -261,32 +262,54 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if (lane == 0) {
       int armed_round[C::STAGES];
       for (int s = 0; s < C::STAGES; ++s) armed_round[s] = -1;
+      // the weights do not depend on the previous kernel: request the first
+      // round's B tiles (and arm those stages) before waiting for it
+      auto load_b = [&](int s, int kb, int li, int n_local) {
+        const uint32_t sb = smem_base + s * C::STAGE_BYTES + C::A_BYTES;
+        if constexpr (CL == 1) {
+          mbar_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(sb, &p.tmap_b[li], kb * BKE, n_local * BN, &full[s]);
+        } else {
+          // both CTAs' bytes complete on the leader's barrier, which the
+          // leader arms for the pair
+          if (rank == 0) mbar_expect_tx(&full[s], CL * C::STAGE_BYTES);
+          tma_load_2d_pair(sb, &p.tmap_b[li], kb * BKE, n_local * BN + rank * C::B_ROWS, mapa_shared(&full[s], 0));
+        }
+      };
+      auto load_a = [&](int s, int kb, int m_blk) {
+        const uint32_t sa = smem_base + s * C::STAGE_BYTES;
+        if constexpr (CL == 1) {
+          tma_load_2d(sa, &p.tmap_a, kb * BKE, m_blk * BM, &full[s]);
+        } else {
+          tma_load_2d_pair(sa, &p.tmap_a, kb * BKE, m_blk * BM, mapa_shared(&full[s], 0));
+        }
+      };
+      int t, kb0, kb1, pc;
+      {
+        int it0 = 0;
+        for (int i = 0; it0 < C::STAGES && work_item(p, cluster_id, nclusters, i, nk, t, kb0, kb1, pc); ++i) {
+          int m_blk, n_glob, li, n_local;
+          decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
+          for (int kb = kb0; kb < kb1 && it0 < C::STAGES; ++kb, ++it0) load_b(it0, kb, li, n_local);
+        }
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int it = 0;
       bool ok = true;
-      int t, kb0, kb1, pc;
       for (int i = 0; ok && work_item(p, cluster_id, nclusters, i, nk, t, kb0, kb1, pc); ++i) {
         int m_blk, n_glob, li, n_local;
         decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES, round = it / C::STAGES;
-          if (!wait_or_abort(&empty[s], (round & 1) ^ 1, p.spin_limit, abort_flag)) {
-            raise_abort(abort_flag);
-            ok = false;
-            break;
+          if (round > 0) {
+            if (!wait_or_abort(&empty[s], (round & 1) ^ 1, p.spin_limit, abort_flag)) {
+              raise_abort(abort_flag);
+              ok = false;
+              break;
+            }
+            load_b(s, kb, li, n_local);
           }
-          const uint32_t sa = smem_base + s * C::STAGE_BYTES;
-          if constexpr (CL == 1) {
-            mbar_expect_tx(&full[s], C::STAGE_BYTES);
-            tma_load_2d(sa, &p.tmap_a, kb * BKE, m_blk * BM, &full[s]);
-            tma_load_2d(sa + C::A_BYTES, &p.tmap_b[li], kb * BKE, n_local * BN, &full[s]);
-          } else {
-            // both CTAs' bytes complete on the leader's barrier, which the
-            // leader arms for the pair
-            if (rank == 0) mbar_expect_tx(&full[s], CL * C::STAGE_BYTES);
-            const uint32_t lb = mapa_shared(&full[s], 0);
-            tma_load_2d_pair(sa, &p.tmap_a, kb * BKE, m_blk * BM, lb);
-            tma_load_2d_pair(sa + C::A_BYTES, &p.tmap_b[li], kb * BKE, n_local * BN + rank * C::B_ROWS, lb);
-          }
+          load_a(s, kb, m_blk);
           armed_round[s] = round;
         }
       }
@@ -369,6 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // s_x comes from the previous kernel
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;    // which half of the BN columns
     const int row_in_tile = q * 32 + lane;
