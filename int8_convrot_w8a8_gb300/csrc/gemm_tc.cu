@@ -76,6 +76,7 @@ constexpr int GROUP_M = 16;
 // 32-byte swizzle: the 16-byte half of row r sits at half ^ (r >> 2 & 1).
 constexpr int OUT_COLS = 16;
 constexpr int OUT_PIECE_BYTES = 1024;
+constexpr int OUT_BUFS = 2;      // output pieces in flight per epilogue warp
 
 // CL = 1: one CTA computes a 128 x BN tile with cta_group::1 MMAs.
 // CL = 2: a cluster pair computes a 256 x BN tile with cta_group::2 MMAs
@@ -89,13 +90,15 @@ struct Cfg {
   static constexpr int B_ROWS = BN / CL;  // rows of B held by one CTA
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int HALF = BN / 2;  // columns per epilogue thread
-  // per epilogue warp: two 32 x 16 bf16 output pieces for the tiled store
-  static constexpr int OUT_BYTES = NUM_EPI_WARPS * 2 * OUT_PIECE_BYTES;
+  // per epilogue warp: OUT_BUFS 32 x 16 bf16 output pieces for the tiled store
+  static constexpr int OUT_BYTES = NUM_EPI_WARPS * OUT_BUFS * OUT_PIECE_BYTES;
   // per epilogue warp: the column scales and biases of its half tile
   static constexpr int EPI_BYTES = NUM_EPI_WARPS * HALF * 2 * 4;
+  // as many stages as fit next to those, at most 200 KB of them
+  static constexpr int STAGES_FIT = (232448 - 1024 - BAR_BYTES - OUT_BYTES - EPI_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT < (200 * 1024) / STAGE_BYTES ? STAGES_FIT : (200 * 1024) / STAGE_BYTES;
   static constexpr int SMEM = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + EPI_BYTES + 1024;
   static_assert(STAGE_BYTES % 1024 == 0, "the output pieces stay 1 KB aligned");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // this warp's copy of the half tile's column scales, then biases
     const uint32_t wsw = smem_u32(epi_smem) + static_cast<uint32_t>((warp - 2) * C::HALF * 2 * 4);
     const uint32_t wbias = wsw + C::HALF * 4;
-    const uint32_t wout = smem_u32(out_smem) + static_cast<uint32_t>((warp - 2) * 2 * OUT_PIECE_BYTES);
+    const uint32_t wout = smem_u32(out_smem) + static_cast<uint32_t>((warp - 2) * OUT_BUFS * OUT_PIECE_BYTES);
     // this lane's row in an output piece, with the 32-byte swizzle
     const uint32_t out_row = static_cast<uint32_t>(lane) * 32;
     const uint32_t out_sw = static_cast<uint32_t>((lane >> 2) & 1) << 4;
@@ -489,9 +492,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         int* wslab = p.ws_acc + static_cast<long long>(slab) * (C::HALF * 32);  // [8-column chunk][lane][8]
 #pragma unroll
         for (int j = 0; j < C::HALF; j += 8) {
-          const uint32_t pb = wout + static_cast<uint32_t>((ob & 1) * OUT_PIECE_BYTES);
-          if (ob >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
+          const uint32_t pb = wout + static_cast<uint32_t>((ob % OUT_BUFS) * OUT_PIECE_BYTES);
+          if (ob >= OUT_BUFS) {
+            if (lane == 0) bulk_wait_read<OUT_BUFS - 1>();
             __syncwarp();
           }
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + lane * 32), "r"(acc[j]), "r"(acc[j + 1]),
@@ -543,9 +546,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 #pragma unroll
         for (int j = 0; j < C::HALF; j += OUT_COLS) {
           if (!rows_in || nb + j >= o.n) continue;  // warp-uniform
-          const uint32_t pb = wout + static_cast<uint32_t>((ob & 1) * OUT_PIECE_BYTES);
-          if (ob >= 2) {
-            if (lane == 0) bulk_wait_read<1>();
+          const uint32_t pb = wout + static_cast<uint32_t>((ob % OUT_BUFS) * OUT_PIECE_BYTES);
+          if (ob >= OUT_BUFS) {
+            if (lane == 0) bulk_wait_read<OUT_BUFS - 1>();
             __syncwarp();
           }
           uint32_t w[8];
