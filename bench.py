@@ -53,15 +53,14 @@ PRE_STEP_SLEEP_CYCLES = 300_000
 # the line reports null.
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
-        "bytes": 253_060_352 + 43_163_648,
+        "bytes": 266_043_392 + 43_902_208,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "d50e73af4e86f3f0cbaba15df3aae89be51da25259a98a684b1b8eee59840b49",
+        "sha256": "569a776c3026abcf47fdffeb6cd0e38a9fda672ce5869c3610ddd4209501845b",
     },
-    # dram__bytes.sum (read + write) = dram__bytes.sum.per_second x duration
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256_W4A4"): {
-        "bytes": 88_587_000,
+        "bytes": 63_675_904 + 24_203_520,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "d50e73af4e86f3f0cbaba15df3aae89be51da25259a98a684b1b8eee59840b49",
+        "sha256": "569a776c3026abcf47fdffeb6cd0e38a9fda672ce5869c3610ddd4209501845b",
     },
 }
 
