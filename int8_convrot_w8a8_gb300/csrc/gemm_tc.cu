@@ -35,10 +35,12 @@
 // Tiles are handed out statically (tile = blockIdx.x + i * gridDim.x) in a
 // grouped order for L2 reuse. When the last round would leave most of the
 // GPU idle and the caller gave a workspace, the tiles of that round are
-// split along K instead, one piece per cluster: each piece adds its int32
-// partial sums into the tile's workspace slot with bulk reductions (TMA,
-// performed in L2), and the warp that brings the last piece of its 32-row
-// slab reads the totals back, clears them and runs the epilogue. Integer
+// split along K instead, one piece per cluster, computed before the
+// cluster's whole tiles: each piece adds its int32 partial sums into the
+// tile's workspace slot with bulk reductions (TMA, performed in L2), and the
+// warp that brings the last piece of its 32-row slab reads the totals back,
+// clears them and runs the epilogue, all while the tensor cores move on to
+// the whole tiles. Integer
 // addition is exact and associative, so the result is bit-identical to the
 // unsplit schedule and does not depend on how the rows are partitioned.
 // Nothing waits on another CTA.
@@ -178,23 +180,26 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int t, int rank, 
 // Work item i of cluster c (of nc): tile t over k blocks [kb0, kb1); piece
 // is -1 for a whole tile, else the index of the K piece of a split tile.
 // Returns false past the cluster's last item.
+// With a split, dp_tiles is a multiple of nc: every cluster has dp_tiles / nc
+// whole tiles and at most one piece. The piece comes first: its reduction,
+// and the epilogue of the last piece of each tile, then overlap the MMAs of
+// the whole tiles instead of trailing them.
 __device__ __forceinline__ bool work_item(const TcParams& p, int c, int nc, int i, int nk, int& t, int& kb0, int& kb1,
                                          int& piece) {
-  const int td = c + i * nc;
-  if (td < p.dp_tiles) {
-    t = td;
-    kb0 = 0;
-    kb1 = nk;
-    piece = -1;
+  const bool has_piece = p.sk_tiles != 0 && c < p.sk_tiles * p.sk_pieces;
+  if (has_piece && i == 0) {
+    t = p.dp_tiles + c / p.sk_pieces;
+    piece = c % p.sk_pieces;
+    kb0 = piece * nk / p.sk_pieces;
+    kb1 = (piece + 1) * nk / p.sk_pieces;
     return true;
   }
-  // with a split, dp_tiles is a multiple of nc: every cluster has dp_tiles / nc
-  // whole tiles, then at most one piece
-  if (p.sk_tiles == 0 || i != p.dp_tiles / nc || c >= p.sk_tiles * p.sk_pieces) return false;
-  t = p.dp_tiles + c / p.sk_pieces;
-  piece = c % p.sk_pieces;
-  kb0 = piece * nk / p.sk_pieces;
-  kb1 = (piece + 1) * nk / p.sk_pieces;
+  const int td = c + (has_piece ? i - 1 : i) * nc;
+  if (td >= p.dp_tiles) return false;
+  t = td;
+  kb0 = 0;
+  kb1 = nk;
+  piece = -1;
   return true;
 }
 

@@ -285,10 +285,16 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
     }
   }
 
+  long long tile = blockIdx.x;
   if (tid == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the first tile's copy is in flight during the set-up below
+    if (tile < ntiles) {
+      mbar_expect_tx(&bar[0], tile_bytes);
+      tma_load_3d(stage_base, &xmap, 0, 0, static_cast<int>(tile * R), &bar[0]);
+    }
   }
   // Row maxima cycle through three buffers. Iteration `it` uses buffer
   // it % 3 and clears (it + 1) % 3, last used two iterations earlier: every
@@ -304,12 +310,6 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   __syncthreads();
   // the line position of this thread in its block (its lines are fixed)
   const uint32_t my_signs = smem_u32(sign_tab) + static_cast<uint32_t>(((tid % lines_per_row) % C::NPOS) * 128);
-
-  long long tile = blockIdx.x;
-  if (tid == 0 && tile < ntiles) {
-    mbar_expect_tx(&bar[0], tile_bytes);
-    tma_load_3d(stage_base, &xmap, 0, 0, static_cast<int>(tile * R), &bar[0]);
-  }
 
   for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
     const int buf = it & 1;
