@@ -112,13 +112,15 @@ WORKLOADS = {
 def rq_kernel_name(wl) -> str:
     """The rotate+quantize kernel the library picks for this workload (bf16,
     aligned torch buffers, K a multiple of 64)."""
-    lane = (wl.K % 64 == 0 and K_LANE_MAX >= wl.K and
+    lines = wl.K // 64
+    parts = (lines + 255) // 256
+    lane = (wl.K % 64 == 0 and K_LANE_MAX >= wl.K and lines % parts == 0 and (parts == 1 or (lines // parts) % 8 == 0) and
             ((wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)) or
              (wl.transform == "rht" and 2 <= wl.group <= 256) or wl.transform == "none"))
     return "rq_lane_kernel" if lane else "rq_generic_kernel"
 
 
-K_LANE_MAX = 64 * 256  # the register kernel takes rows of up to 256 lines
+K_LANE_MAX = 64 * 384  # the register kernel takes rows of up to 384 lines (in up to two TMA boxes)
 
 
 def _w4(wl):
@@ -287,6 +289,20 @@ def reference_main(args, world, rank):
 
 # --------------------------------------------------------------------- GPU ---
 
+def l2_flusher(dev):
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: the written
+        # lines leave L2 (and reach DRAM) here, not inside the next timed step
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_sink)
+
+    return flush_l2
+
+
 def gpu_main(args, world, rank, local):
     import int8_convrot_w8a8_gb300 as cr
 
@@ -324,15 +340,7 @@ def gpu_main(args, world, rank, local):
     act = quant(X, use_f16)
     outs = [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
     gws = cr.gemm_workspace(dev)  # lets the GEMM split a mostly idle last round of tiles
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-
-    def flush_l2():
-        # write a buffer larger than L2, then read another one: the written
-        # lines leave L2 (and reach DRAM) here, not inside the next timed step
-        flush.zero_()
-        torch.sum(flush_rd, dim=0, out=flush_sink)
+    flush_l2 = l2_flusher(dev)
 
     def step():
         # nothing between the two launches: the GEMM is a programmatic
@@ -546,13 +554,154 @@ def gpu_main(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ DiT block ---
+
+BLOCKS = {"dit_block": lambda: WL.dit_block()}
+
+
+def block_main(args, world, rank, local):
+    """The linears of one DiT block, each group one library call from its bf16
+    input (rotate + quantize, then the GEMM as its programmatic dependent):
+    qkv (three linears sharing one packed activation), the output projection,
+    fc1 on the projection's output, fc2 on fc1's output."""
+    import int8_convrot_w8a8_gb300 as cr
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    blk = BLOCKS[args.workload]()
+    G, T = blk.group, blk.transform
+    M, D, H = blk.M, blk.D, blk.fc1.shape[0]
+
+    def prep(W):
+        return cr.convrot_prepare_weights(W.to(dev), G, T)
+
+    qkv_w, qkv_b = [prep(W) for W in blk.qkv], [b.to(dev) for b in blk.qkv_b]
+    out_w, out_b = prep(blk.out), blk.out_b.to(dev)
+    fc1_w, fc1_b = prep(blk.fc1), blk.fc1_b.to(dev)
+    fc2_w, fc2_b = prep(blk.fc2), blk.fc2_b.to(dev)
+    X, A = blk.X.to(dev), blk.A.to(dev)
+    Yqkv = [torch.empty((M, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    Yo = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+    Yh = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+    scratch = cr.int8_linear_scratch(M, max(D, H), dev)  # one scratch, reused in stream order
+    gws = cr.gemm_workspace(dev)
+    flush_l2 = l2_flusher(dev)
+    # (name, input, weights, biases, outputs)
+    layers = [("qkv", X, qkv_w, qkv_b, Yqkv), ("out_proj", A, [out_w], [out_b], [Yo]),
+              ("fc1", Yo, [fc1_w], [fc1_b], [Yh]), ("fc2", Yh, [fc2_w], [fc2_b], [Y2])]
+
+    def run(layer, s=None):
+        _, x, w, b, y = layer
+        cr.convrot_int8_linear(x, w, b, outs=y, scratch=scratch, workspace=gws, stream=s)
+
+    def step():
+        for layer in layers:
+            run(layer)
+
+    def timed(fn):
+        marks = []
+        for i in range(args.warmup + args.steps):
+            flush_l2()
+            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                marks.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in marks) / 1e3
+
+    for _ in range(args.warmup):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if cr.convrot_get_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    barrier(world)
+    with ClockSampler(local) as clocks:
+        step_s = timed(step)
+    total_s = max_over_ranks(step_s * args.steps, world)
+    # each group alone: the whole call, its GEMM on a packed activation made
+    # beforehand, and its rotate+quantize (with the fp16 operand copy)
+    per = []
+    for layer in layers:
+        name, x, w, b, y = layer
+        a = cr.convrot_quantize_act(x, G, T, with_f16=True)
+        gemm_s = timed(lambda: cr.convrot_linear_multi(a, w, b, outs=y, workspace=gws))
+        quant_s = timed(lambda: cr.convrot_quantize_act(x, G, T, with_f16=True, out=a))
+        call_s = timed(lambda: run(layer))
+        K = x.shape[1]
+        ops = 2.0 * M * K * sum(ww.N for ww in w)
+        per.append({"layer": name, "K": K, "N": [ww.N for ww in w], "call_us": call_s * 1e6,
+                    "gemm_us": gemm_s * 1e6, "gemm_tflops": ops / gemm_s / 1e12,
+                    "rotate_quant_us": quant_s * 1e6,
+                    "rotate_quant_gbs": (5.0 * M * K + 4 * M) / quant_s / 1e9, "ops": ops})
+        del a
+    torch.cuda.synchronize()
+    if cr.convrot_get_device_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    ops_step = sum(p_["ops"] for p_ in per)
+    value = world * ops_step * args.steps / total_s / 1e12
+    pk = peaks()
+    gemm_tflops = ops_step / sum(p_["gemm_us"] for p_ in per) * 1e-6
+    q_bytes = sum(5.0 * M * p_["K"] + 4 * M for p_ in per)
+    q_s = sum(p_["rotate_quant_us"] for p_ in per) / 1e6
+
+    # end to end through the public API: X and A in from pinned host memory,
+    # the qkv outputs and the block output back, every step, one stream
+    Xh, Ah = blk.X.pin_memory(), blk.A.pin_memory()
+    Yqkv_h = [torch.empty((M, D), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    Y2_h = torch.empty((M, D), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        X.copy_(Xh, non_blocking=True)
+        A.copy_(Ah, non_blocking=True)
+        step()
+        for y, yh in zip(Yqkv + [Y2], Yqkv_h + [Y2_h]):
+            yh.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(timed(e2e_step) * args.steps, world)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": blk.name, "M": M, "D": D, "mlp_width": H, "group": G, "transform": T,
+                   "seed": blk.seed, "inputs": blk.description,
+                   "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
+                   "calls": "4 x convrot_int8_linear (rotate+quantize, then the GEMM as its programmatic dependent)"},
+        "roofline": {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": gemm_tflops,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
+                     "traffic": None,
+                     "peak_note": f"{pk['source']} bf16 dense burst; the four GEMMs' flops over their summed times"},
+        "rotate_quant": {"kernel": "rq_lane_kernel", "us": q_s * 1e6, "gbs": q_bytes / q_s / 1e9,
+                         "peak_gbs": pk["hbm_gbs"], "frac": q_bytes / q_s / 1e9 / pk["hbm_gbs"],
+                         "algorithmic_bytes": q_bytes,
+                         "note": "the four rotate+quantize launches with their fp16 operand copies (5 bytes per element)"},
+        "layers": per,
+        "gpu_launches": 8 * args.steps,
+        "e2e": {"value": world * ops_step * args.steps / e2e_s / 1e12, "unit": "TOPS",
+                "h2d_bytes_per_step": 2 * 2 * M * D, "d2h_bytes_per_step": 4 * 2 * M * D,
+                "ms_per_step": 1e3 * e2e_s / args.steps, "pipelining": "none: one stream"},
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="dit6144", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="dit6144", choices=sorted(WORKLOADS) + sorted(BLOCKS))
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
@@ -564,7 +713,11 @@ def main():
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
+            if args.workload in BLOCKS:
+                ap.error("the reference arm times single-linear workloads")
             reference_main(args, world, rank)
+        elif args.workload in BLOCKS:
+            block_main(args, world, rank, local)
         else:
             gpu_main(args, world, rank, local)
     finally:

@@ -199,6 +199,44 @@ convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_pa
                                    int32_t* A, int64_t lda, void* workspace, int64_t workspace_bytes,
                                    cudaStream_t stream);
 
+/* ---- The linear from the activation, in one call ---------------------------
+ * The sglang digest's single fused op (its kitchen_int8.py excerpt: Hadamard
+ * rotation -> dynamic per-row activation quantization -> INT8 GEMM -> dequant
+ * epilogue -> bias), for n linears that share the input ("Runtime activation
+ * quantization": one packed activation feeds every linear with the same input
+ * and group size). The rotate+quantize kernel writes the packed activation
+ * into the caller's scratch; the GEMM follows as its programmatic dependent
+ * launch on the same stream. Results are bit-identical to
+ * convrot_quantize_act followed by convrot_linear_multi_ws.
+ *
+ * convrot_int8_linear_scratch_bytes: the scratch size for M rows of K: the
+ * int8 codes [M, K], the fp32 row scales [M] and, when the tensor-core path
+ * runs (M > 64, K a multiple of 64), the fp16 operand copy [M, K], each part
+ * starting on a 256-byte boundary. -1 for M < 0 or K outside [1, CONVROT_MAX_K].
+ *
+ * convrot_int8_linear:
+ *   X, M, K, ldx, group, transform, signs   as for convrot_quantize_act.
+ *   n, w, bias, Y, ldy                      as for convrot_linear_multi; every
+ *                                           w[i] must carry the same K, group
+ *                                           and transform.
+ *   scratch         device memory, 256-byte aligned, at least
+ *                   convrot_int8_linear_scratch_bytes(M, K) bytes; owned by
+ *                   the caller and overwritten by the call (it holds the
+ *                   packed activation until the GEMM has read it, so calls on
+ *                   different streams need different scratch).
+ *   workspace, workspace_bytes   the optional GEMM workspace, as for
+ *                   convrot_linear_multi_ws.
+ * Every argument is checked on the host before anything is launched: errors as
+ * for convrot_quantize_act and convrot_linear_multi_ws, plus INVALID_ARG
+ * (scratch null or too small) and ALIGNMENT (scratch). M == 0 is a no-op. */
+int64_t convrot_int8_linear_scratch_bytes(int64_t M, int64_t K);
+
+convrot_status convrot_int8_linear(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                   int32_t transform, const int8_t* signs, int32_t n,
+                                   const convrot_packed_weight* w, const float* const* bias, uint16_t* const* Y,
+                                   const int64_t* ldy, void* scratch, int64_t scratch_bytes, void* workspace,
+                                   int64_t workspace_bytes, cudaStream_t stream);
+
 /* convrot_linear_multi with the GEMM workspace held by the library instead of
  * the caller: ALLOCATES NOTHING. The pages have no counterpart; this is a
  * deployment convenience of this library.

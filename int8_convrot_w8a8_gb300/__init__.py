@@ -29,7 +29,7 @@ __all__ = [
     "convrot_linear", "convrot_linear_multi", "convrot_linear_multi_static", "convrot_gemm_s32", "gemm_workspace",
     "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
     "PackedAct4", "PackedWeight4", "convrot_prepare_weights4", "convrot_quantize_act4", "convrot_linear4",
-    "convrot_linear4_multi", "convrot_gemm4_s32",
+    "convrot_linear4_multi", "convrot_gemm4_s32", "convrot_int8_linear", "int8_linear_scratch",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -103,6 +103,9 @@ _SIGS = {
     "convrot_linear4_multi": [ctypes.POINTER(_Act4), _I32, ctypes.POINTER(_Weight4), ctypes.POINTER(_P),
                               ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P],
     "convrot_gemm4_s32": [ctypes.POINTER(_Act4), ctypes.POINTER(_Weight4), _P, _I64, _P, _I64, _P],
+    "convrot_int8_linear_scratch_bytes": [_I64, _I64],
+    "convrot_int8_linear": [_P, _I64, _I64, _I64, _I32, _I32, _P, _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
+                            ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P, _I64, _P],
     "convrot_get_device_status": [],
     "convrot_selftest_wait_timeout": [_I64, _P],
     "convrot_status_str": [_I32],
@@ -112,7 +115,8 @@ _SIGS = {
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
     _f.argtypes = _args
-    _f.restype = ctypes.c_char_p if _name in ("convrot_status_str", "convrot_last_error") else ctypes.c_int32
+    _f.restype = (ctypes.c_char_p if _name in ("convrot_status_str", "convrot_last_error") else
+                  ctypes.c_int64 if _name == "convrot_int8_linear_scratch_bytes" else ctypes.c_int32)
 
 EXPORTED = tuple(_SIGS)
 
@@ -290,6 +294,44 @@ def convrot_linear_multi_static(a: PackedAct, ws: Sequence[PackedWeight], biases
     return outs
 
 
+def int8_linear_scratch(M: int, K: int, device=None) -> torch.Tensor:
+    """A scratch buffer for convrot_int8_linear with M rows of K."""
+    nbytes = int(lib.convrot_int8_linear_scratch_bytes(M, K))
+    if nbytes < 0:
+        raise ValueError(f"no scratch size for M={M}, K={K}")
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def convrot_int8_linear(X: torch.Tensor, ws: Sequence[PackedWeight], biases: Optional[Sequence] = None,
+                        signs: Optional[torch.Tensor] = None, outs: Optional[List[torch.Tensor]] = None,
+                        scratch: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> List[torch.Tensor]:
+    """The linears sharing X, from the bf16 activation in one call: rotate +
+    per-row quantize into `scratch`, then the GEMM with the fused epilogue."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2:
+        raise TypeError("X must be a 2-D bf16 tensor")
+    if X.stride(1) != 1:
+        X = X.contiguous()
+    M, K = X.shape
+    n = len(ws)
+    if n == 0:
+        raise ValueError("at least one weight")
+    if outs is None:
+        outs = [torch.empty((M, w.N), dtype=torch.bfloat16, device=X.device) for w in ws]
+    if scratch is None:
+        scratch = int8_linear_scratch(M, K, X.device)
+    warr = (_Weight * n)(*[w._c() for w in ws])
+    barr = (ctypes.c_void_p * n)(*[(_ptr(b) if b is not None else None) for b in (biases or [None] * n)])
+    yarr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    larr = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
+    wsp = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.convrot_int8_linear(X.data_ptr(), M, K, X.stride(0), ws[0].group, ws[0].transform, _ptr(signs), n,
+                                   warr, barr, yarr, larr, scratch.data_ptr(), scratch.numel(), wsp, wsb,
+                                   _stream(stream)))
+    return outs
+
+
 def convrot_gemm_s32(a: PackedAct, w: PackedWeight, out: Optional[torch.Tensor] = None, stream=None,
                      workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Raw int32 accumulators A = Q_x Q_w^T through the linear's GEMM main loop."""
@@ -439,8 +481,9 @@ def convrot_selftest_wait_timeout(spin_limit: int, stream=None) -> None:
 class ConvRotLinear:
     """A linear layer holding prepared ConvRot weights.
 
-    ``forward`` flattens leading dimensions, quantizes the activation once and
-    runs the int8 GEMM with the fused epilogue, then restores the shape.
+    ``forward`` flattens leading dimensions and runs the linear from the
+    activation in one library call (rotate + quantize, then the int8 GEMM with
+    the fused epilogue), then restores the shape.
     """
 
     def __init__(self, packed: PackedWeight, bias: Optional[torch.Tensor], signs: Optional[torch.Tensor] = None,
@@ -460,9 +503,7 @@ class ConvRotLinear:
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         shape = x.shape
         x2 = x.reshape(-1, shape[-1])
-        a = convrot_quantize_act(x2, self.weight.group, self.weight.transform, self.signs,
-                                 with_f16=self.weight.q_f16 is not None)
-        y = convrot_linear(a, self.weight, self.bias, workspace=self.workspace)
+        y = convrot_int8_linear(x2, [self.weight], [self.bias], signs=self.signs, workspace=self.workspace)[0]
         return y.reshape(*shape[:-1], y.shape[-1])
 
     __call__ = forward

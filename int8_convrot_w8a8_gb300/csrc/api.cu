@@ -346,15 +346,17 @@ convrot_status check_workspace(const void* ws, int64_t ws_bytes) {
   return ok();
 }
 
-convrot_status linear_multi(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
-                            const float* const* bias, uint16_t* const* Y, const int64_t* ldy, void* ws,
-                            int64_t ws_bytes, cudaStream_t stream) {
+// Checks n linears against the packed activation and fills the GEMM's
+// output table; launches nothing.
+convrot_status build_outputs(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                             const float* const* bias, uint16_t* const* Y, const int64_t* ldy, void* ws,
+                             int64_t ws_bytes, GemmOutputs* outs) {
   if (n < 1 || n > kMaxLinears) return fail(CONVROT_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, kMaxLinears);
   if (!w || !Y || !ldy) return fail(CONVROT_ERR_INVALID_ARG, "w, Y and ldy arrays must be non-null");
   convrot_status s = check_workspace(ws, ws_bytes);
   if (s != CONVROT_OK) return s;
-  GemmOutputs outs{};
-  outs.count = n;
+  *outs = GemmOutputs{};
+  outs->count = n;
   for (int i = 0; i < n; ++i) {
     s = check_pair(a, &w[i]);
     if (s != CONVROT_OK) return s;
@@ -363,9 +365,35 @@ convrot_status linear_multi(const convrot_packed_act* a, int32_t n, const convro
     if (ldy[i] < w[i].N) return fail(CONVROT_ERR_INVALID_ARG, "ldy[%d] < N", i);
     if (!aligned(Y[i], 16) || ldy[i] % 8) return fail(CONVROT_ERR_ALIGNMENT, "Y[%d] alignment", i);
     if (b && !aligned(b, 16)) return fail(CONVROT_ERR_ALIGNMENT, "bias[%d] must be 16-byte aligned", i);
-    outs.o[i] = GemmOut{w[i].q, w[i].q_f16, w[i].scale, b, Y[i], ldy[i], static_cast<int>(w[i].N), 0};
+    outs->o[i] = GemmOut{w[i].q, w[i].q_f16, w[i].scale, b, Y[i], ldy[i], static_cast<int>(w[i].N), 0};
   }
+  return CONVROT_OK;
+}
+
+convrot_status linear_multi(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                            const float* const* bias, uint16_t* const* Y, const int64_t* ldy, void* ws,
+                            int64_t ws_bytes, cudaStream_t stream) {
+  GemmOutputs outs;
+  convrot_status s = build_outputs(a, n, w, bias, Y, ldy, ws, ws_bytes, &outs);
+  if (s != CONVROT_OK) return s;
   return run_gemm(a, outs, false, ws, ws_bytes, stream);
+}
+
+// The packed activation of convrot_int8_linear inside the caller's scratch:
+// int8 codes [M, K], fp32 row scales [M], and the fp16 operand copy [M, K]
+// when the tensor-core GEMM will read it; each part 256-byte aligned.
+struct ActLayout {
+  long long scale_off, f16_off, total;
+  bool f16;
+};
+ActLayout act_layout(long long M, long long K) {
+  auto up = [](long long v) { return (v + 255) / 256 * 256; };
+  ActLayout l;
+  l.scale_off = up(M * K);
+  l.f16 = gemm_tc_supported(M, static_cast<int>(K));
+  l.f16_off = l.scale_off + up(4 * M);
+  l.total = l.f16_off + (l.f16 ? up(2 * M * K) : 0);
+  return l;
 }
 
 // ---- 4-bit variant
@@ -460,6 +488,48 @@ convrot_status convrot_linear_multi_ws(const convrot_packed_act* a, int32_t n, c
                                        const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
                                        void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
   return linear_multi(a, n, w, bias, Y, ldy, workspace, workspace_bytes, stream);
+}
+
+int64_t convrot_int8_linear_scratch_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K <= 0 || K > CONVROT_MAX_K) return -1;
+  return act_layout(M, K).total;
+}
+
+convrot_status convrot_int8_linear(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                   int32_t transform, const int8_t* signs, int32_t n,
+                                   const convrot_packed_weight* w, const float* const* bias, uint16_t* const* Y,
+                                   const int64_t* ldy, void* scratch, int64_t scratch_bytes, void* workspace,
+                                   int64_t workspace_bytes, cudaStream_t stream) {
+  // every argument is checked before the first launch
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (M > 0 && !X) return fail(CONVROT_ERR_INVALID_ARG, "X is null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (transform == CONVROT_T_RHT && !signs) return fail(CONVROT_ERR_INVALID_ARG, "RHT needs the sign vector");
+  if (!aligned(X, 16) || ldx % 8) return fail(CONVROT_ERR_ALIGNMENT, "X must be 16-byte aligned and ldx a multiple of 8");
+  const ActLayout l = act_layout(M, K);
+  if (M > 0 && !scratch) return fail(CONVROT_ERR_INVALID_ARG, "scratch is null");
+  if (!aligned(scratch, 256)) return fail(CONVROT_ERR_ALIGNMENT, "scratch must be 256-byte aligned");
+  if (scratch_bytes < l.total)
+    return fail(CONVROT_ERR_INVALID_ARG, "scratch_bytes=%lld < %lld needed", static_cast<long long>(scratch_bytes),
+                l.total);
+  char* base = static_cast<char*>(scratch);
+  int8_t* q = reinterpret_cast<int8_t*>(base);
+  float* sx = reinterpret_cast<float*>(base + l.scale_off);
+  uint16_t* q16 = l.f16 ? reinterpret_cast<uint16_t*>(base + l.f16_off) : nullptr;
+  const convrot_packed_act a{q, sx, q16, M, K, group, transform};
+  GemmOutputs outs;
+  s = build_outputs(&a, n, w, bias, Y, ldy, workspace, workspace_bytes, &outs);
+  if (s != CONVROT_OK) return s;
+  if (M == 0) return ok();
+  int path = 0;
+  cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs, q, sx,
+                                  q16, 0, 127, stream, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "activation rotate/quantize launch");
+  // the GEMM is a programmatic dependent launch: its set-up and weight
+  // prefetch overlap the rotate+quantize
+  return run_gemm(&a, outs, false, workspace, workspace_bytes, stream);
 }
 
 convrot_status convrot_prepare_weights4(const void* W, int32_t w_dtype, int64_t N, int64_t K, int32_t group,

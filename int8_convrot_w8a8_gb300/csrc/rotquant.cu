@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
                                                        int R, int NT, const int8_t* __restrict__ signs,
                                                        int8_t* __restrict__ Q, float* __restrict__ S,
                                                        __half* __restrict__ Q16, float s_div, int stage_bytes,
-                                                       int tbytes, long long spin_limit) {
+                                                       int tbytes, int box_lines, long long spin_limit) {
   using C = LaneCfg<T, G>;
   // a programmatic dependent launch (the GEMM) may be scheduled now; it
   // waits for this grid to complete before it reads the codes
@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
     // the first tile's copy is in flight during the set-up below
     if (tile < ntiles) {
       mbar_expect_tx(&bar[0], tile_bytes);
-      tma_load_3d(stage_base, &xmap, 0, 0, static_cast<int>(tile * R), &bar[0]);
+      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
+        tma_load_3d(stage_base + l0 * 128, &xmap, 0, l0, static_cast<int>(tile * R), &bar[0]);
     }
   }
   // Row maxima cycle through three buffers. Iteration `it` uses buffer
@@ -320,7 +321,9 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
     // barrier: refill it with the next tile now
     if (tid == 0 && next < ntiles) {
       mbar_expect_tx(&bar[buf ^ 1], tile_bytes);
-      tma_load_3d(stage_base + (buf ^ 1) * stage_bytes, &xmap, 0, 0, static_cast<int>(next * R), &bar[buf ^ 1]);
+      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
+        tma_load_3d(stage_base + (buf ^ 1) * stage_bytes + l0 * 128, &xmap, 0, l0, static_cast<int>(next * R),
+                    &bar[buf ^ 1]);
     }
     if (!mbar_wait_bounded(&bar[buf], (it >> 1) & 1, spin_limit) && tid == 0) record_status(CONVROT_ERR_TIMEOUT);
 
@@ -603,16 +606,24 @@ template <int T, int G, int QM>
 static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, const int8_t* signs,
                                int8_t* Q, float* S, __half* Q16, cudaStream_t st, bool* launched) {
   *launched = false;
-  if (K % 64 != 0 || K / 64 > 256 || M > 0x7fffffffLL) return cudaSuccess;
+  const int lines = K / 64;
+  if (K % 64 != 0 || lines > 384 || M > 0x7fffffffLL) return cudaSuccess;
   int R = 0, NT = 0;
   if (!choose_rows(K, 64, false, &R, &NT)) return cudaSuccess;
+  // A TMA box spans at most 256 lines: wider rows (one row per tile) arrive
+  // in equal parts, each starting on a 1 KB boundary of the stage so the
+  // 128B swizzle is the same as for one copy.
+  const int parts = (lines + 255) / 256;
+  const int box_lines = lines / parts;
+  if (parts > 1 && (R != 1 || lines % parts != 0 || box_lines % 8 != 0)) return cudaSuccess;
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaSuccess;
-  // X viewed as [M][K/64][64] bf16; one box is one tile of R rows.
+  // X viewed as [M][K/64][64] bf16; one box is one tile of R rows (or a part
+  // of the one row).
   CUtensorMap map;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(M)};
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lines), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(ldx) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(K / 64), static_cast<cuuint32_t>(R)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_lines), static_cast<cuuint32_t>(R)};
   cuuint32_t estr[3] = {1, 1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(X), dims, strides, box, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -638,7 +649,7 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   const long long grid = (tiles + rounds - 1) / rounds;
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, NT, signs, Q, S, Q16,
                                                              scale_divisor(T, G, QM), stage_bytes, tbytes,
-                                                             kDefaultSpinLimit);
+                                                             box_lines, kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
 }

@@ -110,3 +110,36 @@ def test_workspace_validation(cr):
     assert b"256-byte" in cr.lib.convrot_last_error()
     assert f(ctypes.byref(act), 1, w, bias, ys, ld, 0x7000, -1, None) == 1  # negative size
     assert f(ctypes.byref(act), 0, w, bias, ys, ld, None, 0, None) == 1     # n out of range
+
+
+def test_int8_linear_scratch_size(cr):
+    f = cr.lib.convrot_int8_linear_scratch_bytes
+    up = lambda v: (v + 255) // 256 * 256
+    assert f(4, 256) == up(4 * 256) + up(16)                      # weight-stream path: no fp16 copy
+    assert f(128, 256) == up(128 * 256) + up(512) + 2 * 128 * 256  # 2-SM tensor-core path
+    assert f(128, 1040) == up(128 * 1040) + up(512)              # K not a multiple of 64: int8 MMA path
+    assert f(0, 256) == 0
+    assert f(-1, 256) == -1 and f(4, 0) == -1 and f(4, 40000) == -1
+
+
+def test_int8_linear_validation(cr):
+    w = (cr._Weight * 1)(cr._Weight(0x4000, 0x5000, None, 16, 256, 256, 0))
+    w64 = (cr._Weight * 1)(cr._Weight(0x4000, 0x5000, None, 16, 256, 64, 0))
+    bias = (ctypes.c_void_p * 1)(None)
+    ys = (ctypes.c_void_p * 1)(0x6000)
+    ld = (ctypes.c_int64 * 1)(16)
+    need = cr.lib.convrot_int8_linear_scratch_bytes(4, 256)
+    f = cr.lib.convrot_int8_linear
+
+    def call(M=4, group=256, wts=w, scratch=0x10000, nbytes=need, X=0x1000, n=1):
+        return f(X, M, 256, 256, group, 0, None, n, wts, bias, ys, ld, scratch, nbytes, None, 0, None)
+
+    assert call(scratch=0x10010) == 3                     # scratch not 256-byte aligned
+    assert b"256-byte" in cr.lib.convrot_last_error()
+    assert call(nbytes=need - 1) == 1                     # scratch too small
+    assert call(scratch=None) == 1
+    assert call(wts=w64) == 1                             # weight rotated with another group
+    assert call(group=8) == 2                             # not a power of four
+    assert call(X=0x1008) == 3                            # misaligned X
+    assert call(n=0) == 1
+    assert call(M=0, X=None, scratch=None, nbytes=0) == 0  # empty batch: no-op

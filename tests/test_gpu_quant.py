@@ -167,6 +167,22 @@ def test_quantize_act_none_register_kernel(cr, M, K):
     assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
 
 
+@pytest.mark.parametrize("M,K,G,transform", [(9, 21504, 256, "h4"), (9, 24576, 1024, "h4"), (7, 21504, 16, "h4"),
+                                               (9, 21504, 256, "rht"), (5, 21504, 0, "none"), (3, 16896, 256, "h4")])
+def test_wide_rows_register_kernel(cr, M, K, G, transform):
+    """Rows wider than one TMA box (256 lines of 64 values: an MLP width
+    such as 4 x 5376) arrive in two equal copies; codes and scales against
+    the oracle, and bit-identical to the generic kernel."""
+    wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.001, outlier_scale=50.0, group=max(G, 2),
+                      transform=transform, seed=K + G + M)
+    sg = None if wl.signs is None else wl.signs.cuda()
+    fast, gen = _fast_and_generic(cr, wl.X.cuda(), G, transform, sg)
+    Q, s, v = _oracle_act(wl.X, G, transform, wl.signs)
+    check_codes(to_np(fast.q), Q, v, f"{transform} G{G} K{K}")
+    check_scales(to_np(fast.scale), s, f"{transform} G{G} K{K}")
+    assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
+
+
 def test_quantize_act_none_matches_oracle(cr):
     wl = WL.make_case(21, 1152, [], seed=14)
     a = _run_act(cr, wl.X, 0, "none")

@@ -185,3 +185,64 @@ def k2688(seed: int = 5, M: int = 8192) -> Workload:
                   name=f"k2688_{M}x2688x2688_G64")
     w.description = "X bf16 [M,2688] Student-t(3), 0.1% channels x50; W [2688,2688]; G=64"
     return w
+
+
+@dataclasses.dataclass
+class BlockWorkload:
+    """The linears of one DiT block, chained: qkv (three linears sharing the
+    block input X), the output projection on the attention output A, then the
+    MLP pair fc1 (D -> mlp*D) and fc2 (mlp*D -> D), fc2 fed with fc1's output
+    and fc1 with the output projection's. Every layer uses the same group."""
+    name: str
+    X: torch.Tensor                 # bf16 [M, D], the block input (qkv)
+    A: torch.Tensor                 # bf16 [M, D], stand-in for the attention output
+    qkv: List[torch.Tensor]         # 3 x fp32 [D, D]
+    qkv_b: List[torch.Tensor]
+    out: torch.Tensor               # fp32 [D, D]
+    out_b: torch.Tensor
+    fc1: torch.Tensor               # fp32 [mlp*D, D]
+    fc1_b: torch.Tensor
+    fc2: torch.Tensor               # fp32 [D, mlp*D]
+    fc2_b: torch.Tensor
+    group: int
+    transform: str
+    seed: int
+    description: str = ""
+
+    @property
+    def M(self) -> int:
+        return self.X.shape[0]
+
+    @property
+    def D(self) -> int:
+        return self.X.shape[1]
+
+    def layers(self):
+        """(name, K, [N...]) of the four linear groups, in block order."""
+        D, H = self.D, self.fc1.shape[0]
+        return [("qkv", D, [D, D, D]), ("out_proj", D, [D]), ("fc1", D, [H]), ("fc2", H, [D])]
+
+
+def dit_block(seed: int = 6, M: int = 4096, D: int = 5376, mlp: int = 4) -> BlockWorkload:
+    """A MiniMax-H3-style DiT block: hidden width 5376 (the narrow out_proj /
+    fc2 output of the sglang digest's row-split note), qkv 3 x 5376, MLP ratio
+    4 (the pages give no MLP width: the common DiT ratio), G = 256, inputs as
+    for the 6144-wide DiT linear."""
+    g = _gen(seed)
+    X = draw_activations(g, M, D, "t3", 0.001, 50.0, 0, 0.0)
+    A = draw_activations(g, M, D, "t3", 0.001, 50.0, 0, 0.0)
+
+    def lin(n, k):
+        return (torch.randn((n, k), generator=g, dtype=torch.float32) * 0.02,
+                torch.randn((n,), generator=g, dtype=torch.float32) * 0.01)
+
+    qkv = [lin(D, D) for _ in range(3)]
+    out, out_b = lin(D, D)
+    fc1, fc1_b = lin(mlp * D, D)
+    fc2, fc2_b = lin(D, mlp * D)
+    b = BlockWorkload(f"dit_block_{M}x{D}_mlp{mlp}_G256", X, A, [w for w, _ in qkv], [bb for _, bb in qkv],
+                      out, out_b, fc1, fc1_b, fc2, fc2_b, 256, TRANSFORM_H4, seed)
+    b.description = (f"X, A bf16 [{M},{D}] Student-t(3), 0.1% channels x50; qkv 3x[{D},{D}], out_proj "
+                     f"[{D},{D}], fc1 [{mlp * D},{D}], fc2 [{D},{mlp * D}] ~N(0,0.02^2); biases ~N(0,0.01^2); "
+                     "G=256; fc1 reads out_proj's output, fc2 reads fc1's")
+    return b
