@@ -3,7 +3,10 @@
 One step = one pass of the runtime path over one batch: the fused
 rotate + row-absmax + quantize kernel on X, then the int8 GEMM with the
 fused dequant/bias/bf16 epilogue for every linear that shares the packed
-activation. Weights are prepared once before timing (the offline path).
+activation; for 8-bit codes both through one public call
+(convrot_int8_linear), for 4-bit codes through the quantize and linear
+calls. Weights are prepared once before timing (the offline path).
+`--workload dit_block` chains the linears of one DiT block instead.
 
 Timing: W warm-up steps, then K timed steps; each step is bracketed by CUDA
 events on the launching stream (the GEMM is a programmatic dependent launch
@@ -341,12 +344,24 @@ def gpu_main(args, world, rank, local):
     outs = [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
     gws = cr.gemm_workspace(dev)  # lets the GEMM split a mostly idle last round of tiles
     flush_l2 = l2_flusher(dev)
+    # 8-bit steps go through the one-call linear (rotate+quantize, then the
+    # GEMM as its programmatic dependent)
+    one_call = None
+    if bits == 8:
+        scratch = cr.int8_linear_scratch(M, K, dev)
+
+        def one_call(Xq, outs_, scratch_, workspace, stream=None):
+            cr.convrot_int8_linear(Xq, ws, bs, signs=sg, outs=outs_, scratch=scratch_, workspace=workspace,
+                                   stream=stream)
 
     def step():
-        # nothing between the two launches: the GEMM is a programmatic
-        # dependent of the rotate+quantize and may start while it finishes
-        quant(X, use_f16, out=act)
-        lin(act, outs, gws)
+        if one_call is not None:
+            one_call(X, outs, scratch, gws)
+        else:
+            # nothing between the two launches: the GEMM is a programmatic
+            # dependent of the rotate+quantize and may start while it finishes
+            quant(X, use_f16, out=act)
+            lin(act, outs, gws)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for _ in range(args.warmup):
@@ -471,6 +486,7 @@ def gpu_main(args, world, rank, local):
         Xd = torch.empty_like(X)
         bufs.append({"X": Xd,
                      "act": quant(Xd.zero_(), use_f16),
+                     "scratch": cr.int8_linear_scratch(M, K, dev) if one_call is not None else None,
                      "Y": [torch.empty((M, n), dtype=torch.bfloat16, device=dev) for n in Ns],
                      "ws": cr.gemm_workspace(dev),
                      "Yh": [torch.empty((M, n), dtype=torch.bfloat16).pin_memory() for n in Ns]})
@@ -479,8 +495,11 @@ def gpu_main(args, world, rank, local):
         b, s = bufs[i % nbuf], e2e_streams[i % nbuf]
         with torch.cuda.stream(s):
             b["X"].copy_(Xh, non_blocking=True)
-            quant(b["X"], use_f16, out=b["act"], stream=s)
-            lin(b["act"], b["Y"], b["ws"], stream=s)
+            if one_call is not None:
+                one_call(b["X"], b["Y"], b["scratch"], b["ws"], stream=s)
+            else:
+                quant(b["X"], use_f16, out=b["act"], stream=s)
+                lin(b["act"], b["Y"], b["ws"], stream=s)
             for y, yh in zip(b["Y"], b["Yh"]):
                 yh.copy_(y, non_blocking=True)
 
@@ -514,7 +533,9 @@ def gpu_main(args, world, rank, local):
                    "seed": wl.seed, "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
                    "inputs": wl.description,
                    "gemm_path": ("tcgen05 e4m3-exact (kind::f8f6f4)" if bits == 4 else
-                                 "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)")},
+                                 "tcgen05 fp16-exact" if use_f16 else "int8 weight stream (TMA + mma.sync s8)"),
+                   "step": ("convrot_int8_linear" if one_call is not None else
+                            "convrot_quantize_act4 + convrot_linear4_multi")},
         "roofline": dominant,
         "rotate_quant": {"kernel": rq_kernel_name(wl),
                          "us": quant_only_s * 1e6, "gbs": quant_gbs, "peak_gbs": pk["hbm_gbs"],

@@ -27,6 +27,14 @@ CASES = [
     # M, K, Ns, transform, group
     (1, 256, [256], WL.TRANSFORM_H4, 256),
     (16, 1152, [512, 384], WL.TRANSFORM_RHT, 128),
+    (5, 1152, [256, 96], WL.TRANSFORM_RHT, 64),
+    (1, 128, [64], WL.TRANSFORM_RHT, 128),
+    (16, 1024, [512], WL.TRANSFORM_H4, 64),
+    (3, 640, [296], WL.TRANSFORM_H4, 16),
+    (16, 1536, [256], WL.TRANSFORM_H4, 4),
+    (12, 1280, [256], WL.TRANSFORM_NONE, 256),
+    (16, 1280, [512], WL.TRANSFORM_RHT, 256),
+    (16, 1664, [256], WL.TRANSFORM_H4, 64),
     (48, 1152, [256, 136], WL.TRANSFORM_RHT, 128),
     (300, 512, [512, 272], WL.TRANSFORM_H4, 64),
     (1000, 1024, [768], WL.TRANSFORM_NONE, 256),
@@ -77,6 +85,23 @@ def test_scratch_layout_and_reuse(cr):
     Y2 = cr.convrot_int8_linear(X2, [w], scratch=scratch)[0]
     assert torch.equal(Y2, cr.convrot_int8_linear(X2, [w])[0])
     assert torch.equal(Y, cr.convrot_linear(a, w))
+
+
+@pytest.mark.parametrize("M,K,G,transform", [(16, 1152, 128, "rht"), (7, 1024, 64, "h4"), (2, 512, 0, "none")])
+def test_small_m_writes_the_packed_activation(cr, M, K, G, transform):
+    """With a handful of rows the scratch receives the packed activation too
+    (codes and scales, no fp16 copy), equal to convrot_quantize_act's."""
+    wl = WL.make_case(M, K, [128], transform=transform, group=max(G, 2), seed=13, name="small_m")
+    sg = None if wl.signs is None else wl.signs.cuda()
+    w = cr.convrot_prepare_weights(wl.weights[0].cuda(), G, transform, sg)
+    X = wl.X.cuda()
+    scratch = cr.int8_linear_scratch(M, K)
+    cr.convrot_int8_linear(X, [w], signs=sg, scratch=scratch)
+    a = cr.convrot_quantize_act(X, G, transform, sg, with_f16=False)
+    torch.cuda.synchronize()
+    assert torch.equal(scratch[: M * K].view(torch.int8).view(M, K), a.q)
+    off = (M * K + 255) // 256 * 256
+    assert torch.equal(scratch[off: off + 4 * M].view(torch.float32), a.scale)
 
 
 @pytest.mark.parametrize("case", ["dit", "ffn_rht", "g16"])
