@@ -187,8 +187,10 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
 //    after the quad transpose), fp16 copies as 32-byte stores: whole sectors.
 
 // T: the transform; G: the group (regular Hadamard) or block (randomized
-// Hadamard) size; the naive variant takes G = 1.
-template <int T, int G>
+// Hadamard) size; the naive variant takes G = 1. XQ: the randomized
+// Hadamard's cross-line stages through the quad transpose (rows of a
+// multiple of 4 lines), else by shuffles.
+template <int T, int G, bool XQ>
 struct LaneCfg {
   static constexpr bool H4 = T == CONVROT_T_REGULAR_H4;
   static constexpr bool RHT = T == CONVROT_T_RHT;
@@ -203,6 +205,9 @@ struct LaneCfg {
   // line positions with distinct sign patterns (randomized Hadamard)
   static constexpr int NPOS = RHT && G > 64 ? G / 64 : 1;
   static_assert(NX <= 2 && NBX <= 2, "G <= 1024 (regular) or B <= 256 (randomized)");
+  // the quad transpose runs: regular Hadamard digit 3, or the randomized
+  // Hadamard's strides 64 and 128
+  static constexpr bool QT = (H4 && NX >= 1) || (RHT && NBX >= 1 && XQ);
 };
 
 // One radix-2 Walsh-Hadamard stage across lanes (partner lane ^ MASK): the
@@ -232,13 +237,13 @@ __device__ __forceinline__ float2 h4_xlane(float2 x) {
   return f2_add(u, w);
 }
 
-template <int T, int G, int QM>
+template <int T, int G, int QM, bool XQ>
 __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CUtensorMap xmap, long long M, int K,
                                                        int R, int NT, const int8_t* __restrict__ signs,
                                                        int8_t* __restrict__ Q, float* __restrict__ S,
                                                        __half* __restrict__ Q16, float s_div, int stage_bytes,
                                                        int tbytes, int box_lines, long long spin_limit) {
-  using C = LaneCfg<T, G>;
+  using C = LaneCfg<T, G, XQ>;
   // a programmatic dependent launch (the GEMM) may be scheduled now; it
   // waits for this grid to complete before it reads the codes
   asm volatile("griddepcontrol.launch_dependents;");
@@ -265,16 +270,17 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   const int row_first = __shfl_sync(0xffffffffu, my_row, 0);
   const bool warp_one_row = __all_sync(0xffffffffu, my_row == row_first);
 
-  // Quad transpose (G >= 256): the 4 lanes of a quad own the 4 lines of a
-  // group. Each writes its line (fp32, 16 chunks of 16 bytes) and reads back
-  // the 16-element run at offset 16a (a = lane & 3) of all 4 lines, so the
-  // group's digit 3 (the line) becomes a register index. Chunk c of line l
-  // sits at chunk c ^ (bitrev3(l mod 8) ^ ((c >> 3) << 1)) of its 256-byte
-  // slot: conflict-free for the line writes and for the transposed reads.
+  // Quad transpose (regular Hadamard G >= 256, randomized Hadamard B >= 128
+  // on rows of 4k lines): the 4 lanes of a quad own 4 consecutive lines. Each
+  // writes its line (fp32, 16 chunks of 16 bytes) and reads back the
+  // 16-element run at offset 16a (a = lane & 3) of all 4 lines, so the line
+  // index becomes a register index. Chunk c of line l sits at chunk
+  // c ^ (bitrev3(l mod 8) ^ ((c >> 3) << 1)) of its 256-byte slot:
+  // conflict-free for the line writes and for the transposed reads.
   const int qa = tid & 3;
   uint32_t t_wr = 0;      // write base, XOR-ed with the compile-time part of the swizzle
   uint32_t t_rd[4] = {};  // read base of line (tid & ~3) + r, XOR-ed likewise
-  if constexpr (C::NX >= 1) {
+  if constexpr (C::QT) {
     auto bitrev3 = [](int x) { return ((x & 1) << 2) | (x & 2) | ((x >> 2) & 1); };
     t_wr = (tbuf + (static_cast<uint32_t>(tid) << 8)) | (static_cast<uint32_t>(bitrev3(tid & 7)) << 4);
 #pragma unroll
@@ -370,9 +376,9 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
 #pragma unroll
       for (int o = 0; o < 8; ++o) h4_stage(v[o], v[o + 8], v[o + 16], v[o + 24]);
     }
-    // ---- digit 3 through the quad transpose, then in registers: after it
-    // v[8r + i] holds elements 16a + 2i, +1 of line (tid & ~3) + r
-    if constexpr (C::NX >= 1) {
+    // after the quad transpose v[8r + i] holds elements 16a + 2i, +1 of line
+    // (tid & ~3) + r
+    auto quad_transpose = [&]() {
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const uint32_t addr = t_wr ^ (static_cast<uint32_t>(k ^ ((k >> 3) << 1)) << 4);
@@ -393,6 +399,10 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
           v[8 * r + 2 * c] = make_float2(f.x, f.y);
           v[8 * r + 2 * c + 1] = make_float2(f.z, f.w);
         }
+    };
+    // ---- digit 3 through the quad transpose, then in registers
+    if constexpr (C::H4 && C::NX >= 1) {
+      quad_transpose();
 #pragma unroll
       for (int i = 0; i < 8; ++i) h4_stage(v[i], v[8 + i], v[16 + i], v[24 + i]);
     }
@@ -425,13 +435,36 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
         }
       }
     }
-    if constexpr (C::NBX >= 1) {
+    if constexpr (C::RHT && C::QT) {
+      // strides 64 and 128 (lines r ^ 1, r ^ 2) in registers after the transpose
+      quad_transpose();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = wht_xlane<1>(v[i], lane);
-    }
-    if constexpr (C::NBX >= 2) {
+      for (int r = 0; r < 4; r += 2)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = wht_xlane<2>(v[i], lane);
+        for (int i = 0; i < 8; ++i) {
+          const float2 a = v[8 * r + i], b = v[8 * (r + 1) + i];
+          v[8 * r + i] = f2_add(a, b);
+          v[8 * (r + 1) + i] = f2_sub(a, b);
+        }
+      if constexpr (C::NBX >= 2) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 a = v[8 * r + i], b = v[8 * (r + 2) + i];
+            v[8 * r + i] = f2_add(a, b);
+            v[8 * (r + 2) + i] = f2_sub(a, b);
+          }
+      }
+    } else {
+      if constexpr (C::NBX >= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = wht_xlane<1>(v[i], lane);
+      }
+      if constexpr (C::NBX >= 2) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = wht_xlane<2>(v[i], lane);
+      }
     }
 
     // ---- row absmax
@@ -476,7 +509,7 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
         }
       };
       if (tile_e + (static_cast<long long>(tid) << 6) < total_elems) {
-        if constexpr (C::NX >= 1) {
+        if constexpr (C::QT) {
 #pragma unroll
           for (int r = 0; r < 4; ++r)
             emit16_w4(8 * r, tile_e + (static_cast<long long>((tid & ~3) + r) << 6) + 16 * qa);
@@ -519,7 +552,7 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
         }
       };
       if (tile_e + (static_cast<long long>(tid) << 6) < total_elems) {
-        if constexpr (C::NX >= 1) {
+        if constexpr (C::QT) {
 #pragma unroll
           for (int r = 0; r < 4; ++r)
             emit16(8 * r, tile_e + (static_cast<long long>((tid & ~3) + r) << 6) + 16 * qa);
@@ -602,8 +635,8 @@ static bool choose_rows(int K, int ept, bool phase_c, int* R_out, int* NT_out) {
   return true;
 }
 
-template <int T, int G, int QM>
-static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, const int8_t* signs,
+template <int T, int G, int QM, bool XQ>
+static cudaError_t launch_lane_x(const __nv_bfloat16* X, long long M, int K, long long ldx, const int8_t* signs,
                                int8_t* Q, float* S, __half* Q16, cudaStream_t st, bool* launched) {
   *launched = false;
   const int lines = K / 64;
@@ -632,9 +665,10 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
   const int threads = (NT + 31) / 32 * 32;
   const int stage_bytes = ((R * K * 2 + 1023) / 1024) * 1024;
   // the quad transpose needs 256 bytes per thread (one fp32 line)
-  const int tbytes = LaneCfg<T, G>::NX >= 1 ? threads * 256 : 0;
-  const int smem = 1024 + 2 * stage_bytes + tbytes + ((3 * R + 1) & ~1) * 4 + 2 * 8 + 16 + LaneCfg<T, G>::NPOS * 128;
-  auto kern = rq_lane_kernel<T, G, QM>;
+  using C = LaneCfg<T, G, XQ>;
+  const int tbytes = C::QT ? threads * 256 : 0;
+  const int smem = 1024 + 2 * stage_bytes + tbytes + ((3 * R + 1) & ~1) * 4 + 2 * 8 + 16 + C::NPOS * 128;
+  auto kern = rq_lane_kernel<T, G, QM, XQ>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -652,6 +686,18 @@ static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long 
                                                              box_lines, kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
+}
+
+// The randomized Hadamard's strides 64 and 128 go through the quad
+// transpose when a row is a whole number of quads (K a multiple of 256): the
+// stores then fill whole lines, as on the regular Hadamard path.
+template <int T, int G, int QM>
+static cudaError_t launch_lane(const __nv_bfloat16* X, long long M, int K, long long ldx, const int8_t* signs,
+                               int8_t* Q, float* S, __half* Q16, cudaStream_t st, bool* launched) {
+  if constexpr (T == CONVROT_T_RHT && G >= 128) {
+    if (K % 256 == 0) return launch_lane_x<T, G, QM, true>(X, M, K, ldx, signs, Q, S, Q16, st, launched);
+  }
+  return launch_lane_x<T, G, QM, false>(X, M, K, ldx, signs, Q, S, Q16, st, launched);
 }
 
 // Entry used by the ABI layer. Returns a cudaError_t; *path tells which

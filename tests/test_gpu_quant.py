@@ -139,7 +139,8 @@ def _fast_and_generic(cr, X, G, transform, signs=None):
 
 
 @pytest.mark.parametrize("M,K,B", [(37, 1152, 2), (37, 1152, 8), (37, 1152, 32), (37, 1152, 64),
-                                   (37, 1152, 128), (37, 2048, 256), (300, 4096, 256), (1, 256, 256)])
+                                   (37, 1152, 128), (37, 2048, 128), (300, 4096, 128), (37, 2048, 256),
+                                   (300, 4096, 256), (1, 256, 256), (3, 21504, 128)])
 def test_quantize_act_rht_register_kernel(cr, M, K, B):
     """Block randomized Hadamard on the register kernel (signs applied to the
     bf16 bits, radix-2 stages in registers and across lanes): codes and

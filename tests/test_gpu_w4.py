@@ -35,7 +35,8 @@ def _oracle4(X_bf16, G, transform, signs=None):
 
 @pytest.mark.parametrize("M,K,G,transform", [
     (37, 6144, 256, "h4"), (33, 4096, 16, "h4"), (33, 4096, 64, "h4"), (33, 4096, 1024, "h4"),
-    (16, 1152, 128, "rht"), (21, 2048, 256, "rht"), (9, 1152, 0, "none"), (1, 128, 4, "h4"), (300, 3072, 256, "h4"),
+    (16, 1152, 128, "rht"), (21, 2048, 128, "rht"), (21, 2048, 256, "rht"), (9, 1152, 0, "none"), (1, 128, 4, "h4"),
+    (300, 3072, 256, "h4"),
 ])
 def test_quantize_act4_matches_oracle_on_both_kernels(cr, M, K, G, transform):
     wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.002, outlier_scale=40.0, group=max(G, 2),
