@@ -18,8 +18,8 @@
 // c drains. The 4-bit codes of the W4A4 variant ("feat: load ConvRot int4
 // and per-channel int8 safetensors", "Solution": values in [-7, 7]) enter as
 // e4m3 (exact) through kind::f8f6f4 at twice the fp16 rate; a 128-byte stage
-// row then holds 128 K values, and |q*q| <= 49 keeps every partial sum of a
-// 2048-long chunk exact.
+// row then holds 128 K values, and |q*q| <= 49 keeps every partial sum of any
+// supported K exact, so a tile accumulates in one chunk.
 //
 // Structure (one persistent CTA per SM, 320 threads; CTA pairs when M > 128):
 //   warp 0      TMA producer: 128 A rows and BN / CL B rows per stage (128
@@ -68,8 +68,13 @@ using namespace tc;
 constexpr int BM = 128;
 constexpr int BK = 64;           // fp16 elements per stage row = 128 bytes = one swizzle atom
 constexpr int BK8 = 128;         // e4m3 elements per stage row (4-bit variant)
-constexpr int KCHUNK = 1024;     // exact fp32 accumulation span (see above)
+constexpr int KCHUNK = 1024;     // exact fp32 accumulation span of int8 codes (see above)
 constexpr int KITER_PER_CHUNK = KCHUNK / BK;
+// Stage rows per TMEM chunk. 4-bit codes: |q*q| <= 49, so a partial sum stays
+// below 2^24 (exact in fp32) for any K up to 342 000 > CONVROT_MAX_K: one
+// chunk per tile, drained once.
+template <bool F8>
+constexpr int kiter_per_chunk() { return F8 ? (1 << 30) : KITER_PER_CHUNK; }
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr int TMEM_COLS = 512;
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-          const int kend = min(kb + KITER_PER_CHUNK, kb1);
+          const int kend = min(kb + kiter_per_chunk<F8>(), kb1);
           const int kstart = kb;
           for (; kb < kend; ++kb, ++it) {
             const int s = it % C::STAGES, round = it / C::STAGES;
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     for (int i = 0; ok && work_item(p, cluster_id, nclusters, i, nk, t, kb0, kb1, pc); ++i) {
       int m_blk, n_glob, li, n_local;
       decode_tile<CL>(p, t, rank, m_blk, n_glob, li, n_local);
-      const int nch = (kb1 - kb0 + KITER_PER_CHUNK - 1) / KITER_PER_CHUNK;
+      const int nch = (kb1 - kb0 + kiter_per_chunk<F8>() - 1) / kiter_per_chunk<F8>();
       const GemmOut& o = p.outs.o[li];
       const long long m = static_cast<long long>(m_blk) * BM + row_in_tile;
       const int nb = n_local * BN + col0;
