@@ -235,7 +235,7 @@ convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw
 
 extern "C" {
 
-int32_t convrot_version(void) { return 101; }
+int32_t convrot_version(void) { return 102; }
 
 const char* convrot_status_str(convrot_status s) {
   switch (s) {

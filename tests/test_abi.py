@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(cr):
 
 
 def test_version_and_status_strings(cr):
-    assert cr.lib.convrot_version() == 101
+    assert cr.lib.convrot_version() == 102
     for code in range(6):
         assert cr.lib.convrot_status_str(code)
     assert cr.lib.convrot_status_str(99) == b"unknown status"
