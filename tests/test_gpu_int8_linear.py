@@ -134,3 +134,33 @@ def test_layer_forward_uses_the_one_call_path(cr):
     ref = cr.convrot_linear(a, layer.weight, layer.bias)
     assert y.shape == (2, 48, 512)
     assert torch.equal(y.reshape(96, 512), ref)
+
+
+def test_one_call_strided_input_and_empty_batch(cr):
+    """X given as a column slice of a wider buffer (row stride > K), and an
+    empty batch, through the one-call linear."""
+    wl = WL.make_case(130, 1024, [256], group=64, seed=14, name="strided")
+    w = cr.convrot_prepare_weights(wl.weights[0].cuda(), 64, "h4")
+    wide = torch.zeros(130, 1024 + 64, dtype=torch.bfloat16, device="cuda")
+    wide[:, 32:32 + 1024] = wl.X.cuda()
+    Xs = wide[:, 32:32 + 1024]
+    assert Xs.stride(0) == 1088
+    Y = cr.convrot_int8_linear(Xs, [w])[0]
+    a = cr.convrot_quantize_act(wl.X.cuda(), 64, "h4")
+    assert torch.equal(Y, cr.convrot_linear(a, w))
+    E = cr.convrot_int8_linear(torch.empty(0, 1024, dtype=torch.bfloat16, device="cuda"), [w])[0]
+    assert E.shape == (0, 256)
+
+
+def test_one_call_wide_rows(cr):
+    """An MLP-width input (K = 21504, wider than one TMA box of the
+    rotate+quantize kernel) through the one-call linear on the tensor cores."""
+    wl = WL.make_case(300, 21504, [256], group=256, seed=15, name="wide")
+    w = cr.convrot_prepare_weights(wl.weights[0].cuda(), 256, "h4")
+    X = wl.X.cuda()
+    Y = cr.convrot_int8_linear(X, [w], workspace=cr.gemm_workspace())[0]
+    a = cr.convrot_quantize_act(X, 256, "h4")
+    assert torch.equal(Y, cr.convrot_linear(a, w))
+    sgn = None
+    Qx, sx, v = O.quantize_act(wl.X.float().numpy().astype(np.float64), 256, "h4", sgn)
+    check_codes(to_np(a.q), Qx, v, "wide")
