@@ -213,6 +213,9 @@ convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_pa
  * int8 codes [M, K], the fp32 row scales [M] and, when the tensor-core path
  * runs (M > 64, K a multiple of 64), the fp16 operand copy [M, K], each part
  * starting on a 256-byte boundary. -1 for M < 0 or K outside [1, CONVROT_MAX_K].
+ * When that path runs and every weight has its fp16 copy, the GEMM reads only
+ * the fp16 copy and the int8 codes are not written (their region is left as
+ * it was).
  *
  * convrot_int8_linear:
  *   X, M, K, ldx, group, transform, signs   as for convrot_quantize_act.

@@ -523,9 +523,14 @@ convrot_status convrot_int8_linear(const void* X, int64_t M, int64_t K, int64_t 
   s = build_outputs(&a, n, w, bias, Y, ldy, workspace, workspace_bytes, &outs);
   if (s != CONVROT_OK) return s;
   if (M == 0) return ok();
+  // the 2-SM tensor-core GEMM reads only the fp16 copy: the int8 codes are
+  // then not written (run_gemm takes that path exactly when every weight has
+  // its fp16 copy and the activation's is there)
+  bool tc_only = q16 != nullptr;
+  for (int i = 0; i < n; ++i) tc_only = tc_only && w[i].q_f16 != nullptr;
   int path = 0;
-  cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs, q, sx,
-                                  q16, 0, 127, stream, &path);
+  cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs,
+                                  tc_only ? nullptr : q, sx, q16, 0, 127, stream, &path);
   if (e != cudaSuccess) return cuda_fail(e, "activation rotate/quantize launch");
   // the GEMM is a programmatic dependent launch: its set-up and weight
   // prefetch overlap the rotate+quantize

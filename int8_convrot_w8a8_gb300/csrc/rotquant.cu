@@ -137,10 +137,10 @@ __global__ void __launch_bounds__(256) rq_generic_kernel(const Tin* __restrict__
     const float amax = red[0];
     const float inv = amax > 0.0f ? static_cast<float>(qm) / amax : 0.0f;
     if (qm == 127) {
-      int8_t* q = Q + row * (long long)K;
+      int8_t* q = Q ? Q + row * (long long)K : nullptr;
       for (int i = tid; i < K; i += nt) {
         const int c = code_from_magic(fmaf(buf[i], inv, kRoundMagic));
-        q[i] = static_cast<int8_t>(c);
+        if (q) q[i] = static_cast<int8_t>(c);
         if (Q16) Q16[row * (long long)K + i] = __int2half_rn(c);
       }
     } else {
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
             v[p0 + 2 * k + 1] = f2_sub(t23, mg2);
           }
         }
-        stg_128(Q + e, make_uint4(words[0], words[1], words[2], words[3]));
+        if (Q) stg_128(Q + e, make_uint4(words[0], words[1], words[2], words[3]));
         if (Q16) {
           uint32_t hw[8];
 #pragma unroll
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
                 v[16 * h + 2 * k + 1] = f2_sub(t23, mg2);
               }
             }
-            stg_256(Q + e0 + 32 * h, words);
+            if (Q) stg_256(Q + e0 + 32 * h, words);
           }
           if (Q16) {
 #pragma unroll
@@ -734,8 +734,9 @@ static cudaError_t launch_lane_any(const __nv_bfloat16* xb, long long M, int K, 
   return launch_lane<CONVROT_T_NONE, 1, QM>(xb, M, K, ldx, signs, Q, S, q16, st, launched);
 }
 
-// qm = 127: int8 codes (Q) and fp16 copy (Q16); qm = 7: packed 4-bit codes
-// (Q, K / 2 bytes per row) and e4m3 copy (Q16 as bytes).
+// qm = 127: int8 codes (Q) and fp16 copy (Q16), either but not both may be
+// null; qm = 7: packed 4-bit codes (Q, K / 2 bytes per row) and e4m3 copy
+// (Q16 as bytes).
 cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, long long ldx, int G, int transform,
                             const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic, int qm,
                             cudaStream_t st, int* path) {

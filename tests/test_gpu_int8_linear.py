@@ -23,6 +23,16 @@ def cr():
     return cr
 
 
+def _scratch_codes(scratch, M, K):
+    """The codes the GEMM read: the int8 region, or with the 2-SM tensor-core
+    path (M > 64, K a multiple of 64) the fp16 copy."""
+    up = lambda v: (v + 255) // 256 * 256
+    if M > 64 and K % 64 == 0:
+        off16 = up(M * K) + up(4 * M)
+        return scratch[off16: off16 + 2 * M * K].view(torch.float16).view(M, K).to(torch.int8)
+    return scratch[: M * K].view(torch.int8).view(M, K)
+
+
 CASES = [
     # M, K, Ns, transform, group
     (1, 256, [256], WL.TRANSFORM_H4, 256),
@@ -64,8 +74,8 @@ def test_one_call_equals_two_calls(cr, M, K, Ns, transform, group, use_ws):
 
 def test_scratch_layout_and_reuse(cr):
     """The scratch holds the packed activation: codes, scales, and the fp16
-    copy only when the 2-SM tensor-core path runs; one scratch serves
-    successive calls on a stream."""
+    copy when the 2-SM tensor-core path runs (which then needs no codes);
+    one scratch serves successive calls on a stream."""
     K = 512
     for M, f16 in [(16, False), (64, False), (65, True), (300, True)]:
         up = lambda v: (v + 255) // 256 * 256
@@ -77,10 +87,12 @@ def test_scratch_layout_and_reuse(cr):
     X = wl.X.cuda()
     a = cr.convrot_quantize_act(X, 64, "h4")
     Y = cr.convrot_int8_linear(X, [w], scratch=scratch)[0]
-    # the scratch now holds the same packed activation
-    assert torch.equal(scratch[: 300 * K].view(torch.int8).view(300, K), a.q)
+    # the scratch now holds the same scales and fp16 copy (the tensor-core GEMM
+    # reads only the fp16 copy, so the int8 codes are not written)
     off = (300 * K + 255) // 256 * 256
     assert torch.equal(scratch[off: off + 4 * 300].view(torch.float32), a.scale)
+    off16 = off + (4 * 300 + 255) // 256 * 256
+    assert torch.equal(scratch[off16: off16 + 2 * 300 * K].view(torch.float16).view(300, K), a.q_f16)
     X2 = X.flip(0).contiguous()
     Y2 = cr.convrot_int8_linear(X2, [w], scratch=scratch)[0]
     assert torch.equal(Y2, cr.convrot_int8_linear(X2, [w])[0])
@@ -118,7 +130,7 @@ def test_one_call_end_to_end(cr, case):
     sgn = None if wl.signs is None else wl.signs.numpy()
     X64 = wl.X.float().numpy().astype(np.float64)
     Qx, sx, v = O.quantize_act(X64, wl.group, wl.transform, sgn)
-    check_codes(to_np(scratch[: wl.M * wl.K].view(torch.int8).view(wl.M, wl.K)), Qx, v, case)
+    check_codes(to_np(_scratch_codes(scratch, wl.M, wl.K)), Qx, v, case)
     for i, Y in enumerate(Ys):
         Qw, sw, _ = O.prepare_weights(wl.weights[i].numpy().astype(np.float64), wl.group, wl.transform, sgn)
         ref = O.reconstruct(O.int_gemm(Qx, Qw), sx, sw, wl.biases[i].numpy())
