@@ -208,7 +208,17 @@ struct LaneCfg {
   // the quad transpose runs: regular Hadamard digit 3, or the randomized
   // Hadamard's strides 64 and 128
   static constexpr bool QT = (H4 && NX >= 1) || (RHT && NBX >= 1 && XQ);
+  // regular Hadamard: pair (v[2j], v[2j + 1]) holds elements (4j, 4j + 2) and
+  // (4j + 1, 4j + 3), so digit 0 runs on packed pairs too; otherwise the pairs
+  // hold (4j, 4j + 1) and (4j + 2, 4j + 3)
+  static constexpr bool SPLIT = H4;
 };
+
+// Elements 4j .. 4j + 3, in order, from the pairs v[2j], v[2j + 1].
+template <bool SPLIT>
+__device__ __forceinline__ float4 elems4(float2 a, float2 b) {
+  return SPLIT ? make_float4(a.x, b.x, a.y, b.y) : make_float4(a.x, a.y, b.x, b.y);
+}
 
 // One radix-2 Walsh-Hadamard stage across lanes (partner lane ^ MASK): the
 // lower lane of the pair gets a + b, the upper one a - b (a the lower value),
@@ -308,6 +318,14 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   // thread has passed the barrier of iteration it - 1, so every thread has
   // finished reading it.
   for (int i = tid; i < 3 * R; i += blockDim.x) rowmax_buf[i] = 0u;
+  // the slots of threads past NT (padding to whole warps) never receive a
+  // line: they hold zeros, so every thread loads its slot unconditionally
+  for (int i = NT * 8 + tid; i < static_cast<int>(blockDim.x) * 8; i += blockDim.x) {
+    const uint32_t z = 0u;
+    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(stage_base + 16u * i), "r"(z) : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(stage_base + stage_bytes + 16u * i), "r"(z)
+                 : "memory");
+  }
   if constexpr (C::RHT) {
     for (int i = tid; i < C::NPOS * 32; i += blockDim.x) {
       const int e = ((i >> 5) * 64 + 2 * (i & 31)) & (G - 1);  // element of the block
@@ -339,31 +357,47 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
       const uint32_t lb = stage_base + buf * stage_bytes + (static_cast<uint32_t>(tid) << 7);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-        if (active) {
-          const uint32_t addr = lb + ((k ^ (tid & 7)) << 4);
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
-          if constexpr (C::RHT) {
-            uint32_t m0, m1, m2, m3;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
-                         : "r"(my_signs + 16 * k));
-            w0 ^= m0;
-            w1 ^= m1;
-            w2 ^= m2;
-            w3 ^= m3;
-          }
+        // every thread has a slot; the slots of threads past NT hold zeros
+        uint32_t w0, w1, w2, w3;
+        const uint32_t addr = lb + ((k ^ (tid & 7)) << 4);
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
+        if constexpr (C::RHT) {
+          uint32_t m0, m1, m2, m3;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(m0), "=r"(m1), "=r"(m2), "=r"(m3)
+                       : "r"(my_signs + 16 * k));
+          w0 ^= m0;
+          w1 ^= m1;
+          w2 ^= m2;
+          w3 ^= m3;
         }
-        v[4 * k + 0] = make_float2(bf16lo_f32(w0), bf16hi_f32(w0));
-        v[4 * k + 1] = make_float2(bf16lo_f32(w1), bf16hi_f32(w1));
-        v[4 * k + 2] = make_float2(bf16lo_f32(w2), bf16hi_f32(w2));
-        v[4 * k + 3] = make_float2(bf16lo_f32(w3), bf16hi_f32(w3));
+        if constexpr (C::SPLIT) {
+          v[4 * k + 0] = make_float2(bf16lo_f32(w0), bf16lo_f32(w1));
+          v[4 * k + 1] = make_float2(bf16hi_f32(w0), bf16hi_f32(w1));
+          v[4 * k + 2] = make_float2(bf16lo_f32(w2), bf16lo_f32(w3));
+          v[4 * k + 3] = make_float2(bf16hi_f32(w2), bf16hi_f32(w3));
+        } else {
+          v[4 * k + 0] = make_float2(bf16lo_f32(w0), bf16hi_f32(w0));
+          v[4 * k + 1] = make_float2(bf16lo_f32(w1), bf16hi_f32(w1));
+          v[4 * k + 2] = make_float2(bf16lo_f32(w2), bf16hi_f32(w2));
+          v[4 * k + 3] = make_float2(bf16lo_f32(w3), bf16hi_f32(w3));
+        }
       }
     }
-    // ---- digit 0: elements (4q .. 4q+3) = v[2q].x, v[2q].y, v[2q+1].x, v[2q+1].y
+    // ---- digit 0 on elements 4q .. 4q+3, held as v[2q] = (x0, x2), v[2q+1] =
+    // (x1, x3): u = (x0 + x1, x2 + x3), w = (x0 - x1, x2 - x3), then
+    // (x0', x2') = u + (w2, w0) and (x1', x3') = u - (w2, w0), the same single
+    // roundings as the scalar stage
     if constexpr (C::NIN >= 1) {
+      static_assert(C::SPLIT, "the regular Hadamard keeps split pairs");
 #pragma unroll
-      for (int q = 0; q < 16; ++q) h4_stage(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y);
+      for (int q = 0; q < 16; ++q) {
+        const float2 u = f2_add(v[2 * q], v[2 * q + 1]);
+        const float2 w = f2_sub(v[2 * q], v[2 * q + 1]);
+        const float2 ws = make_float2(w.y, w.x);
+        v[2 * q] = f2_add(u, ws);
+        v[2 * q + 1] = f2_sub(u, ws);
+      }
     }
     // ---- digit 1 (stride 4 elements = 2 pairs) and digit 2 (stride 16 = 8 pairs), packed
     if constexpr (C::NIN >= 2) {
@@ -495,15 +529,17 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
         float2 t[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) t[k] = f2_fma(v[p0 + k], inv2, mg2);
-        const uint32_t n0 = nibbles8(t[0].x, t[0].y, t[1].x, t[1].y, t[2].x, t[2].y, t[3].x, t[3].y);
-        const uint32_t n1 = nibbles8(t[4].x, t[4].y, t[5].x, t[5].y, t[6].x, t[6].y, t[7].x, t[7].y);
+        const float4 f0 = elems4<C::SPLIT>(t[0], t[1]), f1 = elems4<C::SPLIT>(t[2], t[3]);
+        const float4 f2 = elems4<C::SPLIT>(t[4], t[5]), f3 = elems4<C::SPLIT>(t[6], t[7]);
+        const uint32_t n0 = nibbles8(f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w);
+        const uint32_t n1 = nibbles8(f2.x, f2.y, f2.z, f2.w, f3.x, f3.y, f3.z, f3.w);
         asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(q4 + (e >> 1)), "r"(n0), "r"(n1) : "memory");
         if (f8) {
           uint32_t fw[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 ca = f2_sub(t[2 * k], mg2), cb = f2_sub(t[2 * k + 1], mg2);
-            fw[k] = e4m3x2(ca.x, ca.y) | (e4m3x2(cb.x, cb.y) << 16);
+            const float4 c = elems4<C::SPLIT>(f2_sub(t[2 * k], mg2), f2_sub(t[2 * k + 1], mg2));
+            fw[k] = e4m3x2(c.x, c.y) | (e4m3x2(c.z, c.w) << 16);
           }
           stg_128(f8 + e, make_uint4(fw[0], fw[1], fw[2], fw[3]));
         }
@@ -530,23 +566,26 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
         uint32_t words[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float2 t01 = f2_fma(v[p0 + 2 * k], inv2, mg2);
-          const float2 t23 = f2_fma(v[p0 + 2 * k + 1], inv2, mg2);
-          const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
-          const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
+          const float2 ta = f2_fma(v[p0 + 2 * k], inv2, mg2);
+          const float2 tb = f2_fma(v[p0 + 2 * k + 1], inv2, mg2);
+          const float4 t = elems4<C::SPLIT>(ta, tb);  // elements 4k .. 4k+3 of the run
+          const uint32_t b01 = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);
+          const uint32_t b23 = __byte_perm(__float_as_uint(t.z), __float_as_uint(t.w), 0x0040);
           words[k] = __byte_perm(b01, b23, 0x5410);
           if (Q16) {  // reuse the rounded values: code = t - magic, exact in fp16
-            v[p0 + 2 * k] = f2_sub(t01, mg2);
-            v[p0 + 2 * k + 1] = f2_sub(t23, mg2);
+            v[p0 + 2 * k] = f2_sub(ta, mg2);
+            v[p0 + 2 * k + 1] = f2_sub(tb, mg2);
           }
         }
         if (Q) stg_128(Q + e, make_uint4(words[0], words[1], words[2], words[3]));
         if (Q16) {
           uint32_t hw[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const __half2 p = __floats2half2_rn(v[p0 + k].x, v[p0 + k].y);
-            hw[k] = *reinterpret_cast<const uint32_t*>(&p);
+          for (int k = 0; k < 4; ++k) {
+            const float4 c = elems4<C::SPLIT>(v[p0 + 2 * k], v[p0 + 2 * k + 1]);
+            const __half2 p = __floats2half2_rn(c.x, c.y), p2 = __floats2half2_rn(c.z, c.w);
+            hw[2 * k] = *reinterpret_cast<const uint32_t*>(&p);
+            hw[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&p2);
           }
           stg_256(Q16 + e, hw);
         }
@@ -564,14 +603,15 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
             uint32_t words[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const float2 t01 = f2_fma(v[16 * h + 2 * k], inv2, mg2);
-              const float2 t23 = f2_fma(v[16 * h + 2 * k + 1], inv2, mg2);
-              const uint32_t b01 = __byte_perm(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x0040);
-              const uint32_t b23 = __byte_perm(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x0040);
+              const float2 ta = f2_fma(v[16 * h + 2 * k], inv2, mg2);
+              const float2 tb = f2_fma(v[16 * h + 2 * k + 1], inv2, mg2);
+              const float4 t = elems4<C::SPLIT>(ta, tb);
+              const uint32_t b01 = __byte_perm(__float_as_uint(t.x), __float_as_uint(t.y), 0x0040);
+              const uint32_t b23 = __byte_perm(__float_as_uint(t.z), __float_as_uint(t.w), 0x0040);
               words[k] = __byte_perm(b01, b23, 0x5410);
               if (Q16) {
-                v[16 * h + 2 * k] = f2_sub(t01, mg2);
-                v[16 * h + 2 * k + 1] = f2_sub(t23, mg2);
+                v[16 * h + 2 * k] = f2_sub(ta, mg2);
+                v[16 * h + 2 * k + 1] = f2_sub(tb, mg2);
               }
             }
             if (Q) stg_256(Q + e0 + 32 * h, words);
@@ -581,9 +621,11 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
             for (int h = 0; h < 4; ++h) {
               uint32_t hw[8];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const __half2 p = __floats2half2_rn(v[8 * h + k].x, v[8 * h + k].y);
-                hw[k] = *reinterpret_cast<const uint32_t*>(&p);
+              for (int k = 0; k < 4; ++k) {
+                const float4 c = elems4<C::SPLIT>(v[8 * h + 2 * k], v[8 * h + 2 * k + 1]);
+                const __half2 p = __floats2half2_rn(c.x, c.y), p2 = __floats2half2_rn(c.z, c.w);
+                hw[2 * k] = *reinterpret_cast<const uint32_t*>(&p);
+                hw[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&p2);
               }
               stg_256(Q16 + e0 + 16 * h, hw);
             }
@@ -663,7 +705,9 @@ static cudaError_t launch_lane_x(const __nv_bfloat16* X, long long M, int K, lon
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaSuccess;
   const int threads = (NT + 31) / 32 * 32;
-  const int stage_bytes = ((R * K * 2 + 1023) / 1024) * 1024;
+  // a 128-byte slot for every thread: R * K * 2 bytes of lines (NT slots),
+  // then the zeroed slots of the padding threads
+  const int stage_bytes = ((threads * 128 + 1023) / 1024) * 1024;
   // the quad transpose needs 256 bytes per thread (one fp32 line)
   using C = LaneCfg<T, G, XQ>;
   const int tbytes = C::QT ? threads * 256 : 0;
