@@ -38,7 +38,7 @@ def _outside_untouched(buf, rows, cols):
 
 
 @pytest.mark.parametrize("M,K,G,transform", [(37, 1152, 64, "h4"), (37, 1152, 128, "rht"), (3, 21504, 256, "h4"),
-                                             (9, 4096, 256, "rht"), (13, 640, 0, "none")])
+                                             (9, 4096, 256, "rht"), (13, 640, 0, "none"), (37, 5376, 256, "h4")])
 def test_rotate_quantize_writes_only_its_outputs(cr, M, K, G, transform):
     wl = WL.make_case(M, K, [], transform=transform, group=max(G, 2), seed=M + K, name="canary")
     sg = None if wl.signs is None else wl.signs.cuda()

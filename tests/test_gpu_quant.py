@@ -184,6 +184,24 @@ def test_wide_rows_register_kernel(cr, M, K, G, transform):
     assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
 
 
+@pytest.mark.parametrize("M,K,G,transform", [(37, 5376, 256, "h4"), (37, 5376, 128, "rht"), (37, 5376, 64, "h4"),
+                                               (29, 2304, 256, "rht"), (41, 2688, 16, "h4"), (11, 1664, 4, "h4")])
+def test_tiles_with_padding_threads(cr, M, K, G, transform):
+    """Widths whose tile is not a whole number of warps (K = 5376, the DiT
+    block width: 3 rows of 84 lines, 252 threads in blocks of 256): the
+    padding threads own no line and must neither change a row maximum nor
+    write. Ragged M leaves a partial last tile. Codes and scales against the
+    oracle, bit-identical to the generic kernel."""
+    wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.001, outlier_scale=50.0, group=G,
+                      transform=transform, seed=M + K + G)
+    sg = None if wl.signs is None else wl.signs.cuda()
+    fast, gen = _fast_and_generic(cr, wl.X.cuda(), G, transform, sg)
+    Q, s, v = _oracle_act(wl.X, G, transform, wl.signs)
+    check_codes(to_np(fast.q), Q, v, f"{transform} G{G} K{K}")
+    check_scales(to_np(fast.scale), s, f"{transform} G{G} K{K}")
+    assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
+
+
 def test_quantize_act_none_matches_oracle(cr):
     wl = WL.make_case(21, 1152, [], seed=14)
     a = _run_act(cr, wl.X, 0, "none")
