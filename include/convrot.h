@@ -190,6 +190,23 @@ convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packe
  * INVALID_ARG (negative size). */
 #define CONVROT_GEMM_WORKSPACE_BYTES (4096 + 40 * 256 * 1024)
 
+/* The schedule the large-M tensor-core GEMM uses for a shape, computed on the
+ * host alone (no device call; a diagnostic and test entry point).
+ *   M, K        rows and depth; bits 8 (the tensor-core path runs for M > 64
+ *               and K a multiple of 64) or 4 (any M >= 1, K a multiple of 128).
+ *   n, N        the n linears sharing the activation (host array of n widths).
+ *   sms         SM count of the target GPU; one cluster is taken to be
+ *               resident per SM pair (per SM when M <= 128, without pairs).
+ *   workspace_bytes   the workspace size the call would be given (0: none).
+ * Outputs: bn, the tile width (256, 224 or 192); whole_tiles, the tiles run
+ * whole; split_tiles, the last round's tiles split along K (0: no split);
+ * pieces, the K pieces of each split tile (1 without a split).
+ * INVALID_ARG for a null pointer, n outside [1, 8], bits other than 8 or 4,
+ * sms < 1, a negative workspace size, or a shape the path does not run. */
+convrot_status convrot_gemm_tc_plan(int64_t M, int64_t K, int32_t n, const int64_t* N, int32_t bits,
+                                    int32_t sms, int64_t workspace_bytes, int32_t* bn,
+                                    int64_t* whole_tiles, int64_t* split_tiles, int32_t* pieces);
+
 convrot_status convrot_linear_multi_ws(const convrot_packed_act* a, int32_t n,
                                        const convrot_packed_weight* w, const float* const* bias,
                                        uint16_t* const* Y, const int64_t* ldy, void* workspace,

@@ -30,6 +30,7 @@ __all__ = [
     "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
     "PackedAct4", "PackedWeight4", "convrot_prepare_weights4", "convrot_quantize_act4", "convrot_linear4",
     "convrot_linear4_multi", "convrot_gemm4_s32", "convrot_int8_linear", "int8_linear_scratch",
+    "gemm_tc_plan",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -106,6 +107,8 @@ _SIGS = {
     "convrot_int8_linear_scratch_bytes": [_I64, _I64],
     "convrot_int8_linear": [_P, _I64, _I64, _I64, _I32, _I32, _P, _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                             ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P, _I64, _P],
+    "convrot_gemm_tc_plan": [_I64, _I64, _I32, ctypes.POINTER(_I64), _I32, _I32, _I64, ctypes.POINTER(_I32),
+                             ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I32)],
     "convrot_get_device_status": [],
     "convrot_selftest_wait_timeout": [_I64, _P],
     "convrot_status_str": [_I32],
@@ -292,6 +295,18 @@ def convrot_linear_multi_static(a: PackedAct, ws: Sequence[PackedWeight], biases
     ca = a._c()
     _check(lib.convrot_linear_multi_static(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
     return outs
+
+
+def gemm_tc_plan(M: int, K: int, Ns: Sequence[int], bits: int = 8, sms: int = 152,
+                 workspace_bytes: int = GEMM_WORKSPACE_BYTES) -> dict:
+    """The large-M tensor-core GEMM's schedule for a shape, from the host
+    alone: tile width, whole tiles, split tiles and K pieces per split tile."""
+    Na = (_I64 * len(Ns))(*[int(n) for n in Ns])
+    bn, pieces = _I32(), _I32()
+    whole, split = _I64(), _I64()
+    _check(lib.convrot_gemm_tc_plan(M, K, len(Ns), Na, bits, sms, workspace_bytes, ctypes.byref(bn),
+                                    ctypes.byref(whole), ctypes.byref(split), ctypes.byref(pieces)))
+    return {"bn": bn.value, "whole_tiles": whole.value, "split_tiles": split.value, "pieces": pieces.value}
 
 
 def int8_linear_scratch(M: int, K: int, device=None) -> torch.Tensor:

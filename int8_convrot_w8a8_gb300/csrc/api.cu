@@ -23,6 +23,8 @@ cudaError_t gemm_mma_launch(const int8_t* Qx, const float* sx, long long M, int 
 cudaError_t gemm_tc_launch(const void* Qx16, const float* sx, long long M, int K, const GemmOutputs& outs, bool raw,
                            bool f8, void* ws, long long ws_bytes, cudaStream_t st);
 bool gemm_tc_supported(long long M, int K);
+bool gemm_tc_plan(long long M, int K, const GemmOutputs& outs, bool f8, int sms, long long ws_bytes, int* bn,
+                  long long* whole, long long* split, int* pieces);
 cudaError_t gemm_small_launch(const int8_t* Qx, const float* sx, long long M, int K, const GemmOutputs& outs,
                               bool raw, cudaStream_t st);
 bool gemm_small_supported(long long M, int K);
@@ -608,6 +610,36 @@ convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packe
 convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
                                    int64_t lda, void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
   return gemm_s32(a, w, A, lda, workspace, workspace_bytes, stream);
+}
+
+convrot_status convrot_gemm_tc_plan(int64_t M, int64_t K, int32_t n, const int64_t* N, int32_t bits, int32_t sms,
+                                    int64_t workspace_bytes, int32_t* bn, int64_t* whole_tiles, int64_t* split_tiles,
+                                    int32_t* pieces) {
+  if (!N || !bn || !whole_tiles || !split_tiles || !pieces) return fail(CONVROT_ERR_INVALID_ARG, "null argument");
+  if (n < 1 || n > kMaxLinears) return fail(CONVROT_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, kMaxLinears);
+  if (bits != 8 && bits != 4) return fail(CONVROT_ERR_INVALID_ARG, "bits=%d is neither 8 nor 4", bits);
+  if (sms < 1) return fail(CONVROT_ERR_INVALID_ARG, "sms=%d < 1", sms);
+  if (workspace_bytes < 0) return fail(CONVROT_ERR_INVALID_ARG, "negative workspace size");
+  if (K < 1 || K > CONVROT_MAX_K) return fail(CONVROT_ERR_INVALID_ARG, "K=%lld outside [1, %d]",
+                                               static_cast<long long>(K), CONVROT_MAX_K);
+  if (bits == 8 ? !gemm_tc_supported(M, static_cast<int>(K)) : (M < 1 || K % 128 != 0))
+    return fail(CONVROT_ERR_INVALID_ARG, "the tensor-core GEMM does not run for M=%lld, K=%lld at %d bits",
+                static_cast<long long>(M), static_cast<long long>(K), bits);
+  GemmOutputs outs{};
+  outs.count = n;
+  for (int i = 0; i < n; ++i) {
+    if (N[i] < 1 || N[i] > 0x7fffffffLL) return fail(CONVROT_ERR_INVALID_ARG, "N[%d]=%lld", i, static_cast<long long>(N[i]));
+    outs.o[i].n = static_cast<int>(N[i]);
+  }
+  int b = 0, pc = 0;
+  long long wh = 0, sp = 0;
+  if (!gemm_tc_plan(M, static_cast<int>(K), outs, bits == 4, sms, workspace_bytes, &b, &wh, &sp, &pc))
+    return fail(CONVROT_ERR_INVALID_ARG, "no plan for this shape");
+  *bn = b;
+  *whole_tiles = wh;
+  *split_tiles = sp;
+  *pieces = pc;
+  return ok();
 }
 
 convrot_status convrot_get_device_status(void) {

@@ -860,4 +860,25 @@ cudaError_t gemm_tc_launch(const void* Qx16, const float* sx, long long M, int K
              : launch_cl<false, 1, false>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
 }
 
+// The schedule gemm_tc_launch picks, computed on the host alone: tile width,
+// whole tiles, and the tiles of the last round split along K with their
+// piece count. It takes one cluster resident per SM pair (per SM without
+// pairs), which is what the kernel's shared memory allows.
+bool gemm_tc_plan(long long M, int K, const GemmOutputs& outs, bool f8, int sms, long long ws_bytes, int* bn,
+                  long long* whole, long long* split, int* pieces) {
+  const int bke = f8 ? BK8 : BK;
+  if (M <= 0 || K < bke || K % bke != 0 || sms < 1 || outs.count < 1) return false;
+  const int cl = M > BM ? 2 : 1;
+  const int b = choose_bn(M, K, bke, outs, sms, cl, ws_bytes);
+  long long nt = 0;
+  for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + b - 1) / b;
+  const long long tiles = ((M + BM - 1) / BM + cl - 1) / cl * nt;
+  const SplitPlan sp = plan_split(tiles, std::max(1, sms / cl), K / bke, b, cl, ws_bytes);
+  *bn = b;
+  *whole = sp.dp_tiles;
+  *split = sp.sk_tiles;
+  *pieces = sp.pieces;
+  return true;
+}
+
 }  // namespace convrot

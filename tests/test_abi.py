@@ -143,3 +143,66 @@ def test_int8_linear_validation(cr):
     assert call(X=0x1008) == 3                            # misaligned X
     assert call(n=0) == 1
     assert call(M=0, X=None, scratch=None, nbytes=0) == 0  # empty batch: no-op
+
+
+def test_gemm_plan_documented_schedules(cr):
+    """The tensor-core GEMM's schedules on the DiT and qkv shapes: 384
+    256-wide tiles are 5 rounds of 76 pairs plus 4 tiles, which are split
+    along K into 19 pieces; without a workspace 224-wide tiles (6 rounds)
+    cost less; the 4-bit path's tiles are half as long, so the split's fixed
+    cost loses to 224-wide tiles there."""
+    plan = lambda *a, **k: tuple(cr.gemm_tc_plan(*a, **k).values())
+    assert plan(4096, 6144, [6144]) == (256, 380, 4, 19)
+    assert plan(4096, 6144, [6144], workspace_bytes=0) == (224, 448, 0, 1)
+    assert plan(4096, 6144, [6144], bits=4) == (224, 448, 0, 1)
+    assert plan(32700, 3072, [3072] * 3) == (256, 4608, 0, 1)
+    assert plan(32700, 3072, [3072] * 3) == plan(32700, 3072, [9216])
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("sms", [152, 148, 132, 8, 2])
+def test_gemm_plan_invariants(cr, bits, sms):
+    """Over shapes, SM counts and workspace sizes: every tile is run once,
+    a split takes only a last round that leaves at least half of the
+    clusters idle, its pieces fit the clusters and keep two k blocks each,
+    and its partial sums fit the workspace."""
+    bke = 64 if bits == 8 else 128
+    for M in (65, 129, 300, 4096, 32700):
+        for K in (128, 1024, 6144):
+            for Ns in ([256], [6144], [3072] * 3, [136, 520]):
+                for ws in (0, 4096 + 256 * 1024, cr.GEMM_WORKSPACE_BYTES):
+                    p = cr.gemm_tc_plan(M, K, Ns, bits=bits, sms=sms, workspace_bytes=ws)
+                    bn = p["bn"]
+                    assert bn in (256, 224, 192)
+                    cl = 2 if M > 128 else 1
+                    clusters = max(1, sms // cl)
+                    tiles = -(-(-(-M // 128)) // cl) * sum(-(-n // bn) for n in Ns)
+                    assert p["whole_tiles"] + p["split_tiles"] == tiles
+                    if p["split_tiles"] == 0:
+                        assert p["pieces"] == 1
+                        continue
+                    assert p["whole_tiles"] % clusters == 0
+                    assert p["split_tiles"] == tiles % clusters
+                    assert 2 <= p["pieces"] <= (K // bke) // 2
+                    assert p["split_tiles"] * p["pieces"] <= clusters
+                    assert 4096 + p["split_tiles"] * cl * 128 * bn * 4 <= ws
+
+
+def test_gemm_plan_validation(cr):
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144, [6144], bits=6)
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(64, 6144, [6144])              # 8-bit tensor-core path needs M > 64
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144 + 64, [6144], bits=4)  # 4-bit needs K a multiple of 128
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144, [])
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144, [256] * 9)
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144, [0])
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144, [6144], sms=0)
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(4096, 6144, [6144], workspace_bytes=-1)
+    assert cr.gemm_tc_plan(1, 128, [256], bits=4)["bn"] in (256, 224, 192)
