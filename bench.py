@@ -58,12 +58,12 @@ NCU_TRAFFIC = {
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
         "bytes": 245_465_600 + 44_179_712,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "d1eea5cee5d35360e1fe324dd6902bd2702cd99bc4238d76bcf7d1ed1de2ecda",
+        "sha256": "7ca86947208241132365343ee29c1b082cfc07d12b165f765ac1fd988c01121d",
     },
     ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256_W4A4"): {
         "bytes": 64_004_864 + 24_824_064,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "d1eea5cee5d35360e1fe324dd6902bd2702cd99bc4238d76bcf7d1ed1de2ecda",
+        "sha256": "7ca86947208241132365343ee29c1b082cfc07d12b165f765ac1fd988c01121d",
     },
 }
 

@@ -202,7 +202,8 @@ convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packe
  * whole; split_tiles, the last round's tiles split along K (0: no split);
  * pieces, the K pieces of each split tile (1 without a split).
  * INVALID_ARG for a null pointer, n outside [1, 8], bits other than 8 or 4,
- * sms < 1, a negative workspace size, or a shape the path does not run. */
+ * sms < 1, a negative workspace size, or a shape the path does not run
+ * (including one with more tiles than one launch takes, 2^31 - 1). */
 convrot_status convrot_gemm_tc_plan(int64_t M, int64_t K, int32_t n, const int64_t* N, int32_t bits,
                                     int32_t sms, int64_t workspace_bytes, int32_t* bn,
                                     int64_t* whole_tiles, int64_t* split_tiles, int32_t* pieces);

@@ -873,6 +873,7 @@ bool gemm_tc_plan(long long M, int K, const GemmOutputs& outs, bool f8, int sms,
   long long nt = 0;
   for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + b - 1) / b;
   const long long tiles = ((M + BM - 1) / BM + cl - 1) / cl * nt;
+  if (tiles > 0x7fffffffLL) return false;  // the launch rejects such a grid too
   const SplitPlan sp = plan_split(tiles, std::max(1, sms / cl), K / bke, b, cl, ws_bytes);
   *bn = b;
   *whole = sp.dp_tiles;

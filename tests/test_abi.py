@@ -205,4 +205,6 @@ def test_gemm_plan_validation(cr):
         cr.gemm_tc_plan(4096, 6144, [6144], sms=0)
     with pytest.raises(cr.ConvRotError):
         cr.gemm_tc_plan(4096, 6144, [6144], workspace_bytes=-1)
+    with pytest.raises(cr.ConvRotError):
+        cr.gemm_tc_plan(1 << 40, 6144, [6144] * 8)     # more tiles than one launch takes
     assert cr.gemm_tc_plan(1, 128, [256], bits=4)["bn"] in (256, 224, 192)
