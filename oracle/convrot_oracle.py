@@ -21,14 +21,16 @@ Sources (page title, section):
   Walsh-Hadamard transform, then 1/sqrt(B), applied to activation and weight
   rows alike) and the naive variant without rotation.
 
-Readings where the pages are silent (each is also listed in the design notes):
+Readings where the pages are silent:
 
 * round() is round-half-to-even (``numpy.rint``).
 * An all-zero row has s = 0 and Q = 0 (the pages divide by s without saying
   what happens at s = 0).
 * Scales are stored as fp32 (the sglang digest stores the weight scale as
   float32); the divide uses the unrounded fp64 scale.
-* The Walsh-Hadamard matrix is in natural (Sylvester) order.
+* The Walsh-Hadamard matrix is in natural (Sylvester) order, and the block
+  transform acts on each row as on the vector it holds (R x, written as the
+  row x R^T), as "(Ra)^T (Rb)" in "Rotation method" has it.
 * Y is reconstructed in fp64 from the stored fp32 scales and rounded once to
   bf16, round-to-nearest-even.
 * 4-bit ConvRot ("feat: load ConvRot int4 and per-channel int8 safetensors",

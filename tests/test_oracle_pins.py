@@ -52,6 +52,25 @@ def load_quantizer_rows():
     return cases
 
 
+def load_rht_basis_rows():
+    """[(B, signs, rows)] from the hand-worked RHT basis rows: rows[j] is
+    sqrt(B) times the rotated form of the basis row e_j."""
+    blocks = []
+    with open(os.path.join(GOLDEN, "rht_basis_rows.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, *vals = line.split()
+            if tag == "block":
+                blocks.append({"B": int(vals[0]), "rows": []})
+            elif tag == "signs":
+                blocks[-1]["signs"] = [float(v) for v in vals]
+            elif tag == "rows":
+                blocks[-1]["rows"].append([float(v) for v in vals])
+    return [(b["B"], np.array(b["signs"]), np.array(b["rows"])) for b in blocks]
+
+
 # --------------------------------------------------------- pin predicates --
 # Written as predicates so the planted-mistake tests can reuse them.
 
@@ -101,6 +120,23 @@ def pin_rht_basis(rht_block, B=16, seed=3):
         e[j] = 1.0
         if np.abs(T @ e - signs[j] * H[:, j] / np.sqrt(B)).max() > 1e-15:
             return False
+    return True
+
+
+def pin_rht_row_orientation(rotate_rows):
+    """Rows rotated by the block randomized Hadamard transform hold the
+    numbers of R x with R = H D / sqrt(B) (gemma.cpp issue, "Rotation
+    method", where R acts on the vectors a and b): the hand-worked rows of
+    tests/golden/rht_basis_rows.txt for every basis row e_j."""
+    for B, signs, rows in load_rht_basis_rows():
+        if rows.shape != (B, B):
+            return False
+        for j in range(B):
+            e = np.zeros((1, B))
+            e[0, j] = 1.0
+            got = rotate_rows(e, B, "rht", signs)[0] * np.sqrt(B)
+            if np.abs(got - rows[j]).max() > 1e-12:
+                return False
     return True
 
 
@@ -212,6 +248,14 @@ def test_rht_step_order_and_orthogonality():
     signs = rng.choice([-1, 1], size=128)
     T = O.rht_block(128, signs)
     assert np.abs(T @ T.T - np.eye(128)).max() < 1e-12
+
+
+def test_rht_row_orientation_hand_rows():
+    """The orientation of the rotation on row-major rows: e_j becomes
+    s_j H[:, j] / sqrt(B), worked out by hand for B = 4 and 8. Both
+    orientations are orthogonal, so only such a pin tells them apart."""
+    assert len(load_rht_basis_rows()) == 2
+    assert pin_rht_row_orientation(O.rotate_rows)
 
 
 def test_none_transform_is_identity():
@@ -363,6 +407,17 @@ def test_planted_transposed_rht_is_caught():
     def rht_swapped(B, signs):
         return np.diag(np.asarray(signs, float)) @ O.sylvester_hadamard(B) / np.sqrt(B)
     assert not pin_rht_basis(rht_swapped)
+
+
+def test_planted_rht_row_orientation_is_caught():
+    # rows multiplied by R instead of R^T (x R in place of R x): orthogonal
+    # too, and every other pin passes; the hand-worked rows reject it
+    def rotate_wrong(X, G, transform, signs=None):
+        X = np.asarray(X, dtype=np.float64)
+        rows, K = X.shape
+        return (X.reshape(rows, K // G, G) @ O.rht_block(G, signs)).reshape(rows, K)
+    assert pin_rht_row_orientation(O.rotate_rows)
+    assert not pin_rht_row_orientation(rotate_wrong)
 
 
 def test_planted_rounding_errors_are_caught():
