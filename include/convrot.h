@@ -147,9 +147,18 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
  *           the group/transform of both must match.
  *   bias    device fp32 [N] or NULL, 16-byte aligned (as must be w->scale).
  *   Y       device bf16 [M, N], row stride ldy >= N (multiple of 8, 16-byte aligned).
- * Paths: M <= 64 streams the int8 weights (warp-level int8 MMA); larger M
- * uses the tcgen05 tensor-core path when both a->q_f16 and w->q_f16 are given
- * and K is a multiple of 64, otherwise the int8 warp-MMA path. */
+ * Paths, chosen by M and K:
+ *   M <= 64      streams the int8 weights: 17..64 rows with K a multiple of
+ *                128 on the tcgen05 tensor cores (weights and codes widened
+ *                to fp16 on chip), otherwise with warp-level int8 MMA;
+ *   M > 64       the 2-SM tcgen05 tensor-core GEMM when K is a multiple of
+ *                64. It reads the fp16 operand copies, so a->q_f16 and
+ *                w->q_f16 are REQUIRED there: without them the call returns
+ *                INVALID_ARG (it never drops silently to a slower kernel);
+ *   M > 64, K not a multiple of 64: the int8 warp-MMA GEMM (~150 TOPS on
+ *                GB300), the only path for such shapes.
+ * convrot_linear_multi_int8mma / convrot_gemm_s32_int8mma run the int8
+ * warp-MMA GEMM for any shape when asked for by name. */
 convrot_status convrot_linear(const convrot_packed_act* a, const convrot_packed_weight* w,
                               const float* bias, uint16_t* Y, int64_t ldy, cudaStream_t stream);
 
@@ -170,6 +179,19 @@ convrot_status convrot_linear_multi(const convrot_packed_act* a, int32_t n,
  * Test and diagnostic entry point. */
 convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w,
                                 int32_t* A, int64_t lda, cudaStream_t stream);
+
+/* The int8 warp-level MMA GEMM (mma.sync m16n8k32 with native int32
+ * accumulation, ~150 TOPS on GB300, about 11x below the tensor-core path),
+ * for any M and K, run only when a caller asks for it by name: it needs no
+ * fp16 operand copies (q_f16 may be NULL). Arguments, results (bit-identical
+ * to the other paths) and errors as convrot_linear_multi and
+ * convrot_gemm_s32. */
+convrot_status convrot_linear_multi_int8mma(const convrot_packed_act* a, int32_t n,
+                                            const convrot_packed_weight* w, const float* const* bias,
+                                            uint16_t* const* Y, const int64_t* ldy,
+                                            cudaStream_t stream);
+convrot_status convrot_gemm_s32_int8mma(const convrot_packed_act* a, const convrot_packed_weight* w,
+                                        int32_t* A, int64_t lda, cudaStream_t stream);
 
 /* GEMM workspace. The pages have no counterpart: this is a scheduling device
  * of the tensor-core path. When the tiles of the last round would leave at
@@ -197,6 +219,10 @@ convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packe
  *   n, N        the n linears sharing the activation (host array of n widths).
  *   sms         SM count of the target GPU; one cluster is taken to be
  *               resident per SM pair (per SM when M <= 128, without pairs).
+ *               The launch takes the resident count from the CUDA occupancy
+ *               query instead, so this is the schedule a launch uses whenever
+ *               that query returns sms / 2 (sms) clusters, as on a GB300
+ *               with all 152 SMs free.
  *   workspace_bytes   the workspace size the call would be given (0: none).
  * Outputs: bn, the tile width (256, 224 or 192); whole_tiles, the tiles run
  * whole; split_tiles, the last round's tiles split along K (0: no split);
@@ -262,18 +288,20 @@ convrot_status convrot_int8_linear(const void* X, int64_t M, int64_t K, int64_t 
  * the caller: ALLOCATES NOTHING. The pages have no counterpart; this is a
  * deployment convenience of this library.
  * The scratch is a static device array of CONVROT_GEMM_WORKSPACE_BYTES, one
- * per device, located with cudaGetSymbolAddress and cleared (synchronously)
- * on the first call on each device; every call whose kernels complete leaves
- * it clear again, and convrot_get_device_status() clears it after reporting
- * CONVROT_ERR_TIMEOUT. A split is planned only within that size (a launch
- * that would need more is rejected before it starts).
+ * per device, zero when the library's module is loaded on that device. The
+ * first call on each device locates it with cudaGetSymbolAddress (no device
+ * work, no wait; make that first call before any stream capture, since it
+ * may load the module). Every call whose kernels complete leaves it clear
+ * again, and convrot_get_device_status() clears it whenever any kernel unit
+ * recorded CONVROT_ERR_TIMEOUT. A split is planned only within that size (a
+ * launch that would need more is rejected before it starts).
  * RACES: every caller on a device shares the one scratch. Calls that may
  * overlap in time on the GPU (different streams, different host threads)
  * race on it and can produce wrong results: serialize them, e.g. on one
  * stream, or give concurrent calls their own workspaces through
  * convrot_linear_multi_ws.
  * Errors: as convrot_linear_multi, plus CUDA if the scratch cannot be
- * located or cleared. */
+ * located. */
 convrot_status convrot_linear_multi_static(const convrot_packed_act* a, int32_t n,
                                            const convrot_packed_weight* w, const float* const* bias,
                                            uint16_t* const* Y, const int64_t* ldy, cudaStream_t stream);
@@ -339,9 +367,13 @@ convrot_status convrot_gemm4_s32(const convrot_packed_act4* a, const convrot_pac
                                  int32_t* A, int64_t lda, void* workspace, int64_t workspace_bytes,
                                  cudaStream_t stream);
 
-/* Reads and clears the device error word of the current device (synchronizes
- * the device first). CONVROT_OK if no kernel reported a problem, else the
- * first status a kernel recorded (e.g. CONVROT_ERR_TIMEOUT). */
+/* Reads and clears the device error words of the current device (one per
+ * kernel unit; synchronizes the device first). Every word is read and cleared
+ * before anything is reported. If any holds CONVROT_ERR_TIMEOUT, the static
+ * scratch of convrot_linear_multi_static is cleared (an aborted split can
+ * leave partial sums there) and CONVROT_ERR_TIMEOUT is returned; otherwise
+ * the first nonzero status, or CONVROT_OK if no kernel reported a problem.
+ * convrot_last_error() then says how many units recorded a status. */
 convrot_status convrot_get_device_status(void);
 
 /* Test hook for the bounded waits: launches one block that waits on an

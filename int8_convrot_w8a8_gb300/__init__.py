@@ -96,6 +96,9 @@ _SIGS = {
     "convrot_linear_multi_ws": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                                 ctypes.POINTER(_P), ctypes.POINTER(_I64), _P, _I64, _P],
     "convrot_gemm_s32": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P],
+    "convrot_linear_multi_int8mma": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
+                                     ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
+    "convrot_gemm_s32_int8mma": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P],
     "convrot_gemm_s32_ws": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _I64, _P, _I64, _P],
     "convrot_linear_multi_static": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                                     ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
@@ -248,12 +251,15 @@ def gemm_workspace(device=None) -> torch.Tensor:
 
 def convrot_linear(a: PackedAct, w: PackedWeight, bias: Optional[torch.Tensor] = None,
                    out: Optional[torch.Tensor] = None, stream=None,
-                   workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Y = A * s_x * s_w + b (bf16) for one linear."""
+                   workspace: Optional[torch.Tensor] = None, int8_mma: bool = False) -> torch.Tensor:
+    """Y = A * s_x * s_w + b (bf16) for one linear. Above 64 rows the
+    tensor-core GEMM needs the fp16 operand copies; ``int8_mma=True`` runs the
+    int8 warp-MMA GEMM instead (no copies needed, about 11x slower)."""
     if out is None:
         out = torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q.device)
-    if workspace is not None:
-        return convrot_linear_multi(a, [w], [bias], outs=[out], stream=stream, workspace=workspace)[0]
+    if workspace is not None or int8_mma:
+        return convrot_linear_multi(a, [w], [bias], outs=[out], stream=stream, workspace=workspace,
+                                    int8_mma=int8_mma)[0]
     ca, cw = a._c(), w._c()
     _check(lib.convrot_linear(ctypes.byref(ca), ctypes.byref(cw), _ptr(bias), out.data_ptr(), out.stride(0),
                               _stream(stream)))
@@ -262,8 +268,9 @@ def convrot_linear(a: PackedAct, w: PackedWeight, bias: Optional[torch.Tensor] =
 
 def convrot_linear_multi(a: PackedAct, ws: Sequence[PackedWeight], biases: Optional[Sequence] = None,
                          outs: Optional[List[torch.Tensor]] = None, stream=None,
-                         workspace: Optional[torch.Tensor] = None) -> List[torch.Tensor]:
-    """Several linears sharing one packed activation, in one launch."""
+                         workspace: Optional[torch.Tensor] = None, int8_mma: bool = False) -> List[torch.Tensor]:
+    """Several linears sharing one packed activation, in one launch
+    (``int8_mma``: the int8 warp-MMA GEMM, asked for by name)."""
     n = len(ws)
     if outs is None:
         outs = [torch.empty((a.M, w.N), dtype=torch.bfloat16, device=a.q.device) for w in ws]
@@ -272,7 +279,11 @@ def convrot_linear_multi(a: PackedAct, ws: Sequence[PackedWeight], biases: Optio
     yarr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
     larr = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
     ca = a._c()
-    if workspace is None:
+    if int8_mma:
+        if workspace is not None:
+            raise ValueError("the int8 warp-MMA GEMM takes no workspace")
+        _check(lib.convrot_linear_multi_int8mma(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
+    elif workspace is None:
         _check(lib.convrot_linear_multi(ctypes.byref(ca), n, warr, barr, yarr, larr, _stream(stream)))
     else:
         _check(lib.convrot_linear_multi_ws(ctypes.byref(ca), n, warr, barr, yarr, larr, workspace.data_ptr(),
@@ -348,12 +359,18 @@ def convrot_int8_linear(X: torch.Tensor, ws: Sequence[PackedWeight], biases: Opt
 
 
 def convrot_gemm_s32(a: PackedAct, w: PackedWeight, out: Optional[torch.Tensor] = None, stream=None,
-                     workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Raw int32 accumulators A = Q_x Q_w^T through the linear's GEMM main loop."""
+                     workspace: Optional[torch.Tensor] = None, int8_mma: bool = False) -> torch.Tensor:
+    """Raw int32 accumulators A = Q_x Q_w^T through the linear's GEMM main loop
+    (``int8_mma``: the int8 warp-MMA GEMM, asked for by name)."""
     if out is None:
         out = torch.empty((a.M, w.N), dtype=torch.int32, device=a.q.device)
     ca, cw = a._c(), w._c()
-    if workspace is None:
+    if int8_mma:
+        if workspace is not None:
+            raise ValueError("the int8 warp-MMA GEMM takes no workspace")
+        _check(lib.convrot_gemm_s32_int8mma(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
+                                            _stream(stream)))
+    elif workspace is None:
         _check(lib.convrot_gemm_s32(ctypes.byref(ca), ctypes.byref(cw), out.data_ptr(), out.stride(0),
                                     _stream(stream)))
     else:

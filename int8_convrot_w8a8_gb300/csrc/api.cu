@@ -208,26 +208,42 @@ convrot_status check_pair(const convrot_packed_act* a, const convrot_packed_weig
   return CONVROT_OK;
 }
 
+// Path choice. M <= 64 streams the int8 weights (tcgen05 for 17..64 rows
+// with K a multiple of 128, warp MMA otherwise). Larger M runs the 2-SM
+// tensor-core GEMM, which reads the fp16 operand copies: a call without them
+// is an error rather than a silent detour through the int8 warp-MMA kernel,
+// about 11x slower on GB300, which a caller gets only by asking for it
+// (int8_mma) or for shapes the tensor-core path does not take (K not a
+// multiple of 64), where it is the only path.
 convrot_status run_gemm(const convrot_packed_act* a, GemmOutputs& outs, bool raw, void* ws, long long ws_bytes,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool int8_mma = false) {
   if (a->M == 0) return ok();
   bool all_f16 = a->q_f16 != nullptr;
   for (int i = 0; i < outs.count; ++i) all_f16 = all_f16 && outs.o[i].qw16 != nullptr;
+  const int K = static_cast<int>(a->K);
   cudaError_t e;
-  if (gemm_small_tc_supported(a->M, static_cast<int>(a->K))) {
+  if (int8_mma) {
+    e = gemm_mma_launch(a->q, a->scale, a->M, K, outs, raw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 MMA GEMM launch");
+  } else if (gemm_small_tc_supported(a->M, K)) {
     // a handful of rows, K a multiple of 128: the int8 weight stream widened
     // to fp16 on chip for the tcgen05 tensor cores
-    e = gemm_small_tc_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    e = gemm_small_tc_launch(a->q, a->scale, a->M, K, outs, raw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M tensor-core GEMM launch");
-  } else if (gemm_small_supported(a->M, static_cast<int>(a->K))) {
+  } else if (gemm_small_supported(a->M, K)) {
     // a handful of rows: the int8 weight stream, no fp16 copies needed
-    e = gemm_small_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    e = gemm_small_launch(a->q, a->scale, a->M, K, outs, raw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "small-M GEMM launch");
-  } else if (all_f16 && gemm_tc_supported(a->M, static_cast<int>(a->K))) {
-    e = gemm_tc_launch(a->q_f16, a->scale, a->M, static_cast<int>(a->K), outs, raw, false, ws, ws_bytes, stream);
+  } else if (gemm_tc_supported(a->M, K)) {
+    if (!all_f16)
+      return fail(CONVROT_ERR_INVALID_ARG,
+                  "M=%lld runs the tensor-core GEMM, which reads the fp16 operand copies: give q_f16 for the "
+                  "activation and every weight (the int8 warp-MMA path runs only when asked for by name)",
+                  static_cast<long long>(a->M));
+    e = gemm_tc_launch(a->q_f16, a->scale, a->M, K, outs, raw, false, ws, ws_bytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core GEMM launch");
   } else {
-    e = gemm_mma_launch(a->q, a->scale, a->M, static_cast<int>(a->K), outs, raw, stream);
+    e = gemm_mma_launch(a->q, a->scale, a->M, K, outs, raw, stream);
     if (e != cudaSuccess) return cuda_fail(e, "int8 MMA GEMM launch");
   }
   return ok();
@@ -314,8 +330,10 @@ convrot_status convrot_quantize_act_hmatmul(const void* X, int64_t M, int64_t K,
 
 namespace {
 
-// Locates this device's static scratch on first use (cudaGetSymbolAddress)
-// and clears it once; later calls reuse the address.
+// Locates this device's static scratch on first use (cudaGetSymbolAddress);
+// later calls reuse the address. The array is zero when the module is
+// loaded, which is the state the split GEMM expects, so nothing is cleared
+// here and nothing waits on the device.
 convrot_status static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -333,9 +351,6 @@ convrot_status static_scratch(void** out) {
   if (e != cudaSuccess) return cuda_fail(e, "locating the static GEMM scratch");
   if (bytes < static_cast<size_t>(CONVROT_GEMM_WORKSPACE_BYTES))
     return fail(CONVROT_ERR_INVALID_ARG, "static GEMM scratch is %zu bytes, below the workspace size", bytes);
-  e = cudaMemset(p, 0, bytes);  // what the split kernels expect to find zero
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the static GEMM scratch");
   g_static_scratch[dev] = p;
   *out = p;
   return ok();
@@ -374,11 +389,11 @@ convrot_status build_outputs(const convrot_packed_act* a, int32_t n, const convr
 
 convrot_status linear_multi(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
                             const float* const* bias, uint16_t* const* Y, const int64_t* ldy, void* ws,
-                            int64_t ws_bytes, cudaStream_t stream) {
+                            int64_t ws_bytes, cudaStream_t stream, bool int8_mma = false) {
   GemmOutputs outs;
   convrot_status s = build_outputs(a, n, w, bias, Y, ldy, ws, ws_bytes, &outs);
   if (s != CONVROT_OK) return s;
-  return run_gemm(a, outs, false, ws, ws_bytes, stream);
+  return run_gemm(a, outs, false, ws, ws_bytes, stream, int8_mma);
 }
 
 // The packed activation of convrot_int8_linear inside the caller's scratch:
@@ -448,7 +463,7 @@ convrot_status gemm4(const convrot_packed_act4* a, int32_t n, const convrot_pack
 }
 
 convrot_status gemm_s32(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A, int64_t lda,
-                        void* ws, int64_t ws_bytes, cudaStream_t stream) {
+                        void* ws, int64_t ws_bytes, cudaStream_t stream, bool int8_mma = false) {
   convrot_status s = check_pair(a, w);
   if (s != CONVROT_OK) return s;
   s = check_workspace(ws, ws_bytes);
@@ -459,7 +474,7 @@ convrot_status gemm_s32(const convrot_packed_act* a, const convrot_packed_weight
   GemmOutputs outs{};
   outs.count = 1;
   outs.o[0] = GemmOut{w->q, w->q_f16, w->scale, nullptr, A, lda, static_cast<int>(w->N), 0};
-  return run_gemm(a, outs, true, ws, ws_bytes, stream);
+  return run_gemm(a, outs, true, ws, ws_bytes, stream, int8_mma);
 }
 
 }  // namespace
@@ -524,12 +539,16 @@ convrot_status convrot_int8_linear(const void* X, int64_t M, int64_t K, int64_t 
   GemmOutputs outs;
   s = build_outputs(&a, n, w, bias, Y, ldy, workspace, workspace_bytes, &outs);
   if (s != CONVROT_OK) return s;
+  // the 2-SM tensor-core GEMM reads only the fp16 copies: every weight must
+  // carry one (checked here, before the first launch); the int8 codes of the
+  // activation are then not written
+  const bool tc_only = q16 != nullptr;
+  for (int i = 0; i < n && tc_only; ++i)
+    if (!w[i].q_f16)
+      return fail(CONVROT_ERR_INVALID_ARG,
+                  "M=%lld runs the tensor-core GEMM, which reads the fp16 operand copies: weight %d has none",
+                  static_cast<long long>(M), i);
   if (M == 0) return ok();
-  // the 2-SM tensor-core GEMM reads only the fp16 copy: the int8 codes are
-  // then not written (run_gemm takes that path exactly when every weight has
-  // its fp16 copy and the activation's is there)
-  bool tc_only = q16 != nullptr;
-  for (int i = 0; i < n; ++i) tc_only = tc_only && w[i].q_f16 != nullptr;
   int path = 0;
   cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs,
                                   tc_only ? nullptr : q, sx, q16, 0, 127, stream, &path);
@@ -607,6 +626,17 @@ convrot_status convrot_gemm_s32(const convrot_packed_act* a, const convrot_packe
   return gemm_s32(a, w, A, lda, nullptr, 0, stream);
 }
 
+convrot_status convrot_linear_multi_int8mma(const convrot_packed_act* a, int32_t n, const convrot_packed_weight* w,
+                                            const float* const* bias, uint16_t* const* Y, const int64_t* ldy,
+                                            cudaStream_t stream) {
+  return linear_multi(a, n, w, bias, Y, ldy, nullptr, 0, stream, true);
+}
+
+convrot_status convrot_gemm_s32_int8mma(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
+                                        int64_t lda, cudaStream_t stream) {
+  return gemm_s32(a, w, A, lda, nullptr, 0, stream, true);
+}
+
 convrot_status convrot_gemm_s32_ws(const convrot_packed_act* a, const convrot_packed_weight* w, int32_t* A,
                                    int64_t lda, void* workspace, int64_t workspace_bytes, cudaStream_t stream) {
   return gemm_s32(a, w, A, lda, workspace, workspace_bytes, stream);
@@ -645,27 +675,38 @@ convrot_status convrot_gemm_tc_plan(int64_t M, int64_t K, int32_t n, const int64
 convrot_status convrot_get_device_status(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  int words[7] = {status_word_rotquant(), status_word_gemm_mma(),   status_word_gemm_tc(), status_word_gemm_small(),
-                  status_word_gemm_small_tc(), status_word_hmatmul(), status_word_api()};
+  // every word is read (and so cleared) before anything is reported
+  const int words[7] = {status_word_rotquant(), status_word_gemm_mma(),   status_word_gemm_tc(),
+                        status_word_gemm_small(), status_word_gemm_small_tc(), status_word_hmatmul(),
+                        status_word_api()};
+  int first = 0, nonzero = 0;
+  bool timeout = false;
   for (int w : words) {
-    if (w != 0) {
-      if (w == CONVROT_ERR_TIMEOUT) {
-        // an aborted split may have left partial sums in the static scratch
-        int dev = 0;
-        void* p = nullptr;
-        if (cudaGetDevice(&dev) == cudaSuccess) {
-          std::lock_guard<std::mutex> lock(g_cache_mu);
-          auto it = g_static_scratch.find(dev);
-          if (it != g_static_scratch.end()) p = it->second;
-        }
-        if (p && (cudaMemset(p, 0, CONVROT_GEMM_WORKSPACE_BYTES) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
-          return cuda_fail(cudaGetLastError(), "clearing the static GEMM scratch");
-      }
-      return fail(static_cast<convrot_status>(w), "a kernel recorded status %d (%s)", w,
-                  convrot_status_str(static_cast<convrot_status>(w)));
+    if (w == 0) continue;
+    ++nonzero;
+    if (first == 0) first = w;
+    timeout = timeout || w == CONVROT_ERR_TIMEOUT;
+  }
+  if (timeout) {
+    // an aborted split may have left partial sums and arrival counts in the
+    // static scratch: clear it before any later call adds onto them
+    int dev = 0;
+    void* p = nullptr;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+      std::lock_guard<std::mutex> lock(g_cache_mu);
+      auto it = g_static_scratch.find(dev);
+      if (it != g_static_scratch.end()) p = it->second;
+    }
+    if (p) {
+      e = cudaMemset(p, 0, CONVROT_GEMM_WORKSPACE_BYTES);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "clearing the static GEMM scratch");
     }
   }
-  return ok();
+  if (first == 0) return ok();
+  if (timeout && first != CONVROT_ERR_TIMEOUT) first = CONVROT_ERR_TIMEOUT;
+  return fail(static_cast<convrot_status>(first), "%d kernel unit(s) recorded a status; reporting %d (%s)", nonzero,
+              first, convrot_status_str(static_cast<convrot_status>(first)));
 }
 
 convrot_status convrot_selftest_wait_timeout(int64_t spin_limit, cudaStream_t stream) {

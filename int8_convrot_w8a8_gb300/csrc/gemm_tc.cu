@@ -717,12 +717,17 @@ SplitPlan plan_split(long long tiles, int clusters, int nk, int bn, int cl, long
 
 constexpr double kSplitOverheadCycles = 15000.0;
 
-int choose_bn(long long M, int K, int bke, const GemmOutputs& outs, int sms, int cl, long long ws_bytes) {
+// Candidate tile widths, and for each the clusters resident at once.
+constexpr int kBnCandidates[3] = {256, 224, 192};
+
+int choose_bn(long long M, int K, int bke, const GemmOutputs& outs, const int (&resident)[3], int cl,
+              long long ws_bytes) {
   const long long mt = ((M + BM - 1) / BM + cl - 1) / cl;
-  const int clusters = std::max(1, sms / cl);
   int best = 256;
   double best_cost = -1.0;
-  for (int bn : {256, 224, 192}) {
+  for (int c = 0; c < 3; ++c) {
+    const int bn = kBnCandidates[c];
+    const int clusters = std::max(1, resident[c]);
     long long nt = 0;
     for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + bn - 1) / bn;
     const long long tiles = mt * nt;
@@ -737,6 +742,22 @@ int choose_bn(long long M, int K, int bke, const GemmOutputs& outs, int sms, int
     }
   }
   return best;
+}
+
+// Clusters of this instantiation that can be resident at once (one CTA per
+// SM without pairs); also sets the kernel's shared-memory limit.
+template <int BN, bool RAW, int CL, bool F8>
+cudaError_t resident_clusters(int sms, int* out) {
+  using C = Cfg<BN, CL>;
+  auto kern = gemm_tc_kernel<BN, RAW, CL, F8>;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (e != cudaSuccess) return e;
+  *out = sms;
+  if constexpr (CL > 1) {
+    e = max_active_clusters(reinterpret_cast<const void*>(kern), THREADS, C::SMEM, CL, out);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 template <int BN, bool RAW, int CL, bool F8>
@@ -783,14 +804,11 @@ cudaError_t launch_bn(EncodeTiledFn enc, const void* Qx16, const float* sx, long
   p.num_tiles = static_cast<int>(tiles);
   p.spin_limit = kDefaultSpinLimit;
   auto kern = gemm_tc_kernel<BN, RAW, CL, F8>;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), C::SMEM);
+  // clusters that are resident together (the count the tile width was chosen
+  // under): the split plan needs the real count
+  int clusters = 0;
+  cudaError_t e = resident_clusters<BN, RAW, CL, F8>(sms, &clusters);
   if (e != cudaSuccess) return e;
-  // clusters that are resident together: the split plan needs the real count
-  int clusters = sms;
-  if constexpr (CL > 1) {
-    e = max_active_clusters(reinterpret_cast<const void*>(kern), THREADS, C::SMEM, CL, &clusters);
-    if (e != cudaSuccess) return e;
-  }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const SplitPlan sp = plan_split(tiles, clusters, K / BKE, BN, CL, ws ? ws_bytes : 0);
   // oversize guard: the split's counters and sums must fit the workspace
@@ -825,7 +843,12 @@ cudaError_t launch_bn(EncodeTiledFn enc, const void* Qx16, const float* sx, long
 template <bool RAW, int CL, bool F8>
 cudaError_t launch_cl(EncodeTiledFn enc, const void* Qx16, const float* sx, long long M, int K,
                       const GemmOutputs& outs, void* ws, long long ws_bytes, cudaStream_t st, int sms) {
-  switch (choose_bn(M, K, F8 ? BK8 : BK, outs, sms, CL, ws ? ws_bytes : 0)) {
+  int resident[3];
+  cudaError_t e = resident_clusters<256, RAW, CL, F8>(sms, &resident[0]);
+  if (e == cudaSuccess) e = resident_clusters<224, RAW, CL, F8>(sms, &resident[1]);
+  if (e == cudaSuccess) e = resident_clusters<192, RAW, CL, F8>(sms, &resident[2]);
+  if (e != cudaSuccess) return e;
+  switch (choose_bn(M, K, F8 ? BK8 : BK, outs, resident, CL, ws ? ws_bytes : 0)) {
     case 256: return launch_bn<256, RAW, CL, F8>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
     case 224: return launch_bn<224, RAW, CL, F8>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
     default: return launch_bn<192, RAW, CL, F8>(enc, Qx16, sx, M, K, outs, ws, ws_bytes, st, sms);
@@ -863,18 +886,22 @@ cudaError_t gemm_tc_launch(const void* Qx16, const float* sx, long long M, int K
 // The schedule gemm_tc_launch picks, computed on the host alone: tile width,
 // whole tiles, and the tiles of the last round split along K with their
 // piece count. It takes one cluster resident per SM pair (per SM without
-// pairs), which is what the kernel's shared memory allows.
+// pairs), which is what the kernel's shared memory allows; the launch takes
+// the count from the occupancy query, so the two agree whenever that query
+// returns sms / cl.
 bool gemm_tc_plan(long long M, int K, const GemmOutputs& outs, bool f8, int sms, long long ws_bytes, int* bn,
                   long long* whole, long long* split, int* pieces) {
   const int bke = f8 ? BK8 : BK;
   if (M <= 0 || K < bke || K % bke != 0 || sms < 1 || outs.count < 1) return false;
   const int cl = M > BM ? 2 : 1;
-  const int b = choose_bn(M, K, bke, outs, sms, cl, ws_bytes);
+  const int per = std::max(1, sms / cl);
+  const int resident[3] = {per, per, per};
+  const int b = choose_bn(M, K, bke, outs, resident, cl, ws_bytes);
   long long nt = 0;
   for (int i = 0; i < outs.count; ++i) nt += (outs.o[i].n + b - 1) / b;
   const long long tiles = ((M + BM - 1) / BM + cl - 1) / cl * nt;
   if (tiles > 0x7fffffffLL) return false;  // the launch rejects such a grid too
-  const SplitPlan sp = plan_split(tiles, std::max(1, sms / cl), K / bke, b, cl, ws_bytes);
+  const SplitPlan sp = plan_split(tiles, per, K / bke, b, cl, ws_bytes);
   *bn = b;
   *whole = sp.dp_tiles;
   *split = sp.sk_tiles;

@@ -88,6 +88,29 @@ def test_linear_validation(cr):
     assert n_bad == 1
 
 
+def test_large_m_without_fp16_copies_is_refused(cr):
+    """Above 64 rows the tensor-core GEMM reads the fp16 operand copies; a
+    call without them is refused on the host, never routed to the ~11x
+    slower int8 warp-MMA kernel unless that kernel is asked for by name."""
+    act = cr._Act(0x1000, 0x2000, None, 300, 256, 256, 0)
+    act16 = cr._Act(0x1000, 0x2000, 0x3000, 300, 256, 256, 0)
+    w = cr._Weight(0x4000, 0x5000, None, 16, 256, 256, 0)
+    f = cr.lib.convrot_linear
+    assert f(ctypes.byref(act), ctypes.byref(w), None, 0x8000, 16, None) == 1
+    assert b"fp16 operand copies" in cr.lib.convrot_last_error()
+    assert f(ctypes.byref(act16), ctypes.byref(w), None, 0x8000, 16, None) == 1  # weight copy missing
+    assert cr.lib.convrot_gemm_s32(ctypes.byref(act), ctypes.byref(w), 0x8000, 16, None) == 1
+    # the one-call linear refuses before its first launch
+    wa = (cr._Weight * 1)(w)
+    bias = (ctypes.c_void_p * 1)(None)
+    ys = (ctypes.c_void_p * 1)(0x6000)
+    ld = (ctypes.c_int64 * 1)(16)
+    need = cr.lib.convrot_int8_linear_scratch_bytes(300, 256)
+    assert cr.lib.convrot_int8_linear(0x1000, 300, 256, 256, 256, 0, None, 1, wa, bias, ys, ld, 0x10000, need,
+                                      None, 0, None) == 1
+    assert b"fp16 operand copies" in cr.lib.convrot_last_error()
+
+
 def test_selftest_argument_check(cr):
     assert cr.lib.convrot_selftest_wait_timeout(0, None) == 1
 

@@ -68,11 +68,14 @@ def test_gemm_writes_only_its_outputs(cr, M, N, K, path):
     w = cr.convrot_prepare_weights(wl.weights[0].cuda(), 64, "h4", with_f16=f16)
     a = cr.convrot_quantize_act(wl.X.cuda(), 64, "h4", with_f16=f16)
     ybuf, y = _guarded((M, N), torch.bfloat16, pad_rows=5, pad_cols=24)
-    cr.convrot_linear(a, w, wl.biases[0].cuda(), out=y, workspace=cr.gemm_workspace())
+    if path == "mma":
+        cr.convrot_linear(a, w, wl.biases[0].cuda(), out=y, int8_mma=True)
+    else:
+        cr.convrot_linear(a, w, wl.biases[0].cuda(), out=y, workspace=cr.gemm_workspace())
     torch.cuda.synchronize()
     assert cr.convrot_get_device_status() == 0
     assert _outside_untouched(ybuf, M, N)
-    assert torch.equal(y, cr.convrot_linear(a, w, wl.biases[0].cuda()))
+    assert torch.equal(y, cr.convrot_linear(a, w, wl.biases[0].cuda(), int8_mma=path == "mma"))
 
 
 def test_w4_gemm_writes_only_its_outputs(cr):

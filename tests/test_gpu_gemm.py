@@ -52,7 +52,7 @@ def test_gemm_s32_bit_exact_on_oracle_codes(cr, path, M, N, K):
     Qw = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
     a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", path == "tc", "act")
     w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", path == "tc", "w")
-    A = to_np(cr.convrot_gemm_s32(a, w))
+    A = to_np(cr.convrot_gemm_s32(a, w, int8_mma=path == "mma"))
     assert np.array_equal(A.astype(np.int64), O.int_gemm(Qx, Qw))
 
 
@@ -71,7 +71,7 @@ def test_gemm_s32_adversarial_magnitudes(cr, path, K):
     Qw[5::7, 1::2] = -1
     a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", path == "tc", "act")
     w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", path == "tc", "w")
-    A = to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64)
+    A = to_np(cr.convrot_gemm_s32(a, w, int8_mma=path == "mma")).astype(np.int64)
     ref = O.int_gemm(Qx, Qw)
     assert np.array_equal(A, ref)
     assert np.abs(ref).max() == 16129 * K
@@ -88,11 +88,11 @@ def test_linear_on_oracle_codes(cr, path, case):
     a = packed_from_codes(cr, Qx, sx, wl.group, wl.transform, path == "tc", "act")
     w = packed_from_codes(cr, Qw, sw, wl.group, wl.transform, path == "tc", "w")
     bias = wl.biases[0]
-    Y = cr.convrot_linear(a, w, bias.cuda())
+    Y = cr.convrot_linear(a, w, bias.cuda(), int8_mma=path == "mma")
     A = O.int_gemm(Qx, Qw)
-    assert np.array_equal(to_np(cr.convrot_gemm_s32(a, w)).astype(np.int64), A)
+    assert np.array_equal(to_np(cr.convrot_gemm_s32(a, w, int8_mma=path == "mma")).astype(np.int64), A)
     check_y_same_codes(to_np(Y.float()), A, sx, sw, bias.numpy(), f"{case}/{path}")
-    Y0 = cr.convrot_linear(a, w, None)
+    Y0 = cr.convrot_linear(a, w, None, int8_mma=path == "mma")
     check_y_same_codes(to_np(Y0.float()), A, sx, sw, None, f"{case}/{path}/nobias")
 
 
@@ -108,7 +108,7 @@ def test_linear_end_to_end(cr, path, case):
     sg = None if wl.signs is None else wl.signs.cuda()
     pw = cr.convrot_prepare_weights(wl.weights[0].cuda(), wl.group, wl.transform, sg, with_f16=f16)
     a = cr.convrot_quantize_act(wl.X.cuda(), wl.group, wl.transform, sg, with_f16=f16)
-    Y = cr.convrot_linear(a, pw, wl.biases[0].cuda())
+    Y = cr.convrot_linear(a, pw, wl.biases[0].cuda(), int8_mma=path == "mma")
     Qx, sx, v, Qw, sw = oracle_case(wl)
     ref = O.reconstruct(O.int_gemm(Qx, Qw), sx, sw, wl.biases[0].numpy())
     check_codes(to_np(a.q), Qx, v, case)
@@ -122,12 +122,12 @@ def test_linear_multi_equals_separate_calls_and_concatenation(cr, path):
     a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4", with_f16=f16)
     ws = [cr.convrot_prepare_weights(W.cuda(), 256, "h4", with_f16=f16) for W in wl.weights]
     bs = [b.cuda() for b in wl.biases]
-    Ys = cr.convrot_linear_multi(a, ws, bs)
+    Ys = cr.convrot_linear_multi(a, ws, bs, int8_mma=path == "mma")
     for Y, w, b in zip(Ys, ws, bs):
-        assert torch.equal(Y, cr.convrot_linear(a, w, b))
+        assert torch.equal(Y, cr.convrot_linear(a, w, b, int8_mma=path == "mma"))
     cat = cr.PackedWeight(torch.cat([w.q for w in ws]), torch.cat([w.scale for w in ws]),
                           torch.cat([w.q_f16 for w in ws]) if f16 else None, 256, 0)
-    Ycat = cr.convrot_linear(a, cat, torch.cat(bs))
+    Ycat = cr.convrot_linear(a, cat, torch.cat(bs), int8_mma=path == "mma")
     assert torch.equal(Ycat, torch.cat(Ys, dim=1))
 
 
@@ -139,8 +139,8 @@ def test_row_split_is_bit_identical(cr, path):
     f16 = path == "tc"
     pw = cr.convrot_prepare_weights(wl.weights[0][:512].cuda(), 256, "h4", with_f16=f16)
     X = wl.X.cuda()
-    full = cr.convrot_linear(cr.convrot_quantize_act(X, 256, "h4", with_f16=f16), pw)
-    parts = [cr.convrot_linear(cr.convrot_quantize_act(X[r:r + 100], 256, "h4", with_f16=f16), pw)
+    full = cr.convrot_linear(cr.convrot_quantize_act(X, 256, "h4", with_f16=f16), pw, int8_mma=path == "mma")
+    parts = [cr.convrot_linear(cr.convrot_quantize_act(X[r:r + 100], 256, "h4", with_f16=f16), pw, int8_mma=path == "mma")
              for r in range(0, 300, 100)]
     assert torch.equal(full, torch.cat(parts))
 
@@ -150,8 +150,11 @@ def test_paths_agree(cr):
     pw = cr.convrot_prepare_weights(wl.weights[0][:640].cuda(), 256, "h4", with_f16=True)
     a = cr.convrot_quantize_act(wl.X.cuda(), 256, "h4", with_f16=True)
     a_int8 = cr.PackedAct(a.q, a.scale, None, a.group, a.transform)
-    assert torch.equal(cr.convrot_gemm_s32(a, pw), cr.convrot_gemm_s32(a_int8, pw))
-    assert torch.equal(cr.convrot_linear(a, pw), cr.convrot_linear(a_int8, pw))
+    assert torch.equal(cr.convrot_gemm_s32(a, pw), cr.convrot_gemm_s32(a_int8, pw, int8_mma=True))
+    assert torch.equal(cr.convrot_linear(a, pw), cr.convrot_linear(a_int8, pw, int8_mma=True))
+    # without the activation's fp16 copy the tensor-core path is not silently replaced
+    with pytest.raises(cr.ConvRotError, match="fp16 operand copies"):
+        cr.convrot_linear(a_int8, pw)
 
 
 def test_output_stride_and_empty(cr):
@@ -253,10 +256,10 @@ def test_epilogue_ragged_columns_and_row_pitch(cr, path, N, ld):
     w = packed_from_codes(cr, Qw, sw, 0, "none", path == "tc", "w")
     A = O.int_gemm(Qx, Qw)
     if ld is None:
-        Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda())
+        Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda(), int8_mma=path == "mma")
     else:
         big = torch.full((M, ld), 7.0, dtype=torch.bfloat16, device="cuda")
-        Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda(), out=big[:, :N])
+        Y = cr.convrot_linear(a, w, torch.from_numpy(bias).cuda(), out=big[:, :N], int8_mma=path == "mma")
         assert torch.all(big[:, N:] == 7.0)
     check_y_same_codes(to_np(Y.float()), A, sx.astype(np.float32), sw.astype(np.float32), bias, f"{path}/{N}/{ld}")
 
