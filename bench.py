@@ -19,6 +19,15 @@ with nvidia-smi during the timed region. The e2e figure repeats the step
 through the public API with host buffers: pinned X copied in, Y copied
 back, inside the timed region.
 
+Default workload: the large-M qkv linear (X bf16 [32700, 3072], three
+3072-wide linears sharing one packed activation, G = 256), the largest
+single-GPU configuration; `--secondary` adds the DiT 4096x6144x6144 step,
+GEMM and rotate+quantize times to the same line. The line also carries the
+integer tensor-path probe (cuBLASLt int8 and this library's int8 warp-MMA
+GEMM at 8192^3, beside torch's fp16 matmul) that the roofline's denominator
+choice rests on, and, from the CPU-baseline leg, the GPU codes compared with
+the oracle's on the sampled rows.
+
 `--impl reference` times the CPU oracle (fp64 numpy) on a bounded row
 sample of the same workload, on the host cores.
 """
@@ -257,13 +266,34 @@ def oracle_sample(wl, rows: int, seed: int = 0):
     idx = np.sort(rng.choice(wl.M, size=min(rows, wl.M), replace=False))
     X64 = wl.X[torch.from_numpy(idx)].float().numpy().astype(np.float64)
     t0 = time.perf_counter()
-    Qx, sx, _ = O.quantize_act(X64, wl.group, wl.transform, sg, qmax)
+    Qx, sx, v = O.quantize_act(X64, wl.group, wl.transform, sg, qmax)
     t1 = time.perf_counter()
     for (Qw, sw, _), b in zip(Ws, wl.biases):
         O.round_to_bf16(O.reconstruct(O.int_gemm(Qx, Qw), sx, sw, b.numpy()))
     t2 = time.perf_counter()
     ops = 2.0 * len(idx) * sum(wl.Ns) * wl.K
-    return {"rows": len(idx), "seconds": t2 - t0, "quant_seconds": t1 - t0, "ops": ops}
+    return {"rows": len(idx), "seconds": t2 - t0, "quant_seconds": t1 - t0, "ops": ops,
+            "idx": idx, "Qx": Qx, "sx": sx, "v": v}
+
+
+def code_parity(ref, q_gpu, s_gpu, bits: int):
+    """The GPU's codes and scales on the oracle's sampled rows: code flips
+    (|dQ| = 1 near a rounding boundary is the tolerated case), the largest
+    distance of a flipped code's fp64 value to its boundary, and the largest
+    relative scale error."""
+    import oracle as O
+    q = q_gpu[ref["idx"]]
+    if bits == 4:
+        q = O.unpack_int4(q)
+    d = q.astype(np.int64) - ref["Qx"].astype(np.int64)
+    flips = d != 0
+    dist = O.boundary_distance(ref["v"][flips])
+    s_ref = ref["sx"].astype(np.float64)
+    s_err = np.abs(s_gpu[ref["idx"]].astype(np.float64) - s_ref) / np.where(s_ref > 0, s_ref, 1.0)
+    return {"rows": int(len(ref["idx"])), "elements": int(d.size), "flips": int(flips.sum()),
+            "max_abs_dq": int(np.abs(d).max(initial=0)),
+            "code_flip_max_boundary_distance": float(dist.max()) if dist.size else None,
+            "scale_max_rel_err": float(s_err.max(initial=0.0))}
 
 
 def reference_main(args, world, rank):
@@ -292,6 +322,83 @@ def reference_main(args, world, rank):
 
 # --------------------------------------------------------------------- GPU ---
 
+def _best_ms(fn, reps: int = 5, warm: int = 2) -> float:
+    for _ in range(warm):
+        fn()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    return best
+
+
+def int8_peak_probe(cr, dev, n: int = 8192) -> dict:
+    """The integer tensor paths this chip offers, at n^3: cuBLASLt's int8
+    GEMM (torch._int_mm, measurement only) and this library's int8 warp-MMA
+    GEMM, beside torch's fp16 matmul. sm_103a has no integer tcgen05 MMA, so
+    the library feeds the int8 codes to the fp16 tensor cores (exact); its
+    roofline is the bf16/fp16 dense peak, the fastest exact path there is."""
+    g = torch.Generator(device="cpu").manual_seed(11)
+    a8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, generator=g).to(dev)
+    b8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, generator=g).to(dev)
+    ops = 2.0 * n ** 3
+    res = {"shape": f"{n}x{n}x{n}"}
+    try:
+        bt = b8.t()
+        res["int_mm_tops"] = ops / _best_ms(lambda: torch._int_mm(a8, bt)) / 1e9
+    except RuntimeError as e:  # not every torch build has it for this arch
+        res["int_mm_tops"] = None
+        res["int_mm_error"] = str(e).splitlines()[0][:120]
+    ones_x = torch.ones(n, dtype=torch.float32, device=dev)
+    act = cr.PackedAct(a8, ones_x, None, 0, cr.TRANSFORMS["none"])
+    w = cr.PackedWeight(b8, ones_x.clone(), None, 0, cr.TRANSFORMS["none"])
+    y = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+    res["int8_mma_sync_tops"] = ops / _best_ms(lambda: cr.convrot_linear(act, w, out=y, int8_mma=True)) / 1e9
+    h = a8.to(torch.float16)
+    ht = b8.to(torch.float16).t()
+    res["fp16_matmul_tflops"] = ops / _best_ms(lambda: torch.matmul(h, ht)) / 1e9
+    if cr.convrot_get_device_status() != 0:
+        raise RuntimeError("device status after the int8 probe")
+    best_int = max(v for v in (res["int_mm_tops"], res["int8_mma_sync_tops"]) if v is not None)
+    res["best_integer_path_tops"] = best_int
+    res["denominator"] = ("bf16 dense burst peak (MEASURED_PEAKS.json): the int8 codes run exactly on the "
+                          "fp16 tensor cores, whose rate equals bf16's; the integer paths above are "
+                          "the dense INT8 figures this chip offers")
+    return res
+
+
+def read_floor(dev, nbytes: int, flush_l2, steps: int, warmup: int) -> dict:
+    """A plain read of nbytes from HBM (torch amax over an fp32 buffer of that
+    size) and a plain copy of them, timed like a step (L2 flushed, GPU-side
+    pause): the practical floor for streaming that many bytes once."""
+    src = torch.zeros(max(1, nbytes // 4), dtype=torch.float32, device=dev)
+    dst = torch.empty_like(src)
+    out = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        marks = []
+        for i in range(warmup + steps):
+            flush_l2()
+            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= warmup:
+                marks.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in marks) * 1e3
+
+    return {"bytes": 4 * src.numel(), "read_us": timed(lambda: torch.amax(src, dim=0, out=out)),
+            "copy_us": timed(lambda: dst.copy_(src))}
+
+
 def l2_flusher(dev):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -304,6 +411,55 @@ def l2_flusher(dev):
         torch.sum(flush_rd, dim=0, out=flush_sink)
 
     return flush_l2
+
+
+
+def secondary_figures(cr, args, name, dev, flush_l2) -> dict:
+    """Step, GEMM and rotate+quantize (int8 contract) times of a second 8-bit
+    workload, same protocol as the main line (L2 flushed, GPU-side pause,
+    CUDA events on the launching stream)."""
+    wl = WORKLOADS[name]()
+    stream = torch.cuda.current_stream()
+    sg = None if wl.signs is None else wl.signs.to(dev)
+    use_f16 = wl.M > 64
+    ws = [cr.convrot_prepare_weights(W.to(dev), wl.group, wl.transform, sg, with_f16=use_f16) for W in wl.weights]
+    bs = [b.to(dev) for b in wl.biases]
+    X = wl.X.to(dev)
+    outs = [torch.empty((wl.M, n), dtype=torch.bfloat16, device=dev) for n in wl.Ns]
+    gws = cr.gemm_workspace(dev)
+    scratch = cr.int8_linear_scratch(wl.M, wl.K, dev)
+    act = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=use_f16)
+    act8 = cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False)
+
+    def timed(fn):
+        marks = []
+        for i in range(args.warmup + args.steps):
+            flush_l2()
+            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                marks.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in marks) / 1e3
+
+    step_s = timed(lambda: cr.convrot_int8_linear(X, ws, bs, signs=sg, outs=outs, scratch=scratch, workspace=gws))
+    gemm_s = timed(lambda: cr.convrot_linear_multi(act, ws, bs, outs=outs, workspace=gws))
+    q_s = timed(lambda: cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False, out=act8))
+    if cr.convrot_get_device_status() != 0:
+        raise RuntimeError(f"device status after the {name} figures")
+    pk = peaks()
+    M, K, Ns = wl.M, wl.K, wl.Ns
+    ops = 2.0 * M * sum(Ns) * K
+    q_bytes = 3 * M * K + 4 * M
+    gemm_tflops = ops / gemm_s / 1e12
+    return {"workload": wl.name, "step_us": step_s * 1e6, "step_tops": ops / step_s / 1e12,
+            "gemm_us": gemm_s * 1e6, "gemm_tflops": gemm_tflops,
+            "gemm_frac": gemm_tflops / pk["bf16_tflops"] if use_f16 else None,
+            "rotate_quant": {"kernel": rq_kernel_name(wl), "us": q_s * 1e6, "algorithmic_bytes": q_bytes,
+                             "gbs": q_bytes / q_s / 1e9, "frac": q_bytes / q_s / 1e9 / pk["hbm_gbs"]}}
 
 
 def gpu_main(args, world, rank, local):
@@ -469,9 +625,24 @@ def gpu_main(args, world, rank, local):
     else:
         w_bytes = sum(n * K + 4 * n for n in Ns) + M * K + 4 * M + 2 * M * sum(Ns)
         gbs = w_bytes / gemm_s / 1e9
-        dominant = {"kernel": "gemm_small_kernel", "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+        floor = read_floor(dev, w_bytes, flush_l2, args.steps, args.warmup)
+        dominant = {"kernel": "gemm_small_tc_kernel" if M > 16 and K % 128 == 0 else "gemm_small_kernel",
+                    "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
                     "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None,
-                    "peak_note": f"{pk['source']} HBM copy bandwidth"}
+                    "peak_note": f"{pk['source']} HBM copy bandwidth",
+                    "read_floor": dict(floor, gemm_us=gemm_s * 1e6,
+                                       ratio_to_read=gemm_s * 1e6 / floor["read_us"],
+                                       ratio_to_copy=gemm_s * 1e6 / floor["copy_us"],
+                                       note="the weight-stream GEMM against a plain torch read (amax) and copy "
+                                            "of the same number of bytes, same flush and pause")}
+
+    secondary = None
+    if args.secondary != "none" and args.secondary != args.workload and bits == 8:
+        secondary = secondary_figures(cr, args, args.secondary, dev, flush_l2)
+    probe = None if args.no_int8_probe else int8_peak_probe(cr, dev)
+    if probe is not None and use_f16 and bits == 8:
+        probe["gemm_over_best_integer_path"] = gemm_tflops / probe["best_integer_path_tops"]
+        probe["gemm_frac_of_fp16_matmul"] = gemm_tflops / probe["fp16_matmul_tflops"]
 
     # ---- end to end through the public API with host buffers: every step
     # copies its X in from pinned host memory and its Y back out; three streams
@@ -551,6 +722,8 @@ def gpu_main(args, world, rank, local):
             "frac": q_bytes / (statistics.mean(hm_ms) / 1e3) / 1e9 / pk["hbm_gbs"],
             "tensor_tflops": 2.0 * M * K * max(wl.group, 64) / (statistics.mean(hm_ms) / 1e3) / 1e12},
         "gemm_us": gemm_s * 1e6,
+        "int8_peak_probe": probe,
+        "secondary": secondary,
         "gpu_launches": 2 * args.steps,
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": 2 * M * K,
                 "d2h_bytes_per_step": 2 * M * sum(Ns), "ms_per_step": statistics.mean(e2e_ms),
@@ -560,18 +733,27 @@ def gpu_main(args, world, rank, local):
         "host_us_per_step": statistics.median(host_us),
     }
     if world == 1 and not args.no_cpu_baseline:
-        # about 10 s of oracle work: seeded row samples of the same workload
+        # about 10 s of oracle work: seeded row samples of the same workload;
+        # the first sample's codes are also compared with the GPU's int8-only
+        # launch on the same rows
         secs, ops, rows, reps = 0.0, 0.0, 0, 0
+        q_gpu = (act8.q4 if bits == 4 else act8.q).cpu().numpy()
+        s_gpu = act8.scale.cpu().numpy()
+        parity = None
         while secs < args.cpu_seconds:
             ref = oracle_sample(wl, args.ref_rows, seed=100 + reps)
             secs += ref["seconds"]
             ops += ref["ops"]
             rows += ref["rows"]
+            if parity is None:
+                parity = code_parity(ref, q_gpu, s_gpu, bits)
             reps += 1
         cores = blas_threads()
         line["cpu_baseline"] = {"value": ops / secs / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
                                 "sample": f"{reps} x {args.ref_rows} seeded rows of {M} ({rows} rows, full K, "
                                           f"all N), fp64 numpy, {secs:.1f} s"}
+        line["code_parity"] = dict(parity, tolerance="|dQ| <= 1 on <= 1e-4 of elements, flips within "
+                                                     "1e-6 * 127 code units of a rounding boundary")
     print(json.dumps(line), flush=True)
 
 
@@ -722,7 +904,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="dit6144", choices=sorted(WORKLOADS) + sorted(BLOCKS))
+    ap.add_argument("--workload", default="qkv32700", choices=sorted(WORKLOADS) + sorted(BLOCKS))
+    ap.add_argument("--secondary", default="dit6144", choices=["none"] + sorted(WORKLOADS),
+                    help="a second 8-bit workload whose step, GEMM and rotate+quantize times go in the same line")
+    ap.add_argument("--no-int8-probe", action="store_true",
+                    help="skip the integer tensor-path probe (torch._int_mm, the int8 warp-MMA GEMM)")
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",

@@ -83,3 +83,22 @@ def test_static_scratch_allocates_nothing(cr):
     assert free1 == free0
     assert torch.cuda.memory_allocated() == alloc0
     assert cr.convrot_get_device_status() == 0
+
+
+def test_static_scratch_is_cleared_after_a_timeout(cr):
+    """A kernel that gives up a bounded wait records a timeout; reading the
+    device status then clears the static scratch, where an aborted split
+    could have left partial sums. The recovery runs here because an earlier
+    static call has located the scratch; the next static call still equals
+    the unsplit call bit for bit."""
+    a, ws, _, _, host = _codes(cr, 300, 1000, 1024, 9)
+    bs = [torch.from_numpy(b).cuda() for _, _, b in host]
+    y0 = cr.convrot_linear_multi(a, ws, bs)[0]
+    assert torch.equal(cr.convrot_linear_multi_static(a, ws, bs)[0], y0)
+    assert cr.convrot_get_device_status() == 0
+    cr.convrot_selftest_wait_timeout(2000)
+    assert cr.convrot_get_device_status() == 5   # CONVROT_ERR_TIMEOUT, scratch cleared
+    assert cr.convrot_get_device_status() == 0
+    for _ in range(2):
+        assert torch.equal(cr.convrot_linear_multi_static(a, ws, bs)[0], y0)
+    assert cr.convrot_get_device_status() == 0
