@@ -123,10 +123,14 @@ WORKLOADS = {
 
 def rq_kernel_name(wl) -> str:
     """The rotate+quantize kernel the library picks for this workload (bf16,
-    aligned torch buffers, K a multiple of 64)."""
+    aligned torch buffers)."""
     lines = wl.K // 64
     parts = (lines + 255) // 256
-    lane = (wl.K % 64 == 0 and K_LANE_MAX >= wl.K and lines % parts == 0 and (parts == 1 or (lines // parts) % 8 == 0) and
+    boxes = wl.K % 64 == 0 and lines % parts == 0 and (parts == 1 or (lines // parts) % 8 == 0)
+    if (boxes and getattr(wl, "bits", 8) == 8 and wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)
+            and wl.K % max(256, wl.group) == 0):
+        return "rq_mma_kernel"
+    lane = (boxes and K_LANE_MAX >= wl.K and
             ((wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)) or
              (wl.transform == "rht" and 2 <= wl.group <= 256) or wl.transform == "none"))
     return "rq_lane_kernel" if lane else "rq_generic_kernel"
@@ -595,6 +599,13 @@ def gpu_main(args, world, rank, local):
                 hm_ms.append((b0, b1))
         torch.cuda.synchronize()
         hm_ms = [b0.elapsed_time(b1) for b0, b1 in hm_ms]
+    # the same contract on the all-fp32 register butterfly kernel, where the
+    # library runs the tensor-core stage instead
+    bf_ms = None
+    if bits == 8 and rq_kernel_name(wl) == "rq_mma_kernel":
+        actb = quant(X, False)
+        bf_ms = timed(lambda: cr.convrot_quantize_act_kernel(X, wl.group, wl.transform, sg, kernel="butterfly",
+                                                             with_f16=False, out=actb))
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
 
@@ -721,6 +732,10 @@ def gpu_main(args, world, rank, local):
             "gbs": q_bytes / (statistics.mean(hm_ms) / 1e3) / 1e9,
             "frac": q_bytes / (statistics.mean(hm_ms) / 1e3) / 1e9 / pk["hbm_gbs"],
             "tensor_tflops": 2.0 * M * K * max(wl.group, 64) / (statistics.mean(hm_ms) / 1e3) / 1e12},
+        "rotate_quant_butterfly": None if bf_ms is None else {
+            "kernel": "rq_lane_kernel", "us": statistics.mean(bf_ms) * 1e3,
+            "gbs": q_bytes / (statistics.mean(bf_ms) / 1e3) / 1e9,
+            "frac": q_bytes / (statistics.mean(bf_ms) / 1e3) / 1e9 / pk["hbm_gbs"]},
         "gemm_us": gemm_s * 1e6,
         "int8_peak_probe": probe,
         "secondary": secondary,

@@ -130,6 +130,35 @@ convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t
                                     int8_t* Qx, float* sx, uint16_t* Qx_f16,
                                     cudaStream_t stream);
 
+/* convrot_quantize_act with the kernel chosen by the caller (a diagnostic
+ * and test entry point; the pages have no counterpart). kernel:
+ *   CONVROT_RQ_AUTO         what convrot_quantize_act runs (the fastest one
+ *                           that takes the shape);
+ *   CONVROT_RQ_GENERIC      one CTA per row, every stage through shared
+ *                           memory (any transform, alignment and K);
+ *   CONVROT_RQ_BUTTERFLY    the register kernel: every radix stage on fp32
+ *                           registers, bit-identical to the generic kernel;
+ *   CONVROT_RQ_TENSOR_CORE  the regular Hadamard with its 16-point stage on
+ *                           the tensor cores (mma.sync bf16 -> fp32 from the
+ *                           staged tile) and the higher digits on fp32
+ *                           registers: G in {4, 16, 64, 256, 1024}, K a
+ *                           multiple of 256 (1024 for G = 1024). The tensor
+ *                           core sums its 16 exact products in fp32 in its own
+ *                           order, so codes can differ from the butterfly's
+ *                           by one where the value lies within a few fp32
+ *                           ulps of a rounding boundary.
+ * The fast kernels want X 16-byte and Qx, Qx_f16 32-byte aligned. Arguments
+ * and errors as convrot_quantize_act, plus INVALID_ARG when the chosen kernel
+ * does not take the shape or alignment (nothing is launched then). */
+#define CONVROT_RQ_AUTO 0
+#define CONVROT_RQ_GENERIC 1
+#define CONVROT_RQ_BUTTERFLY 2
+#define CONVROT_RQ_TENSOR_CORE 3
+convrot_status convrot_quantize_act_kernel(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                           int32_t group, int32_t transform, const int8_t* signs,
+                                           int8_t* Qx, float* sx, uint16_t* Qx_f16, int32_t kernel,
+                                           cudaStream_t stream);
+
 /* The H-as-a-matrix variant of convrot_quantize_act: each group is multiplied
  * by the dense G x G rotation on the tensor cores ("feat: load ConvRot int4
  * and per-channel int8 safetensors", section "The rotation": the rotation

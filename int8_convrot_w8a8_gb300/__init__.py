@@ -26,6 +26,7 @@ import torch
 __all__ = [
     "ConvRotError", "PackedAct", "PackedWeight", "ConvRotLinear", "TRANSFORMS",
     "convrot_prepare_weights", "convrot_quantize_act", "convrot_quantize_act_hmatmul",
+    "convrot_quantize_act_kernel", "RQ_KERNELS",
     "convrot_linear", "convrot_linear_multi", "convrot_linear_multi_static", "convrot_gemm_s32", "gemm_workspace",
     "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
     "PackedAct4", "PackedWeight4", "convrot_prepare_weights4", "convrot_quantize_act4", "convrot_linear4",
@@ -90,6 +91,7 @@ _SIGS = {
     "convrot_prepare_weights": [_P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
     "convrot_quantize_act": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
     "convrot_quantize_act_hmatmul": [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P],
+    "convrot_quantize_act_kernel": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P],
     "convrot_linear": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _P, _I64, _P],
     "convrot_linear_multi": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                              ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
@@ -224,6 +226,32 @@ def convrot_quantize_act(X: torch.Tensor, group: int, transform="h4", signs: Opt
         out = PackedAct(q, s, q16, group, t)
     _check(lib.convrot_quantize_act(X.data_ptr(), M, K, X.stride(0), group, t, _ptr(signs), out.q.data_ptr(),
                                     out.scale.data_ptr(), _ptr(out.q_f16), _stream(stream)))
+    return out
+
+
+RQ_KERNELS = {"auto": 0, "generic": 1, "butterfly": 2, "tensor_core": 3}
+
+
+def convrot_quantize_act_kernel(X: torch.Tensor, group: int, transform="h4", signs: Optional[torch.Tensor] = None,
+                                kernel: str = "auto", with_f16: bool = True, out: Optional[PackedAct] = None,
+                                stream=None) -> PackedAct:
+    """convrot_quantize_act with the rotate+quantize kernel chosen by name
+    ("auto", "generic", "butterfly", "tensor_core"); raises if that kernel
+    does not take the shape."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2:
+        raise TypeError("X must be a 2-D bf16 tensor")
+    if X.stride(1) != 1:
+        X = X.contiguous()
+    M, K = X.shape
+    t = _transform_id(transform)
+    if out is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        s = torch.empty((M,), dtype=torch.float32, device=X.device)
+        q16 = torch.empty((M, K), dtype=torch.float16, device=X.device) if with_f16 else None
+        out = PackedAct(q, s, q16, group, t)
+    _check(lib.convrot_quantize_act_kernel(X.data_ptr(), M, K, X.stride(0), group, t, _ptr(signs),
+                                           out.q.data_ptr(), out.scale.data_ptr(), _ptr(out.q_f16),
+                                           RQ_KERNELS[kernel], _stream(stream)))
     return out
 
 

@@ -13,7 +13,7 @@
 namespace convrot {
 
 cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, long long ldx, int G, int transform,
-                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic, int qm,
+                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int kernel, int qm,
                             cudaStream_t st, int* path);
 cudaError_t hmatmul_launch(const void* X, long long M, int K, long long ldx, int G, int8_t* Q, float* S,
                            uint16_t* Q16, cudaStream_t st);
@@ -283,7 +283,7 @@ convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N
     return fail(CONVROT_ERR_ALIGNMENT, "pointers must be 16-byte aligned (scales 4-byte)");
   int path = 0;
   cudaError_t e = rotquant_launch(W, w_dtype, N, static_cast<int>(K), K, group, transform, signs, Qw, sw, Qw_f16,
-                                  w_dtype == CONVROT_DTYPE_F32, 127, stream, &path);
+                                  w_dtype == CONVROT_DTYPE_F32 ? kRqGeneric : kRqAuto, 127, stream, &path);
   if (e != cudaSuccess) return cuda_fail(e, "weight rotate/quantize launch");
   return ok();
 }
@@ -304,6 +304,33 @@ convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t
   cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs, Qx,
                                   sx, Qx_f16, 0, 127, stream, &path);
   if (e != cudaSuccess) return cuda_fail(e, "activation rotate/quantize launch");
+  return ok();
+}
+
+convrot_status convrot_quantize_act_kernel(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                           int32_t transform, const int8_t* signs, int8_t* Qx, float* sx,
+                                           uint16_t* Qx_f16, int32_t kernel, cudaStream_t stream) {
+  if (kernel < CONVROT_RQ_AUTO || kernel > CONVROT_RQ_TENSOR_CORE)
+    return fail(CONVROT_ERR_INVALID_ARG, "kernel %d is not a rotate+quantize kernel choice", kernel);
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (M == 0) return ok();
+  if (!X || !Qx || !sx) return fail(CONVROT_ERR_INVALID_ARG, "X, Qx and sx must be non-null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (transform == CONVROT_T_RHT && !signs) return fail(CONVROT_ERR_INVALID_ARG, "RHT needs the sign vector");
+  if (!aligned(X, 16) || ldx % 8 || !aligned(Qx, 16) || !aligned(sx, 4) || (Qx_f16 && !aligned(Qx_f16, 16)))
+    return fail(CONVROT_ERR_ALIGNMENT, "X, Qx, Qx_f16 must be 16-byte aligned and ldx a multiple of 8");
+  static_assert(CONVROT_RQ_GENERIC == kRqGeneric && CONVROT_RQ_BUTTERFLY == kRqLane &&
+                    CONVROT_RQ_TENSOR_CORE == kRqMma && CONVROT_RQ_AUTO == kRqAuto,
+                "kernel choice constants");
+  int path = 0;
+  cudaError_t e = rotquant_launch(X, CONVROT_DTYPE_BF16, M, static_cast<int>(K), ldx, group, transform, signs, Qx,
+                                  sx, Qx_f16, kernel, 127, stream, &path);
+  if (e != cudaSuccess) return cuda_fail(e, "activation rotate/quantize launch");
+  if (path < 0)
+    return fail(CONVROT_ERR_INVALID_ARG, "kernel %d does not take this shape (transform %d, G=%d, K=%lld, alignment)",
+                kernel, transform, group, static_cast<long long>(K));
   return ok();
 }
 
@@ -574,7 +601,7 @@ convrot_status convrot_prepare_weights4(const void* W, int32_t w_dtype, int64_t 
   int path = 0;
   cudaError_t e = rotquant_launch(W, w_dtype, N, static_cast<int>(K), K, group, transform, signs,
                                   reinterpret_cast<int8_t*>(Qw4), sw, reinterpret_cast<uint16_t*>(Qw_f8),
-                                  w_dtype == CONVROT_DTYPE_F32, 7, stream, &path);
+                                  w_dtype == CONVROT_DTYPE_F32 ? kRqGeneric : kRqAuto, 7, stream, &path);
   if (e != cudaSuccess) return cuda_fail(e, "4-bit weight rotate/quantize launch");
   return ok();
 }

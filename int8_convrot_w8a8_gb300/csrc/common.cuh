@@ -34,6 +34,10 @@ namespace convrot {
 
 int status_word_rotquant();
 
+// Rotate+quantize kernel choice (rotquant_launch): the fastest kernel that
+// takes the shape, or one kernel by name.
+constexpr int kRqAuto = 0, kRqGeneric = 1, kRqLane = 2, kRqMma = 3;
+
 // Host-side launch helpers. They remember, per device, the kernel attributes
 // already set and the occupancy / SM-count queries already answered, so a
 // call costs no repeated driver round trips. No device memory is involved.

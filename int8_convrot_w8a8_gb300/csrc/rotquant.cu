@@ -638,6 +638,288 @@ __global__ void __launch_bounds__(384) rq_lane_kernel(const __grid_constant__ CU
   }
 }
 
+// ========================================================== tensor-core ===
+// Regular Hadamard (G = 4 .. 1024, K a multiple of 256) with the two lowest
+// radix-4 digits, the 16-point stage, on the tensor cores: mma.sync m16n8k16
+// bf16 -> fp32 straight from the TMA-staged tile, against the unnormalized
+// +-1 matrix of that stage (exact in bf16; the products are exact and the
+// tensor core sums 16 of them in fp32). The digits above it run on fp32
+// registers, as in the register kernel, and the codes and scales follow the
+// same arithmetic (one division per row, one rounding per code).
+//
+// Work split. Every 256 consecutive values of a row form a superblock of 16
+// chunks of 16 values. A warp owns 8 consecutive superblocks of the tile;
+// the thread with MMA group id g = lane / 4 owns superblock g of its warp,
+// and in it positions 4t .. 4t + 3 (t = lane % 4) of all 16 chunks: the 64
+// values that the digits above the chunk combine.
+//  * A operand: 8 MMA tiles of 16 rows. Row g + 8h of tile u is chunk
+//    (2u + h) ^ g of superblock g, so every thread group meets each of its
+//    chunks once, and the XOR spreads the eight rows one ldmatrix phase
+//    reads over distinct 16-byte bank groups of the 128B-swizzled stage (the
+//    superblock's first line is 4 x its index, so the swizzle phase of each
+//    row is known on the host; the same holds for the int8 stores).
+//  * B operand: the 16 x 16 matrix with its output columns permuted so that
+//    the thread's four result columns are positions 4t .. 4t + 3 (n-block 0:
+//    4t, 4t + 1; n-block 1: 4t + 2, 4t + 3).
+//  * Results: slot s = 2u + h holds chunk s ^ g. The radix-4 stage is
+//    unchanged when all four digit values are XOR-ed with one constant (its
+//    -1 sits where b = a ^ 3), so the digits above the chunk run on slots,
+//    with compile-time register indices; across lanes (G = 1024) a partner's
+//    matching chunk sits in its slot s ^ (g ^ g_partner).
+//  * Row maximum, quantization and stores as in the register kernel; the
+//    codes leave as 4-byte words (4 consecutive codes), the fp16 copy as
+//    8-byte pieces.
+// Pipeline: persistent CTAs, a ring of STAGES TMA stages (3-D box of R
+// rows as 128-byte lines, 128B swizzle), each refilled with the tile STAGES
+// iterations ahead as soon as every warp has passed the row-max barrier.
+
+// Entry (p, k) of the unnormalized 16-point stage: the Kronecker square of
+// 2*H4 (entries +-1, -1 where the two digits satisfy b = a ^ 3), or for
+// G = 4 the block-diagonal I4 (x) 2*H4.
+__host__ __device__ constexpr float h16_entry(int G, int p, int k) {
+  const float lo = ((p & 3) ^ (k & 3)) == 3 ? -1.0f : 1.0f;
+  if (G == 4) return (p >> 2) == (k >> 2) ? lo : 0.0f;
+  return (((p >> 2) ^ (k >> 2)) == 3 ? -1.0f : 1.0f) * lo;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+constexpr int kMmaMaxWarps = 12;
+
+template <int G, int STAGES>
+__global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
+    const __grid_constant__ CUtensorMap xmap, long long M, int K, int R, int nsb, int8_t* __restrict__ Q,
+    float* __restrict__ S, __half* __restrict__ Q16, float s_div, int stage_bytes, int box_lines,
+    long long spin_limit) {
+  static_assert(G == 4 || G == 16 || G == 64 || G == 256 || G == 1024, "regular Hadamard group");
+  asm volatile("griddepcontrol.launch_dependents;");  // see rq_lane_kernel
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_base = smem_u32(smem);
+  // output staging: the tile's int8 codes [R, K] and fp16 copy [R, K] (each
+  // present when asked for), written out by one bulk copy per tile
+  const uint32_t tile_elems = static_cast<uint32_t>(R) * static_cast<uint32_t>(K);
+  const uint32_t out_q = stage_base + STAGES * stage_bytes;
+  const uint32_t out_h = out_q + (Q ? tile_elems : 0u);
+  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(
+      smem + STAGES * stage_bytes + (Q ? tile_elems : 0u) + (Q16 ? 2u * tile_elems : 0u));  // [3][R]
+  uint64_t* full = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));          // [STAGES]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long ntiles = (M + R - 1) / R;
+  const int lines_per_row = K >> 6;
+  const int sb_per_row = K >> 8;
+  const uint32_t tile_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(K) * 2u;
+
+  // ---- result side: this thread's superblock and positions
+  const int g = lane >> 2, t = lane & 3;
+  const int sb = warp * 8 + g;
+  const bool sb_valid = sb < nsb;
+  const int my_row = sb_valid ? sb / sb_per_row : -1;            // row within the tile
+  // staging addresses of positions 4t .. 4t + 3 of chunk 0 of this superblock
+  // (the superblocks of a tile are consecutive in the dense output)
+  const uint32_t my_q = out_q + static_cast<uint32_t>(sb) * 256u + 4u * t;
+  const uint32_t my_h = out_h + static_cast<uint32_t>(sb) * 512u + 8u * t;
+
+  // ---- operand side: the rows this lane addresses for ldmatrix.x4
+  // (matrix m = lane / 8: h = m & 1 picks row g + 8h, hf = m >> 1 the 8-value
+  // half of the chunk; the row's superblock is that of group lane % 8)
+  uint32_t a_off[8];
+  {
+    const int ga = lane & 7, h = (lane >> 3) & 1, hf = lane >> 4;
+    int sba = warp * 8 + ga;
+    if (sba >= nsb) sba = ga < nsb ? ga : 0;  // padding groups read real data; their results are dropped
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = (2 * u + h) ^ ga;
+      const int L = 4 * sba + (j >> 2);
+      const int c = (2 * (j & 3) + hf) ^ (L & 7);
+      a_off[u] = static_cast<uint32_t>(L * 128 + c * 16);
+    }
+  }
+  // ---- B fragments of the two n-blocks: b0 = rows k = 2t, 2t + 1 and b1 =
+  // rows 2t + 8, 2t + 9 of column n = g, which is position 4(g / 2) + 2nb + g % 2
+  uint32_t bfrag[2][2];
+#pragma unroll
+  for (int nb = 0; nb < 2; ++nb) {
+    const int p = 4 * (g >> 1) + 2 * nb + (g & 1);
+    bfrag[nb][0] = bf16x2_bits(h16_entry(G, p, 2 * t), h16_entry(G, p, 2 * t + 1));
+    bfrag[nb][1] = bf16x2_bits(h16_entry(G, p, 2 * t + 8), h16_entry(G, p, 2 * t + 9));
+  }
+
+  long long tile = blockIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the first STAGES tiles are in flight during the set-up below
+    for (int s = 0; s < STAGES; ++s) {
+      const long long tl = tile + static_cast<long long>(s) * gridDim.x;
+      if (tl >= ntiles) break;
+      mbar_expect_tx(&full[s], tile_bytes);
+      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
+        tma_load_3d(stage_base + s * stage_bytes + l0 * 128, &xmap, 0, l0, static_cast<int>(tl * R), &full[s]);
+    }
+  }
+  for (int i = tid; i < 3 * R; i += blockDim.x) rowmax_buf[i] = 0u;
+  __syncthreads();
+
+  const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+  for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+    const int st = it % STAGES;
+    unsigned int* rowmax = rowmax_buf + (it % 3) * R;
+    for (int i = tid; i < R; i += blockDim.x) rowmax_buf[((it + 1) % 3) * R + i] = 0u;
+    if (!mbar_wait_bounded(&full[st], (it / STAGES) & 1, spin_limit) && tid == 0) record_status(CONVROT_ERR_TIMEOUT);
+
+    // ---- 16-point stage on the tensor cores: v[s][nb] = positions
+    // (4t + 2nb, 4t + 2nb + 1) of the chunk in slot s
+    float2 v[16][2];
+    const uint32_t sbase = stage_base + st * stage_bytes;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint32_t a0, a1, a2, a3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                   : "r"(sbase + a_off[u]));
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        float d[4];
+        mma_bf16_16816(d, a0, a1, a2, a3, bfrag[nb][0], bfrag[nb][1]);
+        v[2 * u][nb] = make_float2(d[0], d[1]);
+        v[2 * u + 1][nb] = make_float2(d[2], d[3]);
+      }
+    }
+    // ---- digit 2 (chunk stride 1) and digit 3 (chunk stride 4) on slots
+    if constexpr (G >= 64) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int a = 0; a < 16; a += 4) h4_stage(v[a][q], v[a + 1][q], v[a + 2][q], v[a + 3][q]);
+    }
+    if constexpr (G >= 256) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) h4_stage(v[b][q], v[b + 4][q], v[b + 8][q], v[b + 12][q]);
+    }
+    // ---- digit 4 (G = 1024): the four superblocks of a group sit in groups
+    // g ^ {0, 1, 2, 3} (lanes ^ 4, ^ 8); partner g ^ c keeps my chunk in its
+    // slot s ^ c. u = x + x[a^1], w = x - x[a^1], y = u + w[a^2].
+    if constexpr (G == 1024) {
+      float2 w[16][2];
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float2 p;
+          p.x = __shfl_xor_sync(0xffffffffu, v[s ^ 1][q].x, 4);
+          p.y = __shfl_xor_sync(0xffffffffu, v[s ^ 1][q].y, 4);
+          w[s][q] = p;
+        }
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float2 p = w[s][q];
+          w[s][q] = f2_sub(v[s][q], p);
+          v[s][q] = f2_add(v[s][q], p);
+        }
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float2 p;
+          p.x = __shfl_xor_sync(0xffffffffu, w[s ^ 2][q].x, 8);
+          p.y = __shfl_xor_sync(0xffffffffu, w[s ^ 2][q].y, 8);
+          v[s][q] = f2_add(v[s][q], p);
+        }
+    }
+
+    // ---- row absmax
+    float m = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      m = fmax3(m, fabsf(v[s][0].x), fabsf(v[s][0].y));
+      m = fmax3(m, fabsf(v[s][1].x), fabsf(v[s][1].y));
+    }
+    {
+      const unsigned grp = __match_any_sync(0xffffffffu, my_row);
+      const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
+      if (sb_valid && lane == __ffs(grp) - 1) atomicMax(&rowmax[my_row], mx);
+    }
+    // the previous tile's bulk store has finished reading the staging buffers
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncthreads();
+    // every warp has read stage st: refill it with the tile STAGES rounds ahead
+    if (tid == 0) {
+      const long long nxt = tile + static_cast<long long>(STAGES) * gridDim.x;
+      if (nxt < ntiles) {
+        mbar_expect_tx(&full[st], tile_bytes);
+        for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
+          tma_load_3d(sbase + l0 * 128, &xmap, 0, l0, static_cast<int>(nxt * R), &full[st]);
+      }
+    }
+
+    // ---- quantize into the staging buffers (4-byte code words, 8-byte fp16
+    // pieces; both conflict-free), then one bulk copy per output
+    if (sb_valid) {
+      const float amax = __uint_as_float(rowmax[my_row]);
+      const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+      const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        const float2 t0 = f2_fma(v[s][0], inv2, mg2);  // positions 4t, 4t + 1
+        const float2 t1 = f2_fma(v[s][1], inv2, mg2);  // positions 4t + 2, 4t + 3
+        const uint32_t j = static_cast<uint32_t>(s ^ g);
+        if (Q) {
+          const uint32_t b01 = __byte_perm(__float_as_uint(t0.x), __float_as_uint(t0.y), 0x0040);
+          const uint32_t b23 = __byte_perm(__float_as_uint(t1.x), __float_as_uint(t1.y), 0x0040);
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(my_q + 16u * j), "r"(__byte_perm(b01, b23, 0x5410))
+                       : "memory");
+        }
+        if (Q16) {
+          const float2 c0 = f2_sub(t0, mg2), c1 = f2_sub(t1, mg2);
+          const __half2 h0 = __floats2half2_rn(c0.x, c0.y), h1 = __floats2half2_rn(c1.x, c1.y);
+          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(my_h + 32u * j),
+                       "r"(*reinterpret_cast<const uint32_t*>(&h0)), "r"(*reinterpret_cast<const uint32_t*>(&h1))
+                       : "memory");
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // staging writes -> the bulk copy
+    __syncthreads();
+    if (tid == 0) {
+      const long long rows = M - tile * R < R ? M - tile * R : R;
+      const long long e0 = tile * R * static_cast<long long>(K);
+      const uint32_t n = static_cast<uint32_t>(rows * K);
+      if (Q)
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Q + e0), "r"(out_q), "r"(n)
+                     : "memory");
+      if (Q16)
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Q16 + e0), "r"(out_h),
+                     "r"(2u * n)
+                     : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    for (int i = tid; i < R; i += blockDim.x)
+      if (tile * R + i < M) S[tile * R + i] = __uint_as_float(rowmax[i]) / s_div;
+  }
+  // the last bulk stores complete before the CTA (and its shared memory) ends
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ================================================================ host =====
 
 static float scale_divisor(int transform, int G, int qm) {
@@ -732,6 +1014,94 @@ static cudaError_t launch_lane_x(const __nv_bfloat16* X, long long M, int K, lon
   return cudaGetLastError();
 }
 
+// Tiles of the tensor-core kernel: R rows whose superblocks fill whole warps
+// (or nearly), at most kMmaMaxWarps warps and 48 KB per tile.
+static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
+  const int sbpr = K / 256;
+  int bestR = -1;
+  double best = -1.0;
+  for (int R = 1; R <= 64; ++R) {
+    const int nsb = R * sbpr;
+    const int warps = (nsb + 7) / 8;
+    if (warps > kMmaMaxWarps || static_cast<long long>(R) * K * 2 > 48 * 1024) break;
+    const double eff = static_cast<double>(nsb) / (8.0 * warps);
+    if (warps >= 2 && eff >= 0.999) {
+      bestR = R;
+      break;
+    }
+    if (eff > best + 1e-9) {
+      best = eff;
+      bestR = R;
+    }
+  }
+  if (bestR < 0) return false;
+  *R_out = bestR;
+  *nsb_out = bestR * sbpr;
+  return true;
+}
+
+template <int G, int STAGES>
+static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int R, int nsb, int box_lines, int8_t* Q,
+                                float* S, __half* Q16, cudaStream_t st, bool* launched) {
+  const int threads = 32 * ((nsb + 7) / 8);
+  const int stage_bytes = (R * K * 2 + 1023) / 1024 * 1024;
+  const int out_bytes = (Q ? R * K : 0) + (Q16 ? 2 * R * K : 0);
+  const int smem = 1024 + STAGES * stage_bytes + out_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 8;
+  auto kern = rq_mma_kernel<G, STAGES>;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = blocks_per_sm(reinterpret_cast<const void*>(kern), threads, smem, &per_sm);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaSuccess;
+  const long long tiles = (M + R - 1) / R;
+  const long long slots = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
+  const long long rounds = (tiles + slots - 1) / slots;
+  const long long grid = (tiles + rounds - 1) / rounds;
+  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, nsb, Q, S, Q16,
+                                                           scale_divisor(CONVROT_T_REGULAR_H4, G, 127), stage_bytes,
+                                                           box_lines, kDefaultSpinLimit);
+  *launched = true;
+  return cudaGetLastError();
+}
+
+// X viewed as [M][K / 64][64] bf16 with a box of R rows of box_lines lines
+// (128B swizzle); false if the encoder is missing or refuses.
+static bool make_x_map(const __nv_bfloat16* X, long long M, int K, long long ldx, int R, int box_lines,
+                       CUtensorMap* map) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(ldx) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_lines), static_cast<cuuint32_t>(R)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(X), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-core kernel: regular Hadamard, int8 codes (and fp16 copy), K a
+// multiple of 256 (1024 for G = 1024). *launched stays false for shapes it
+// does not take.
+template <int G>
+static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
+                              __half* Q16, cudaStream_t st, bool* launched) {
+  *launched = false;
+  if (K % 256 != 0 || (G == 1024 && K % 1024 != 0) || M > 0x7fffffffLL) return cudaSuccess;
+  int R = 0, nsb = 0;
+  if (!choose_rows_mma(K, &R, &nsb)) return cudaSuccess;
+  const int lines = K / 64;
+  const int parts = (lines + 255) / 256;
+  const int box_lines = lines / parts;
+  if (parts > 1 && (R != 1 || lines % parts != 0 || box_lines % 8 != 0)) return cudaSuccess;
+  CUtensorMap map;
+  if (!make_x_map(X, M, K, ldx, R, box_lines, &map)) return cudaSuccess;
+  const int tile = R * K * 2;
+  if (tile <= 16 * 1024) return launch_mma_s<G, 4>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  if (tile <= 32 * 1024) return launch_mma_s<G, 3>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  return launch_mma_s<G, 2>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+}
+
 // The randomized Hadamard's strides 64 and 128 go through the quad
 // transpose when a row is a whole number of quads (K a multiple of 256): the
 // stores then fill whole lines, as on the regular Hadamard path.
@@ -780,20 +1150,45 @@ static cudaError_t launch_lane_any(const __nv_bfloat16* xb, long long M, int K, 
 
 // qm = 127: int8 codes (Q) and fp16 copy (Q16), either but not both may be
 // null; qm = 7: packed 4-bit codes (Q, K / 2 bytes per row) and e4m3 copy
-// (Q16 as bytes).
+// (Q16 as bytes). kernel: kRqAuto picks the fastest kernel that takes the
+// shape; the others ask for one kernel (a diagnostic): *path = -1 if it does
+// not take the shape, else 0 = generic, 1 = register butterfly, 2 =
+// tensor-core stage.
 cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, long long ldx, int G, int transform,
-                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int force_generic, int qm,
+                            const int8_t* signs, int8_t* Q, float* S, uint16_t* Q16, int kernel, int qm,
                             cudaStream_t st, int* path) {
   *path = 0;
   if (M <= 0) return cudaSuccess;
   __half* q16 = reinterpret_cast<__half*>(Q16);
-  // the fast kernel reads X by TMA (16-byte aligned base, row stride a
-  // multiple of 16 bytes) and stores 32-byte pieces
+  // the fast kernels read X by TMA (16-byte aligned base, row stride a
+  // multiple of 16 bytes) and store 32-byte pieces
   const bool aligned32 = (reinterpret_cast<uintptr_t>(X) % 16 == 0) && (ldx % 8 == 0) &&
                          (reinterpret_cast<uintptr_t>(Q) % 32 == 0) &&
                          (Q16 == nullptr || reinterpret_cast<uintptr_t>(Q16) % 32 == 0);
-  if (!force_generic && in_dtype == CONVROT_DTYPE_BF16 && aligned32 && K % 16 == 0) {
-    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
+  const bool fast_ok = in_dtype == CONVROT_DTYPE_BF16 && aligned32 && K % 16 == 0;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
+  if (fast_ok && qm == 127 && transform == CONVROT_T_REGULAR_H4 && (kernel == kRqAuto || kernel == kRqMma)) {
+    bool launched = false;
+    cudaError_t e = cudaSuccess;
+    switch (G) {
+      case 4: e = launch_mma<4>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 16: e = launch_mma<16>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 64: e = launch_mma<64>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 256: e = launch_mma<256>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      case 1024: e = launch_mma<1024>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
+      default: break;
+    }
+    if (e != cudaSuccess) return e;
+    if (launched) {
+      *path = 2;
+      return cudaSuccess;
+    }
+  }
+  if (kernel == kRqMma) {
+    *path = -1;
+    return cudaSuccess;
+  }
+  if (fast_ok && (kernel == kRqAuto || kernel == kRqLane)) {
     bool launched = false;
     cudaError_t e = qm == 7 ? launch_lane_any<7>(xb, M, K, ldx, G, transform, signs, Q, S, q16, st, &launched)
                             : launch_lane_any<127>(xb, M, K, ldx, G, transform, signs, Q, S, q16, st, &launched);
@@ -802,6 +1197,10 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
       *path = 1;
       return cudaSuccess;
     }
+  }
+  if (kernel == kRqLane) {
+    *path = -1;
+    return cudaSuccess;
   }
   const int threads = 256;
   const size_t smem = static_cast<size_t>(K) * sizeof(float);

@@ -60,15 +60,15 @@ def test_tiny_workload_spikes_spread(cr):
     assert np.mean(np.abs(to_np(a.q)) > 10) > 0.5
 
 
-def test_fast_and_generic_paths_are_bit_identical(cr):
+def test_misaligned_outputs_take_the_generic_kernel(cr):
     """Outputs at a 16- but not 32-byte aligned address make the library take
-    the generic kernel; both kernels run the same fp32 operations in the same
-    order, so codes, scales and fp16 copies are equal bit for bit."""
+    the generic kernel: bit-identical to the butterfly kernel asked for by
+    name (both run the same fp32 operations in the same order)."""
     for G in (16, 64, 256, 1024):
         wl = WL.make_case(40, 4096, [], seed=11 + G, group=G)
         X = wl.X.cuda()
         M, K = X.shape
-        fast = cr.convrot_quantize_act(X, G, "h4")
+        fast = cr.convrot_quantize_act_kernel(X, G, "h4", kernel="butterfly")
         qbuf = torch.empty(M * K + 16, dtype=torch.int8, device="cuda")
         hbuf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
         q_un = qbuf[16:].view(M, K)
@@ -80,6 +80,44 @@ def test_fast_and_generic_paths_are_bit_identical(cr):
         assert torch.equal(gen.q, fast.q), G
         assert torch.equal(gen.scale, fast.scale), G
         assert torch.equal(gen.q_f16, fast.q_f16), G
+
+
+@pytest.mark.parametrize("M,K,G", [(37, 6144, 256), (130, 3072, 256), (33, 4096, 16), (33, 4096, 64),
+                                   (33, 4096, 1024), (7, 1024, 4), (37, 5376, 256), (37, 5376, 64),
+                                   (3, 21504, 256), (2, 24576, 1024), (1, 256, 16), (300, 1024, 1024)])
+def test_tensor_core_kernel_matches_oracle(cr, M, K, G):
+    """The 16-point stage on the tensor cores (mma.sync bf16 -> fp32 from the
+    staged tile), the higher digits on fp32 registers: codes and scales
+    against the oracle; against the all-fp32 butterfly kernel at most one
+    code apart, on at most 1e-4 of the elements (the tensor core sums its 16
+    exact products in its own order)."""
+    wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.001, outlier_scale=50.0, group=G, seed=M + K + 3 * G)
+    X = wl.X.cuda()
+    tc = cr.convrot_quantize_act_kernel(X, G, "h4", kernel="tensor_core")
+    auto = cr.convrot_quantize_act(X, G, "h4")
+    bf = cr.convrot_quantize_act_kernel(X, G, "h4", kernel="butterfly")
+    torch.cuda.synchronize()
+    Q, s, v = _oracle_act(wl.X, G, "h4")
+    check_codes(to_np(tc.q), Q, v, f"tc M{M} K{K} G{G}")
+    check_scales(to_np(tc.scale), s, f"tc M{M} K{K} G{G}")
+    assert torch.equal(tc.q_f16.float(), tc.q.float())
+    # the library's choice for this shape is the tensor-core kernel
+    assert torch.equal(auto.q, tc.q) and torch.equal(auto.scale, tc.scale) and torch.equal(auto.q_f16, tc.q_f16)
+    d = (tc.q.int() - bf.q.int()).abs()
+    assert int(d.max()) <= 1 and int((d > 0).sum()) <= max(1, int(1e-4 * d.numel()))
+
+
+def test_tensor_core_kernel_refuses_other_shapes(cr):
+    X = torch.zeros((4, 2688), dtype=torch.bfloat16, device="cuda")   # K not a multiple of 256
+    with pytest.raises(cr.ConvRotError, match="does not take"):
+        cr.convrot_quantize_act_kernel(X, 64, "h4", kernel="tensor_core")
+    Y = torch.zeros((4, 1536), dtype=torch.bfloat16, device="cuda")   # G = 1024 needs K % 1024 == 0
+    with pytest.raises(cr.ConvRotError):
+        cr.convrot_quantize_act_kernel(Y, 1024, "h4", kernel="tensor_core")
+    Z = torch.zeros((4, 1024), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(128, dtype=torch.int8, device="cuda")
+    with pytest.raises(cr.ConvRotError):                               # RHT stays on the butterfly
+        cr.convrot_quantize_act_kernel(Z, 128, "rht", g, kernel="tensor_core")
 
 
 def test_without_f16_copy(cr):
@@ -124,18 +162,27 @@ def test_quantize_act_rht_matches_oracle(cr, M, K, B):
 
 
 def _fast_and_generic(cr, X, G, transform, signs=None):
-    """The same call twice: outputs 32-byte aligned (register kernel) and at a
-    16- but not 32-byte aligned address (generic kernel)."""
-    M, K = X.shape
-    fast = cr.convrot_quantize_act(X, G, transform, signs)
-    qbuf = torch.empty(M * K + 16, dtype=torch.int8, device="cuda")
-    hbuf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
-    q_un, h_un = qbuf[16:].view(M, K), hbuf[8:].view(M, K)
-    assert q_un.data_ptr() % 32 == 16 and h_un.data_ptr() % 32 == 16
-    out = cr.PackedAct(q_un, torch.empty(M, dtype=torch.float32, device="cuda"), h_un, G, cr.TRANSFORMS[transform])
-    gen = cr.convrot_quantize_act(X, G, transform, signs, out=out)
+    """The register butterfly kernel and the generic kernel, each asked for
+    by name, on the same input (the generic kernel twice where the register
+    kernel does not take the shape, e.g. a row of 264 lines, which does not
+    split into TMA boxes that start on whole 1 KB swizzle atoms)."""
+    try:
+        fast = cr.convrot_quantize_act_kernel(X, G, transform, signs, kernel="butterfly")
+    except cr.ConvRotError as e:
+        assert "does not take" in str(e)
+        fast = cr.convrot_quantize_act_kernel(X, G, transform, signs, kernel="generic")
+    gen = cr.convrot_quantize_act_kernel(X, G, transform, signs, kernel="generic")
     torch.cuda.synchronize()
     return fast, gen
+
+
+def _check_auto(cr, X, G, transform, signs, Q, s, v, label):
+    """What convrot_quantize_act picks for the shape, against the oracle."""
+    a = cr.convrot_quantize_act(X, G, transform, signs)
+    torch.cuda.synchronize()
+    check_codes(to_np(a.q), Q, v, label + " auto")
+    check_scales(to_np(a.scale), s, label + " auto")
+    assert torch.equal(a.q_f16.float(), a.q.float())
 
 
 @pytest.mark.parametrize("M,K,B", [(37, 1152, 2), (37, 1152, 8), (37, 1152, 32), (37, 1152, 64),
@@ -182,6 +229,7 @@ def test_wide_rows_register_kernel(cr, M, K, G, transform):
     check_codes(to_np(fast.q), Q, v, f"{transform} G{G} K{K}")
     check_scales(to_np(fast.scale), s, f"{transform} G{G} K{K}")
     assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
+    _check_auto(cr, wl.X.cuda(), G, transform, sg, Q, s, v, f"{transform} G{G} K{K}")
 
 
 @pytest.mark.parametrize("M,K,G,transform", [(37, 5376, 256, "h4"), (37, 5376, 128, "rht"), (37, 5376, 64, "h4"),
@@ -200,6 +248,7 @@ def test_tiles_with_padding_threads(cr, M, K, G, transform):
     check_codes(to_np(fast.q), Q, v, f"{transform} G{G} K{K}")
     check_scales(to_np(fast.scale), s, f"{transform} G{G} K{K}")
     assert torch.equal(fast.q, gen.q) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f16, gen.q_f16)
+    _check_auto(cr, wl.X.cuda(), G, transform, sg, Q, s, v, f"{transform} G{G} K{K}")
 
 
 def test_quantize_act_none_matches_oracle(cr):
