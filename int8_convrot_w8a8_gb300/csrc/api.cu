@@ -33,6 +33,7 @@ cudaError_t gemm_small_tc_launch(const int8_t* Qx, const float* sx, long long M,
 bool gemm_small_tc_supported(long long M, int K);
 int status_word_gemm_small_tc();
 cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st);
+cudaError_t rq_sched_reset();
 
 CONVROT_DEFINE_STATUS_WORD(status_word_api)
 
@@ -729,6 +730,9 @@ convrot_status convrot_get_device_status(void) {
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
       if (e != cudaSuccess) return cuda_fail(e, "clearing the static GEMM scratch");
     }
+    // and the rotate+quantize tile hand-out counters
+    e = rq_sched_reset();
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the tile hand-out counters");
   }
   if (first == 0) return ok();
   if (timeout && first != CONVROT_ERR_TIMEOUT) first = CONVROT_ERR_TIMEOUT;

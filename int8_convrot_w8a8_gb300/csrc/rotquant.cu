@@ -27,6 +27,7 @@
 //    2j in the low nibble of byte j, plus an e4m3 copy (every integer in
 //    [-7, 7] is exact in e4m3) that the tensor cores read.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 
 #include "common.cuh"
@@ -697,11 +698,23 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 constexpr int kMmaMaxWarps = 12;
+constexpr int kMmaMinWarps = 6;
 
-template <int G, int STAGES>
+// Dynamic tile hand-out of the tensor-core kernel. Static round-robin tiles
+// leave the GPU waiting on its slowest CTAs (on GB300 the CTAs of one launch,
+// each with the same tile count, finish up to 25 % apart). Instead every CTA
+// claims its next tile from a counter; one counter pair (tiles claimed, CTAs
+// done) per launch slot, zero when the module loads; the last CTA of a launch
+// to finish puts its pair back to zero. Launches take the slots in turn, so
+// up to kRqSchedSlots launches may be in flight on a device at once.
+constexpr int kRqSchedSlots = 256;
+static __device__ unsigned int g_rq_sched[kRqSchedSlots][2];
+
+// WQ / WH: the int8 codes / the fp16 copy are written.
+template <int G, int STAGES, bool WQ, bool WH>
 __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     const __grid_constant__ CUtensorMap xmap, long long M, int K, int R, int nsb, int8_t* __restrict__ Q,
-    float* __restrict__ S, __half* __restrict__ Q16, float s_div, int stage_bytes, int box_lines,
+    float* __restrict__ S, __half* __restrict__ Q16, float s_div, int stage_bytes, int box_lines, int slot,
     long long spin_limit) {
   static_assert(G == 4 || G == 16 || G == 64 || G == 256 || G == 1024, "regular Hadamard group");
   asm volatile("griddepcontrol.launch_dependents;");  // see rq_lane_kernel
@@ -709,14 +722,16 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_base = smem_u32(smem);
-  // output staging: the tile's int8 codes [R, K] and fp16 copy [R, K] (each
-  // present when asked for), written out by one bulk copy per tile
+  // output staging: the tile's fp16 copy [R, K] and int8 codes [R, K] (each
+  // present when asked for; both start on a 512-byte boundary), written out
+  // by one bulk copy per tile
   const uint32_t tile_elems = static_cast<uint32_t>(R) * static_cast<uint32_t>(K);
-  const uint32_t out_q = stage_base + STAGES * stage_bytes;
-  const uint32_t out_h = out_q + (Q ? tile_elems : 0u);
+  const uint32_t out_h = stage_base + STAGES * stage_bytes;
+  const uint32_t out_q = out_h + (WH ? 2u * tile_elems : 0u);
   unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(
-      smem + STAGES * stage_bytes + (Q ? tile_elems : 0u) + (Q16 ? 2u * tile_elems : 0u));  // [3][R]
-  uint64_t* full = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));          // [STAGES]
+      smem + STAGES * stage_bytes + (WQ ? tile_elems : 0u) + (WH ? 2u * tile_elems : 0u));  // [3][R]
+  uint64_t* full = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));            // [STAGES]
+  long long* stage_tile = reinterpret_cast<long long*>(full + STAGES);                      // [STAGES]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long ntiles = (M + R - 1) / R;
@@ -729,10 +744,12 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   const int sb = warp * 8 + g;
   const bool sb_valid = sb < nsb;
   const int my_row = sb_valid ? sb / sb_per_row : -1;            // row within the tile
-  // staging addresses of positions 4t .. 4t + 3 of chunk 0 of this superblock
-  // (the superblocks of a tile are consecutive in the dense output)
-  const uint32_t my_q = out_q + static_cast<uint32_t>(sb) * 256u + 4u * t;
-  const uint32_t my_h = out_h + static_cast<uint32_t>(sb) * 512u + 8u * t;
+  // staging address of positions 4t .. 4t + 3 of chunk g of this superblock
+  // (the superblocks of a tile are consecutive in the dense output); chunk
+  // s ^ g is then at that address XOR 16 s (32 s for fp16), since the chunk
+  // offset bits of the superblock's base are zero
+  const uint32_t my_q = (out_q + static_cast<uint32_t>(sb) * 256u + 4u * t) | (16u * g);
+  const uint32_t my_h = (out_h + static_cast<uint32_t>(sb) * 512u + 8u * t) | (32u * g);
 
   // ---- operand side: the rows this lane addresses for ldmatrix.x4
   // (matrix m = lane / 8: h = m & 1 picks row g + 8h, hf = m >> 1 the 8-value
@@ -760,28 +777,47 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     bfrag[nb][1] = bf16x2_bits(h16_entry(G, p, 2 * t + 8), h16_entry(G, p, 2 * t + 9));
   }
 
-  long long tile = blockIdx.x;
+  // Tiles: the first STAGES rounds go out round-robin (tile blockIdx.x +
+  // k * gridDim.x for the k-th stage filled), the rest by claims on the
+  // counter, numbered from STAGES * gridDim.x. Only tid 0 claims, one claim
+  // ahead (the atomic's round trip overlaps a whole tile). Tiles come out in
+  // increasing order for each CTA, so once one lies past the end every later
+  // one does too, and a CTA leaves with no copy in flight.
+  unsigned int* claims = &g_rq_sched[slot][0];
+  const long long dyn_base = static_cast<long long>(STAGES) * gridDim.x;
+  unsigned int pending = 0;  // tid 0: the claim for the next refill
+  bool exhausted = false;    // tid 0: a claim came back past the end
+  auto fill = [&](int s, long long c) {  // tid 0: start stage s on tile c (or mark it empty)
+    if (c < ntiles) {
+      stage_tile[s] = c;
+      mbar_expect_tx(&full[s], tile_bytes);
+      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
+        tma_load_3d(stage_base + s * stage_bytes + l0 * 128, &xmap, 0, l0, static_cast<int>(c * R), &full[s]);
+    } else {
+      exhausted = true;
+      stage_tile[s] = -1;
+      mbar_arrive(&full[s]);
+    }
+  };
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the first STAGES tiles are in flight during the set-up below
-    for (int s = 0; s < STAGES; ++s) {
-      const long long tl = tile + static_cast<long long>(s) * gridDim.x;
-      if (tl >= ntiles) break;
-      mbar_expect_tx(&full[s], tile_bytes);
-      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
-        tma_load_3d(stage_base + s * stage_bytes + l0 * 128, &xmap, 0, l0, static_cast<int>(tl * R), &full[s]);
-    }
+    for (int s = 0; s < STAGES; ++s) fill(s, blockIdx.x + static_cast<long long>(s) * gridDim.x);
+    if (!exhausted) pending = atomicAdd(claims, 1u);
   }
   for (int i = tid; i < 3 * R; i += blockDim.x) rowmax_buf[i] = 0u;
   __syncthreads();
 
   const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
-  for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+  for (int it = 0;; ++it) {
     const int st = it % STAGES;
     unsigned int* rowmax = rowmax_buf + (it % 3) * R;
     for (int i = tid; i < R; i += blockDim.x) rowmax_buf[((it + 1) % 3) * R + i] = 0u;
     if (!mbar_wait_bounded(&full[st], (it / STAGES) & 1, spin_limit) && tid == 0) record_status(CONVROT_ERR_TIMEOUT);
+    // the stage's tile (written by tid 0 before its barrier phase completed)
+    const long long tile = *reinterpret_cast<volatile long long*>(&stage_tile[st]);
+    if (tile < 0) break;
 
     // ---- 16-point stage on the tensor cores: v[s][nb] = positions
     // (4t + 2nb, 4t + 2nb + 1) of the chunk in slot s
@@ -862,13 +898,13 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     // the previous tile's bulk store has finished reading the staging buffers
     if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     __syncthreads();
-    // every warp has read stage st: refill it with the tile STAGES rounds ahead
+    // every warp has read stage st (and its tile index): refill it
     if (tid == 0) {
-      const long long nxt = tile + static_cast<long long>(STAGES) * gridDim.x;
-      if (nxt < ntiles) {
-        mbar_expect_tx(&full[st], tile_bytes);
-        for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
-          tma_load_3d(sbase + l0 * 128, &xmap, 0, l0, static_cast<int>(nxt * R), &full[st]);
+      if (exhausted) {
+        fill(st, ntiles);
+      } else {
+        fill(st, dyn_base + pending);
+        if (!exhausted) pending = atomicAdd(claims, 1u);
       }
     }
 
@@ -882,17 +918,16 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
       for (int s = 0; s < 16; ++s) {
         const float2 t0 = f2_fma(v[s][0], inv2, mg2);  // positions 4t, 4t + 1
         const float2 t1 = f2_fma(v[s][1], inv2, mg2);  // positions 4t + 2, 4t + 3
-        const uint32_t j = static_cast<uint32_t>(s ^ g);
-        if (Q) {
+        if constexpr (WQ) {
           const uint32_t b01 = __byte_perm(__float_as_uint(t0.x), __float_as_uint(t0.y), 0x0040);
           const uint32_t b23 = __byte_perm(__float_as_uint(t1.x), __float_as_uint(t1.y), 0x0040);
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(my_q + 16u * j), "r"(__byte_perm(b01, b23, 0x5410))
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(my_q ^ (16u * s)), "r"(__byte_perm(b01, b23, 0x5410))
                        : "memory");
         }
-        if (Q16) {
+        if constexpr (WH) {
           const float2 c0 = f2_sub(t0, mg2), c1 = f2_sub(t1, mg2);
           const __half2 h0 = __floats2half2_rn(c0.x, c0.y), h1 = __floats2half2_rn(c1.x, c1.y);
-          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(my_h + 32u * j),
+          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(my_h ^ (32u * s)),
                        "r"(*reinterpret_cast<const uint32_t*>(&h0)), "r"(*reinterpret_cast<const uint32_t*>(&h1))
                        : "memory");
         }
@@ -904,10 +939,10 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
       const long long rows = M - tile * R < R ? M - tile * R : R;
       const long long e0 = tile * R * static_cast<long long>(K);
       const uint32_t n = static_cast<uint32_t>(rows * K);
-      if (Q)
+      if constexpr (WQ)
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Q + e0), "r"(out_q), "r"(n)
                      : "memory");
-      if (Q16)
+      if constexpr (WH)
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Q16 + e0), "r"(out_h),
                      "r"(2u * n)
                      : "memory");
@@ -916,8 +951,23 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     for (int i = tid; i < R; i += blockDim.x)
       if (tile * R + i < M) S[tile * R + i] = __uint_as_float(rowmax[i]) / s_div;
   }
-  // the last bulk stores complete before the CTA (and its shared memory) ends
-  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (tid == 0) {
+    // the last bulk stores complete before the CTA (and its shared memory) ends
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    // this CTA's claims are over; the last CTA of the launch resets the slot
+    __threadfence();
+    if (atomicAdd(&g_rq_sched[slot][1], 1u) == gridDim.x - 1) {
+      g_rq_sched[slot][0] = 0u;
+      g_rq_sched[slot][1] = 0u;
+    }
+  }
+}
+
+// Puts every launch slot of the tensor-core kernel's tile hand-out back to
+// zero (after a kernel gave up a wait; a completed launch restores its own).
+cudaError_t rq_sched_reset() {
+  static const unsigned int zero[kRqSchedSlots][2] = {};
+  return cudaMemcpyToSymbol(g_rq_sched, zero, sizeof(zero));
 }
 
 // ================================================================ host =====
@@ -1015,7 +1065,10 @@ static cudaError_t launch_lane_x(const __nv_bfloat16* X, long long M, int K, lon
 }
 
 // Tiles of the tensor-core kernel: R rows whose superblocks fill whole warps
-// (or nearly), at most kMmaMaxWarps warps and 48 KB per tile.
+// (or nearly), at least kMmaMinWarps warps where the shape allows, at most
+// kMmaMaxWarps warps and 48 KB per tile. Larger CTAs pay the two barriers of
+// a tile over more work (GB300: 6 warps of 24 KB tiles beat 2-3 warps of 8-12
+// KB tiles by 5-10 % on the DiT, qkv and group-sweep activations).
 static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
   const int sbpr = K / 256;
   int bestR = -1;
@@ -1025,7 +1078,7 @@ static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
     const int warps = (nsb + 7) / 8;
     if (warps > kMmaMaxWarps || static_cast<long long>(R) * K * 2 > 48 * 1024) break;
     const double eff = static_cast<double>(nsb) / (8.0 * warps);
-    if (warps >= 2 && eff >= 0.999) {
+    if (warps >= kMmaMinWarps && eff >= 0.999) {
       bestR = R;
       break;
     }
@@ -1040,14 +1093,14 @@ static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
   return true;
 }
 
-template <int G, int STAGES>
+template <int G, int STAGES, bool WQ, bool WH>
 static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int R, int nsb, int box_lines, int8_t* Q,
                                 float* S, __half* Q16, cudaStream_t st, bool* launched) {
   const int threads = 32 * ((nsb + 7) / 8);
   const int stage_bytes = (R * K * 2 + 1023) / 1024 * 1024;
-  const int out_bytes = (Q ? R * K : 0) + (Q16 ? 2 * R * K : 0);
-  const int smem = 1024 + STAGES * stage_bytes + out_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 8;
-  auto kern = rq_mma_kernel<G, STAGES>;
+  const int out_bytes = (WQ ? R * K : 0) + (WH ? 2 * R * K : 0);
+  const int smem = 1024 + STAGES * stage_bytes + out_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 16;
+  auto kern = rq_mma_kernel<G, STAGES, WQ, WH>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -1058,9 +1111,11 @@ static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int 
   const long long slots = std::min<long long>(tiles, static_cast<long long>(per_sm) * device_sm_count());
   const long long rounds = (tiles + slots - 1) / slots;
   const long long grid = (tiles + rounds - 1) / rounds;
+  static std::atomic<unsigned int> launches{0};
+  const int slot = static_cast<int>(launches.fetch_add(1u, std::memory_order_relaxed) % kRqSchedSlots);
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, nsb, Q, S, Q16,
                                                            scale_divisor(CONVROT_T_REGULAR_H4, G, 127), stage_bytes,
-                                                           box_lines, kDefaultSpinLimit);
+                                                           box_lines, slot, kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
 }
@@ -1096,10 +1151,19 @@ static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long l
   if (parts > 1 && (R != 1 || lines % parts != 0 || box_lines % 8 != 0)) return cudaSuccess;
   CUtensorMap map;
   if (!make_x_map(X, M, K, ldx, R, box_lines, &map)) return cudaSuccess;
+  // stages: up to three tiles in flight behind the one being worked on,
+  // within about 72 KB of staging per CTA
   const int tile = R * K * 2;
-  if (tile <= 16 * 1024) return launch_mma_s<G, 4>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
-  if (tile <= 32 * 1024) return launch_mma_s<G, 3>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
-  return launch_mma_s<G, 2>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  if (Q && Q16) {
+    if (tile <= 24 * 1024) return launch_mma_s<G, 3, true, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+    return launch_mma_s<G, 2, true, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  }
+  if (Q16) {
+    if (tile <= 24 * 1024) return launch_mma_s<G, 3, false, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+    return launch_mma_s<G, 2, false, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  }
+  if (tile <= 24 * 1024) return launch_mma_s<G, 3, true, false>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  return launch_mma_s<G, 2, true, false>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
 }
 
 // The randomized Hadamard's strides 64 and 128 go through the quad

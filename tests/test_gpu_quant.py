@@ -107,6 +107,32 @@ def test_tensor_core_kernel_matches_oracle(cr, M, K, G):
     assert int(d.max()) <= 1 and int((d > 0).sum()) <= max(1, int(1e-4 * d.numel()))
 
 
+def test_tensor_core_kernel_concurrent_launches(cr):
+    """The kernel hands out its tiles through a counter slot per launch:
+    launches in flight together on four streams, and 300 launches in a row
+    (more than the slots, so every slot is reused), each give the result of
+    a lone launch."""
+    wl = WL.make_case(300, 3072, [], seed=77, group=256)
+    X = wl.X.cuda()
+    ref = cr.convrot_quantize_act(X, 256, "h4")
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    outs = []
+    for i in range(40):
+        s = streams[i % 4]
+        with torch.cuda.stream(s):
+            outs.append(cr.convrot_quantize_act(X, 256, "h4", stream=s))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.q, ref.q) and torch.equal(o.scale, ref.scale) and torch.equal(o.q_f16, ref.q_f16)
+    a = cr.convrot_quantize_act(X, 256, "h4")
+    for _ in range(300):
+        cr.convrot_quantize_act(X, 256, "h4", out=a)
+    torch.cuda.synchronize()
+    assert torch.equal(a.q, ref.q) and torch.equal(a.scale, ref.scale)
+    assert cr.convrot_get_device_status() == 0
+
+
 def test_tensor_core_kernel_refuses_other_shapes(cr):
     X = torch.zeros((4, 2688), dtype=torch.bfloat16, device="cuda")   # K not a multiple of 256
     with pytest.raises(cr.ConvRotError, match="does not take"):
