@@ -122,8 +122,17 @@ convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N
  *   signs   device int8 [group] for CONVROT_T_RHT, else ignored.
  *   Qx      device int8 [M, K] (out), sx device fp32 [M] (out),
  *   Qx_f16  device fp16 [M, K] (out) or NULL.
- * X must be 16-byte aligned with ldx a multiple of 8; the fastest path is
- * taken when X is 32-byte aligned and ldx is a multiple of 16.
+ * X must be 16-byte aligned with ldx a multiple of 8. The fast kernels run
+ * when X is 16-byte aligned and Qx, Qx_f16 32-byte aligned: for the regular
+ * Hadamard with K a multiple of 256 (1024 for G = 1024) the tensor-core
+ * kernel (see convrot_quantize_act_kernel), else the register butterfly,
+ * else the generic kernel.
+ * The tensor-core kernel hands its tiles out through a small counter array
+ * of the library (one pair of counters per launch slot, 256 slots per
+ * device, zero when the library is loaded; each completed launch puts its
+ * slot back to zero; convrot_get_device_status() clears them all after a
+ * timeout). Launches take the slots in turn, so at most 256 rotate+quantize
+ * launches may be in flight on one device at the same time.
  * M == 0 is a no-op. */
 convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t ldx,
                                     int32_t group, int32_t transform, const int8_t* signs,
