@@ -56,6 +56,7 @@ __all__ = [
     "quantize_rows", "prepare_weights", "quantize_act", "int_gemm",
     "reconstruct", "round_to_bf16", "linear", "float_linear",
     "boundary_distance", "QMAX", "QMAX4", "pack_int4", "unpack_int4",
+    "row_absmax", "quantize_rows_given",
 ]
 
 # "INT8 Convrot Safetensors", "How INT8 convrot works": the printed matrix,
@@ -183,6 +184,35 @@ def quantize_rows(Xrot, qmax: int = QMAX):
     Xrot = np.asarray(Xrot, dtype=np.float64)
     amax = np.abs(Xrot).max(axis=1) if Xrot.shape[1] else np.zeros(Xrot.shape[0])
     s64 = amax / qmax
+    safe = np.where(s64 > 0, s64, 1.0)
+    v = np.where(s64[:, None] > 0, Xrot / safe[:, None], 0.0)
+    Q = np.clip(np.rint(v), -qmax, qmax).astype(np.int8)
+    return Q, s64.astype(np.float32), v, s64
+
+
+def row_absmax(Xrot) -> np.ndarray:
+    """max_i |X_rot[r, i]| for every row, in fp64: the numerator of the row
+    scale of "Runtime activation quantization"."""
+    Xrot = np.asarray(Xrot, dtype=np.float64)
+    return np.abs(Xrot).max(axis=1) if Xrot.shape[1] else np.zeros(Xrot.shape[0])
+
+
+def quantize_rows_given(Xrot, amax, qmax: int = QMAX):
+    """Per-row quantization with each row's maximum supplied instead of
+    taken over the given columns:
+
+        s[r]    = amax[r] / 127
+        Q[r, i] = clamp(round(X_rot[r, i] / s[r]), -127, 127)
+
+    This is the step a row-parallel linear needs (sglang digest, "风险与影响",
+    on tensor parallelism splitting the rotated input dimension over ranks,
+    each with whole groups): the scale belongs to the whole row, so its
+    maximum is the largest of the slices' maxima, and every slice is
+    quantized with it. With amax = row_absmax(Xrot) this is quantize_rows.
+    Returns (Q int8, s float32 as stored, v = X_rot / s in fp64, s in fp64).
+    """
+    Xrot = np.asarray(Xrot, dtype=np.float64)
+    s64 = np.asarray(amax, dtype=np.float64) / qmax
     safe = np.where(s64 > 0, s64, 1.0)
     v = np.where(s64[:, None] > 0, Xrot / safe[:, None], 0.0)
     Q = np.clip(np.rint(v), -qmax, qmax).astype(np.int8)

@@ -71,6 +71,21 @@ def load_rht_basis_rows():
     return [(b["B"], np.array(b["signs"]), np.array(b["rows"])) for b in blocks]
 
 
+def load_given_max_rows():
+    cases, cur = [], {}
+    with open(os.path.join(GOLDEN, "quantizer_given_max.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, *vals = line.split()
+            cur[tag] = [float(v) for v in vals]
+            if tag == "s":
+                cases.append(cur)
+                cur = {}
+    return cases
+
+
 # --------------------------------------------------------- pin predicates --
 # Written as predicates so the planted-mistake tests can reuse them.
 
@@ -383,6 +398,94 @@ def test_missing_rotation_gives_noise():
 def test_boundary_distance():
     d = O.boundary_distance(np.array([0.5, 1.0, -2.5, 2.499, -0.75]))
     assert np.allclose(d, [0.0, 0.5, 0.0, 0.001, 0.25])
+
+
+# ----------------------------------------------------- row-parallel split --
+# sglang digest, "风险与影响": tensor parallelism splits the rotated input
+# dimension over ranks, each slice a whole number of groups.
+
+def pin_given_max_rows(quantize_rows_given):
+    for case in load_given_max_rows():
+        Q, s, v, _ = quantize_rows_given(np.array([case["row"]]), np.array(case["amax"]))
+        if not (np.array_equal(Q[0].astype(np.int64), np.array(case["q"], dtype=np.int64))
+                and float(s[0]) == case["s"][0]):
+            return False
+    return True
+
+
+def sharded_linear(X, Qw, sw, bias, G, shards, combine_max=True):
+    """The row-parallel evaluation of the layer, step by step: every slice is
+    rotated alone, the row maxima are combined by max (the all-reduce), every
+    slice is quantized with them, the int32 partial products are summed (the
+    all-reduce) and the output is reconstructed once."""
+    K = X.shape[1]
+    w = K // shards
+    sl = [slice(i * w, (i + 1) * w) for i in range(shards)]
+    rot = [O.rotate_rows(X[:, c], G, "h4") for c in sl]
+    maxima = [O.row_absmax(r) for r in rot]
+    parts = []
+    for r, c, m in zip(rot, sl, maxima):
+        amax = np.maximum.reduce(maxima) if combine_max else m
+        Q, sx, _, _ = O.quantize_rows_given(r, amax)
+        parts.append((Q, sx, O.int_gemm(Q, Qw[:, c])))
+    A = sum(p[2] for p in parts)
+    return np.concatenate([p[0] for p in parts], axis=1), parts[0][1], A, O.reconstruct(A, parts[0][1], sw, bias)
+
+
+def test_row_absmax_and_given_max_hand_rows():
+    assert len(load_given_max_rows()) == 3
+    assert pin_given_max_rows(O.quantize_rows_given)
+    assert np.array_equal(O.row_absmax(np.array([[1.0, -3.0, 2.0], [0.0, 0.0, 0.0]])), [3.0, 0.0])
+
+
+def test_given_max_of_the_row_itself_is_the_plain_quantizer():
+    rng = np.random.default_rng(21)
+    X = rng.standard_t(3, size=(50, 256)) * np.where(rng.random(256) < 0.01, 50.0, 1.0)
+    X[3] = 0.0
+    a, b = O.quantize_rows_given(X, O.row_absmax(X)), O.quantize_rows(X)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("shards,G", [(2, 256), (4, 64), (3, 16)])
+def test_row_parallel_split_reproduces_the_whole_row(shards, G):
+    """Whole groups per slice: rotating a slice alone gives that slice of the
+    whole row's rotation (R is block-diagonal), so with the combined maximum
+    the codes, the scales, the int32 accumulators and Y are exactly those of
+    the layer on the whole row."""
+    rng = np.random.default_rng(shards * G)
+    K = 1536
+    X = rng.standard_t(3, size=(20, K)) * np.where(rng.random(K) < 0.01, 50.0, 1.0)
+    W = rng.normal(0, 0.02, size=(40, K))
+    b = rng.normal(0, 0.01, size=40)
+    Qw, sw, _ = O.prepare_weights(W, G, "h4")
+    whole = O.linear(X, Qw, sw, b, G, "h4")
+    Q, sx, A, Y = sharded_linear(X, Qw, sw, b, G, shards)
+    assert np.array_equal(Q, whole["Qx"]) and np.array_equal(sx, whole["sx"])
+    assert np.array_equal(A, whole["A"]) and np.array_equal(Y, whole["Y64"])
+    w = K // shards
+    assert np.array_equal(O.rotate_rows(X[:, w:2 * w], G, "h4"), O.rotate_rows(X, G, "h4")[:, w:2 * w])
+
+
+def test_row_parallel_slice_must_hold_whole_groups():
+    # a slice of 384 values cuts a group of 256 (the constraint the digest names)
+    with pytest.raises(ValueError):
+        O.rotate_rows(np.zeros((2, 384)), 256, "h4")
+
+
+def test_planted_slice_local_maximum_is_caught():
+    # quantizing every slice with its own maximum (no all-reduce) changes the
+    # codes and the output: the whole-row comparison rejects it
+    rng = np.random.default_rng(5)
+    X = rng.standard_t(3, size=(20, 512))
+    X[:, 7] *= 50.0  # one large channel in the first slice only
+    W = rng.normal(0, 0.02, size=(16, 512))
+    Qw, sw, _ = O.prepare_weights(W, 256, "h4")
+    whole = O.linear(X, Qw, sw, None, 256, "h4")
+    Q, _, A, _ = sharded_linear(X, Qw, sw, None, 256, 2, combine_max=False)
+    assert not np.array_equal(Q, whole["Qx"]) and not np.array_equal(A, whole["A"])
+    wrong = lambda Xr, amax: O.quantize_rows(Xr)  # ignores the given maximum
+    assert not pin_given_max_rows(wrong)
 
 
 # ----------------------------------------------------- planted mistakes --
