@@ -168,6 +168,51 @@ convrot_status convrot_quantize_act_kernel(const void* X, int64_t M, int64_t K, 
                                            int8_t* Qx, float* sx, uint16_t* Qx_f16, int32_t kernel,
                                            cudaStream_t stream);
 
+/* ---- Row-parallel (K-sharded) linear --------------------------------------
+ * The sglang digest ("风险与影响") notes that tensor parallelism with row-
+ * parallel linears splits the rotated input dimension, and requires each
+ * rank's slice (input_size_per_partition) to be a whole number of groups. A
+ * rank then holds X[:, K_r] and Q_w[:, K_r]. The row scale of
+ * "Runtime activation quantization" is a maximum over the WHOLE row, and
+ * A = sum_i Q_x Q_w is a sum over all of K, so the linear needs two
+ * exchanges: an all-reduce (max) of every row's maximum, and an all-reduce
+ * (sum) of the int32 partial accumulators, which is exact. These three calls
+ * are the per-rank steps around those exchanges; the exchanges themselves are
+ * the caller's (NCCL, or any other all-reduce). With the slices of one row
+ * and weights prepared on the whole K (then sliced by columns):
+ *   1. convrot_rotate_absmax on X[:, K_r]            -> amax_r [M]
+ *   2. all-reduce max over ranks                     -> amax   [M]
+ *   3. convrot_quantize_act_given_max(X[:, K_r], amax) -> Q_x,r and s_x
+ *   4. convrot_gemm_s32(Q_x,r, Q_w[:, K_r])          -> A_r int32 [M, N]
+ *   5. all-reduce sum over ranks                     -> A
+ *   6. convrot_dequant(A, s_x, s_w, b)               -> Y bf16
+ * gives codes, scales, A and Y bit-identical to the one-device path on the
+ * whole row (the row maximum and the int32 sums are exact, and every value
+ * is computed from the same operations).
+ * Regular Hadamard only (the tensor-core kernel): each slice's K a multiple
+ * of 256 (1024 for G = 1024); X 16-byte aligned, ldx a multiple of 8, Qx and
+ * Qx_f16 32-byte aligned. UNSUPPORTED_GROUP for other transforms or slice
+ * widths.
+ *
+ * convrot_rotate_absmax: amax[r] = max_i |X_rot[r, i]| over the given columns
+ *   (the normalized rotation), fp32 [M] on the device.
+ * convrot_quantize_act_given_max: as convrot_quantize_act, with the row
+ *   maxima read from amax (fp32 [M], normalized as above) instead of taken
+ *   over the given columns: s_x = amax / 127, Q_x = round(X_rot / s_x).
+ * convrot_dequant: Y[r, o] = bf16(fma(float(A[r, o]), s_x[r] * s_w[o], b[o]))
+ *   for int32 A [M, N] (row stride lda, a multiple of 4, 16-byte aligned),
+ *   the same expression and rounding as the GEMM epilogues. bias may be NULL;
+ *   Y bf16 [M, N], ldy a multiple of 8, 16-byte aligned. */
+convrot_status convrot_rotate_absmax(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                    int32_t transform, float* amax, cudaStream_t stream);
+convrot_status convrot_quantize_act_given_max(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                              int32_t group, int32_t transform, const float* amax,
+                                              int8_t* Qx, float* sx, uint16_t* Qx_f16,
+                                              cudaStream_t stream);
+convrot_status convrot_dequant(const int32_t* A, int64_t M, int64_t N, int64_t lda, const float* sx,
+                               const float* sw, const float* bias, uint16_t* Y, int64_t ldy,
+                               cudaStream_t stream);
+
 /* The H-as-a-matrix variant of convrot_quantize_act: each group is multiplied
  * by the dense G x G rotation on the tensor cores ("feat: load ConvRot int4
  * and per-channel int8 safetensors", section "The rotation": the rotation

@@ -26,7 +26,8 @@ import torch
 __all__ = [
     "ConvRotError", "PackedAct", "PackedWeight", "ConvRotLinear", "TRANSFORMS",
     "convrot_prepare_weights", "convrot_quantize_act", "convrot_quantize_act_hmatmul",
-    "convrot_quantize_act_kernel", "RQ_KERNELS",
+    "convrot_quantize_act_kernel", "RQ_KERNELS", "convrot_rotate_absmax", "convrot_quantize_act_given_max",
+    "convrot_dequant",
     "convrot_linear", "convrot_linear_multi", "convrot_linear_multi_static", "convrot_gemm_s32", "gemm_workspace",
     "GEMM_WORKSPACE_BYTES", "convrot_get_device_status", "convrot_selftest_wait_timeout", "lib", "lib_path",
     "PackedAct4", "PackedWeight4", "convrot_prepare_weights4", "convrot_quantize_act4", "convrot_linear4",
@@ -92,6 +93,9 @@ _SIGS = {
     "convrot_quantize_act": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
     "convrot_quantize_act_hmatmul": [_P, _I64, _I64, _I64, _I32, _P, _P, _P, _P],
     "convrot_quantize_act_kernel": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P],
+    "convrot_rotate_absmax": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P],
+    "convrot_quantize_act_given_max": [_P, _I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P],
+    "convrot_dequant": [_P, _I64, _I64, _I64, _P, _P, _P, _P, _I64, _P],
     "convrot_linear": [ctypes.POINTER(_Act), ctypes.POINTER(_Weight), _P, _P, _I64, _P],
     "convrot_linear_multi": [ctypes.POINTER(_Act), _I32, ctypes.POINTER(_Weight), ctypes.POINTER(_P),
                              ctypes.POINTER(_P), ctypes.POINTER(_I64), _P],
@@ -252,6 +256,54 @@ def convrot_quantize_act_kernel(X: torch.Tensor, group: int, transform="h4", sig
     _check(lib.convrot_quantize_act_kernel(X.data_ptr(), M, K, X.stride(0), group, t, _ptr(signs),
                                            out.q.data_ptr(), out.scale.data_ptr(), _ptr(out.q_f16),
                                            RQ_KERNELS[kernel], _stream(stream)))
+    return out
+
+
+def convrot_rotate_absmax(X: torch.Tensor, group: int, transform="h4", out: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """Row-parallel step 1: amax[r] = max |X_rot[r, :]| over X's columns (a
+    slice of whole groups of a longer row), fp32 [M]."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2 or X.stride(1) != 1:
+        raise TypeError("X must be a 2-D bf16 tensor with unit column stride")
+    M, K = X.shape
+    if out is None:
+        out = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(lib.convrot_rotate_absmax(X.data_ptr(), M, K, X.stride(0), group, _transform_id(transform),
+                                     out.data_ptr(), _stream(stream)))
+    return out
+
+
+def convrot_quantize_act_given_max(X: torch.Tensor, amax: torch.Tensor, group: int, transform="h4",
+                                   with_f16: bool = True, out: Optional[PackedAct] = None,
+                                   stream=None) -> PackedAct:
+    """Row-parallel step 3: quantize X's columns with the whole row's maxima
+    (amax fp32 [M], the all-reduced step-1 values)."""
+    if X.dtype != torch.bfloat16 or X.dim() != 2 or X.stride(1) != 1:
+        raise TypeError("X must be a 2-D bf16 tensor with unit column stride")
+    M, K = X.shape
+    t = _transform_id(transform)
+    if out is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        s = torch.empty((M,), dtype=torch.float32, device=X.device)
+        q16 = torch.empty((M, K), dtype=torch.float16, device=X.device) if with_f16 else None
+        out = PackedAct(q, s, q16, group, t)
+    _check(lib.convrot_quantize_act_given_max(X.data_ptr(), M, K, X.stride(0), group, t, amax.data_ptr(),
+                                              out.q.data_ptr(), out.scale.data_ptr(), _ptr(out.q_f16),
+                                              _stream(stream)))
+    return out
+
+
+def convrot_dequant(A: torch.Tensor, sx: torch.Tensor, sw: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y = A * s_x * s_w + b (bf16) from int32 accumulators (row-parallel
+    step 6, after the all-reduce of the partial A)."""
+    if A.dtype != torch.int32 or A.dim() != 2:
+        raise TypeError("A must be a 2-D int32 tensor")
+    M, N = A.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib.convrot_dequant(A.data_ptr(), M, N, A.stride(0), sx.data_ptr(), sw.data_ptr(), _ptr(bias),
+                               out.data_ptr(), out.stride(0), _stream(stream)))
     return out
 
 

@@ -34,6 +34,11 @@ bool gemm_small_tc_supported(long long M, int K);
 int status_word_gemm_small_tc();
 cudaError_t selftest_wait_launch(long long spin_limit, cudaStream_t st);
 cudaError_t rq_sched_reset();
+cudaError_t rotquant_sharded_launch(const void* X, long long M, int K, long long ldx, int G, bool give_max,
+                                    float* amax, int8_t* Q, float* S, uint16_t* Q16, cudaStream_t st,
+                                    bool* launched);
+cudaError_t dequant_launch(const int32_t* A, long long M, int N, long long lda, const float* sx, const float* sw,
+                           const float* bias, uint16_t* Y, long long ldy, cudaStream_t st);
 
 CONVROT_DEFINE_STATUS_WORD(status_word_api)
 
@@ -332,6 +337,65 @@ convrot_status convrot_quantize_act_kernel(const void* X, int64_t M, int64_t K, 
   if (path < 0)
     return fail(CONVROT_ERR_INVALID_ARG, "kernel %d does not take this shape (transform %d, G=%d, K=%lld, alignment)",
                 kernel, transform, group, static_cast<long long>(K));
+  return ok();
+}
+
+convrot_status convrot_rotate_absmax(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                    int32_t transform, float* amax, cudaStream_t stream) {
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (transform != CONVROT_T_REGULAR_H4)
+    return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "the row-parallel steps take the regular Hadamard only");
+  if (M == 0) return ok();
+  if (!X || !amax) return fail(CONVROT_ERR_INVALID_ARG, "X and amax must be non-null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (!aligned(X, 16) || ldx % 8 || !aligned(amax, 4))
+    return fail(CONVROT_ERR_ALIGNMENT, "X must be 16-byte aligned, ldx a multiple of 8, amax 4-byte aligned");
+  bool launched = false;
+  cudaError_t e = rotquant_sharded_launch(X, M, static_cast<int>(K), ldx, group, false, amax, nullptr, nullptr,
+                                          nullptr, stream, &launched);
+  if (e != cudaSuccess) return cuda_fail(e, "row-max launch");
+  if (!launched)
+    return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "the row-parallel steps need K a multiple of 256 (1024 for G=1024)");
+  return ok();
+}
+
+convrot_status convrot_quantize_act_given_max(const void* X, int64_t M, int64_t K, int64_t ldx, int32_t group,
+                                              int32_t transform, const float* amax, int8_t* Qx, float* sx,
+                                              uint16_t* Qx_f16, cudaStream_t stream) {
+  if (M < 0) return fail(CONVROT_ERR_INVALID_ARG, "M=%lld < 0", static_cast<long long>(M));
+  convrot_status s = check_shape(K, group, transform);
+  if (s != CONVROT_OK) return s;
+  if (transform != CONVROT_T_REGULAR_H4)
+    return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "the row-parallel steps take the regular Hadamard only");
+  if (M == 0) return ok();
+  if (!X || !amax || !Qx || !sx) return fail(CONVROT_ERR_INVALID_ARG, "X, amax, Qx and sx must be non-null");
+  if (ldx < K) return fail(CONVROT_ERR_INVALID_ARG, "ldx=%lld < K=%lld", static_cast<long long>(ldx), static_cast<long long>(K));
+  if (!aligned(X, 16) || ldx % 8 || !aligned(amax, 4) || !aligned(Qx, 32) || !aligned(sx, 4) ||
+      (Qx_f16 && !aligned(Qx_f16, 32)))
+    return fail(CONVROT_ERR_ALIGNMENT, "X must be 16-byte aligned, Qx and Qx_f16 32-byte aligned, ldx a multiple of 8");
+  bool launched = false;
+  cudaError_t e = rotquant_sharded_launch(X, M, static_cast<int>(K), ldx, group, true, const_cast<float*>(amax), Qx,
+                                          sx, Qx_f16, stream, &launched);
+  if (e != cudaSuccess) return cuda_fail(e, "given-max rotate/quantize launch");
+  if (!launched)
+    return fail(CONVROT_ERR_UNSUPPORTED_GROUP, "the row-parallel steps need K a multiple of 256 (1024 for G=1024)");
+  return ok();
+}
+
+convrot_status convrot_dequant(const int32_t* A, int64_t M, int64_t N, int64_t lda, const float* sx,
+                               const float* sw, const float* bias, uint16_t* Y, int64_t ldy, cudaStream_t stream) {
+  if (M < 0 || N < 1 || N > 0x7fffffffLL)
+    return fail(CONVROT_ERR_INVALID_ARG, "M=%lld, N=%lld", static_cast<long long>(M), static_cast<long long>(N));
+  if (M == 0) return ok();
+  if (!A || !sx || !sw || !Y) return fail(CONVROT_ERR_INVALID_ARG, "A, sx, sw and Y must be non-null");
+  if (lda < N || ldy < N) return fail(CONVROT_ERR_INVALID_ARG, "lda and ldy must be >= N");
+  if (!aligned(A, 16) || lda % 4 || !aligned(Y, 16) || ldy % 8 || !aligned(sx, 4) || !aligned(sw, 4) ||
+      (bias && !aligned(bias, 4)))
+    return fail(CONVROT_ERR_ALIGNMENT, "A and Y must be 16-byte aligned, lda a multiple of 4 and ldy of 8");
+  cudaError_t e = dequant_launch(A, M, static_cast<int>(N), lda, sx, sw, bias, Y, ldy, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
   return ok();
 }
 

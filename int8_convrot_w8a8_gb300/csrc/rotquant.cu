@@ -710,12 +710,23 @@ constexpr int kMmaMinWarps = 6;
 constexpr int kRqSchedSlots = 256;
 static __device__ unsigned int g_rq_sched[kRqSchedSlots][2];
 
+// What a launch computes. kRqFull: codes and scales (the row maximum taken
+// over the given columns). kRqAbsmax: only the row maxima of the rotated
+// slice, max_i |X_rot[r, i]|, into amax. kRqGivenMax: codes and scales with
+// the row maxima read from amax (taken over a whole row whose columns are
+// split over several calls, as in a row-parallel linear).
+constexpr int kRqFull = 0, kRqAbsmax = 1, kRqGivenMax = 2;
+
 // WQ / WH: the int8 codes / the fp16 copy are written.
-template <int G, int STAGES, bool WQ, bool WH>
+template <int G, int STAGES, bool WQ, bool WH, int MODE>
 __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     const __grid_constant__ CUtensorMap xmap, long long M, int K, int R, int nsb, int8_t* __restrict__ Q,
-    float* __restrict__ S, __half* __restrict__ Q16, float s_div, int stage_bytes, int box_lines, int slot,
-    long long spin_limit) {
+    float* __restrict__ S, __half* __restrict__ Q16, float* __restrict__ amax, float s_div, int stage_bytes,
+    int box_lines, int slot, long long spin_limit) {
+  static_assert(MODE != kRqAbsmax || (!WQ && !WH), "the row-max mode writes no codes");
+  // the normalization 2^-n of R_G is a power of two: scaling a maximum by it
+  // (or back) is exact
+  constexpr float kNorm = 1.0f / static_cast<float>(1 << ilog4_c(G));
   static_assert(G == 4 || G == 16 || G == 64 || G == 256 || G == 1024, "regular Hadamard group");
   asm volatile("griddepcontrol.launch_dependents;");  // see rq_lane_kernel
   extern __shared__ unsigned char smem_raw[];
@@ -883,14 +894,14 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
         }
     }
 
-    // ---- row absmax
-    float m = 0.0f;
+    // ---- row absmax (taken here, or read below in the given-max mode)
+    if constexpr (MODE != kRqGivenMax) {
+      float m = 0.0f;
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      m = fmax3(m, fabsf(v[s][0].x), fabsf(v[s][0].y));
-      m = fmax3(m, fabsf(v[s][1].x), fabsf(v[s][1].y));
-    }
-    {
+      for (int s = 0; s < 16; ++s) {
+        m = fmax3(m, fabsf(v[s][0].x), fabsf(v[s][0].y));
+        m = fmax3(m, fabsf(v[s][1].x), fabsf(v[s][1].y));
+      }
       const unsigned grp = __match_any_sync(0xffffffffu, my_row);
       const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
       if (sb_valid && lane == __ffs(grp) - 1) atomicMax(&rowmax[my_row], mx);
@@ -910,9 +921,15 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
 
     // ---- quantize into the staging buffers (4-byte code words, 8-byte fp16
     // pieces; both conflict-free), then one bulk copy per output
-    if (sb_valid) {
-      const float amax = __uint_as_float(rowmax[my_row]);
-      const float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+    if (sb_valid && (WQ || WH)) {
+      float amax_u;  // the row maximum of the unnormalized rotation
+      if constexpr (MODE == kRqGivenMax) {
+        const long long grow = tile * R + my_row;
+        amax_u = grow < M ? amax[grow] / kNorm : 0.0f;
+      } else {
+        amax_u = __uint_as_float(rowmax[my_row]);
+      }
+      const float inv = amax_u > 0.0f ? 127.0f / amax_u : 0.0f;
       const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
@@ -933,6 +950,11 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
         }
       }
     }
+    if constexpr (MODE == kRqAbsmax) {
+      for (int i = tid; i < R; i += blockDim.x)
+        if (tile * R + i < M) amax[tile * R + i] = __uint_as_float(rowmax[i]) * kNorm;
+      continue;
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // staging writes -> the bulk copy
     __syncthreads();
     if (tid == 0) {
@@ -949,7 +971,8 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
     for (int i = tid; i < R; i += blockDim.x)
-      if (tile * R + i < M) S[tile * R + i] = __uint_as_float(rowmax[i]) / s_div;
+      if (tile * R + i < M)
+        S[tile * R + i] = (MODE == kRqGivenMax ? amax[tile * R + i] / kNorm : __uint_as_float(rowmax[i])) / s_div;
   }
   if (tid == 0) {
     // the last bulk stores complete before the CTA (and its shared memory) ends
@@ -1093,14 +1116,14 @@ static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
   return true;
 }
 
-template <int G, int STAGES, bool WQ, bool WH>
+template <int G, int STAGES, bool WQ, bool WH, int MODE>
 static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int R, int nsb, int box_lines, int8_t* Q,
-                                float* S, __half* Q16, cudaStream_t st, bool* launched) {
+                                float* S, __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   const int threads = 32 * ((nsb + 7) / 8);
   const int stage_bytes = (R * K * 2 + 1023) / 1024 * 1024;
   const int out_bytes = (WQ ? R * K : 0) + (WH ? 2 * R * K : 0);
   const int smem = 1024 + STAGES * stage_bytes + out_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 16;
-  auto kern = rq_mma_kernel<G, STAGES, WQ, WH>;
+  auto kern = rq_mma_kernel<G, STAGES, WQ, WH, MODE>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -1113,7 +1136,7 @@ static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int 
   const long long grid = (tiles + rounds - 1) / rounds;
   static std::atomic<unsigned int> launches{0};
   const int slot = static_cast<int>(launches.fetch_add(1u, std::memory_order_relaxed) % kRqSchedSlots);
-  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, nsb, Q, S, Q16,
+  kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, nsb, Q, S, Q16, amax,
                                                            scale_divisor(CONVROT_T_REGULAR_H4, G, 127), stage_bytes,
                                                            box_lines, slot, kDefaultSpinLimit);
   *launched = true;
@@ -1138,9 +1161,9 @@ static bool make_x_map(const __nv_bfloat16* X, long long M, int K, long long ldx
 // The tensor-core kernel: regular Hadamard, int8 codes (and fp16 copy), K a
 // multiple of 256 (1024 for G = 1024). *launched stays false for shapes it
 // does not take.
-template <int G>
+template <int G, int MODE>
 static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
-                              __half* Q16, cudaStream_t st, bool* launched) {
+                              __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   *launched = false;
   if (K % 256 != 0 || (G == 1024 && K % 1024 != 0) || M > 0x7fffffffLL) return cudaSuccess;
   int R = 0, nsb = 0;
@@ -1153,17 +1176,32 @@ static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long l
   if (!make_x_map(X, M, K, ldx, R, box_lines, &map)) return cudaSuccess;
   // stages: up to three tiles in flight behind the one being worked on,
   // within about 72 KB of staging per CTA
-  const int tile = R * K * 2;
-  if (Q && Q16) {
-    if (tile <= 24 * 1024) return launch_mma_s<G, 3, true, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
-    return launch_mma_s<G, 2, true, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+  const bool three = R * K * 2 <= 24 * 1024;
+#define CONVROT_RQ_MMA(WQ, WH)                                                                                  \
+  return three ? launch_mma_s<G, 3, WQ, WH, MODE>(map, M, K, R, nsb, box_lines, Q, S, Q16, amax, st, launched) \
+               : launch_mma_s<G, 2, WQ, WH, MODE>(map, M, K, R, nsb, box_lines, Q, S, Q16, amax, st, launched)
+  if constexpr (MODE == kRqAbsmax) {
+    CONVROT_RQ_MMA(false, false);
+  } else {
+    if (Q && Q16) CONVROT_RQ_MMA(true, true);
+    if (Q16) CONVROT_RQ_MMA(false, true);
+    CONVROT_RQ_MMA(true, false);
   }
-  if (Q16) {
-    if (tile <= 24 * 1024) return launch_mma_s<G, 3, false, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
-    return launch_mma_s<G, 2, false, true>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
+#undef CONVROT_RQ_MMA
+}
+
+template <int MODE>
+static cudaError_t launch_mma_any(const __nv_bfloat16* X, long long M, int K, long long ldx, int G, int8_t* Q,
+                                  float* S, __half* Q16, float* amax, cudaStream_t st, bool* launched) {
+  *launched = false;
+  switch (G) {
+    case 4: return launch_mma<4, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 16: return launch_mma<16, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 64: return launch_mma<64, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 256: return launch_mma<256, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 1024: return launch_mma<1024, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    default: return cudaSuccess;
   }
-  if (tile <= 24 * 1024) return launch_mma_s<G, 3, true, false>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
-  return launch_mma_s<G, 2, true, false>(map, M, K, R, nsb, box_lines, Q, S, Q16, st, launched);
 }
 
 // The randomized Hadamard's strides 64 and 128 go through the quad
@@ -1233,15 +1271,7 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
   if (fast_ok && qm == 127 && transform == CONVROT_T_REGULAR_H4 && (kernel == kRqAuto || kernel == kRqMma)) {
     bool launched = false;
-    cudaError_t e = cudaSuccess;
-    switch (G) {
-      case 4: e = launch_mma<4>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 16: e = launch_mma<16>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 64: e = launch_mma<64>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 256: e = launch_mma<256>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      case 1024: e = launch_mma<1024>(xb, M, K, ldx, Q, S, q16, st, &launched); break;
-      default: break;
-    }
+    cudaError_t e = launch_mma_any<kRqFull>(xb, M, K, ldx, G, Q, S, q16, nullptr, st, &launched);
     if (e != cudaSuccess) return e;
     if (launched) {
       *path = 2;
@@ -1284,6 +1314,24 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
                                                              signs, Q, S, q16, sdiv, qm);
   }
   return cudaGetLastError();
+}
+
+// Row-parallel building blocks (regular Hadamard on the tensor-core kernel):
+// give_max = false writes the row maxima of the rotated slice into amax;
+// give_max = true quantizes with the row maxima read from amax. *launched
+// is false for shapes the kernel does not take.
+cudaError_t rotquant_sharded_launch(const void* X, long long M, int K, long long ldx, int G, bool give_max,
+                                    float* amax, int8_t* Q, float* S, uint16_t* Q16, cudaStream_t st,
+                                    bool* launched) {
+  *launched = false;
+  if (M <= 0) return cudaSuccess;
+  if (reinterpret_cast<uintptr_t>(X) % 16 != 0 || ldx % 8 != 0 || reinterpret_cast<uintptr_t>(Q) % 32 != 0 ||
+      reinterpret_cast<uintptr_t>(Q16) % 32 != 0)
+    return cudaSuccess;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
+  __half* q16 = reinterpret_cast<__half*>(Q16);
+  if (give_max) return launch_mma_any<kRqGivenMax>(xb, M, K, ldx, G, Q, S, q16, amax, st, launched);
+  return launch_mma_any<kRqAbsmax>(xb, M, K, ldx, G, nullptr, nullptr, nullptr, amax, st, launched);
 }
 
 }  // namespace convrot
