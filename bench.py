@@ -127,7 +127,7 @@ def rq_kernel_name(wl) -> str:
     lines = wl.K // 64
     parts = (lines + 255) // 256
     boxes = wl.K % 64 == 0 and lines % parts == 0 and (parts == 1 or (lines // parts) % 8 == 0)
-    if (boxes and getattr(wl, "bits", 8) == 8 and wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)
+    if (boxes and wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)
             and wl.K % max(256, wl.group) == 0):
         return "rq_mma_kernel"
     lane = (boxes and K_LANE_MAX >= wl.K and
@@ -452,6 +452,7 @@ def secondary_figures(cr, args, name, dev, flush_l2) -> dict:
     step_s = timed(lambda: cr.convrot_int8_linear(X, ws, bs, signs=sg, outs=outs, scratch=scratch, workspace=gws))
     gemm_s = timed(lambda: cr.convrot_linear_multi(act, ws, bs, outs=outs, workspace=gws))
     q_s = timed(lambda: cr.convrot_quantize_act(X, wl.group, wl.transform, sg, with_f16=False, out=act8))
+    floor = read_floor(dev, (3 * wl.M * wl.K + 4 * wl.M) // 2, flush_l2, args.steps, args.warmup)
     if cr.convrot_get_device_status() != 0:
         raise RuntimeError(f"device status after the {name} figures")
     pk = peaks()
@@ -463,7 +464,8 @@ def secondary_figures(cr, args, name, dev, flush_l2) -> dict:
             "gemm_us": gemm_s * 1e6, "gemm_tflops": gemm_tflops,
             "gemm_frac": gemm_tflops / pk["bf16_tflops"] if use_f16 else None,
             "rotate_quant": {"kernel": rq_kernel_name(wl), "us": q_s * 1e6, "algorithmic_bytes": q_bytes,
-                             "gbs": q_bytes / q_s / 1e9, "frac": q_bytes / q_s / 1e9 / pk["hbm_gbs"]}}
+                             "gbs": q_bytes / q_s / 1e9, "frac": q_bytes / q_s / 1e9 / pk["hbm_gbs"],
+                             "copy_floor_us": floor["copy_us"], "frac_of_copy_floor": floor["copy_us"] / (q_s * 1e6)}}
 
 
 def gpu_main(args, world, rank, local):
@@ -621,6 +623,9 @@ def gpu_main(args, world, rank, local):
     q_bytes_f16 = q_bytes + (2 if bits == 8 else 1) * M * K if use_f16 else q_bytes
     quant_only_s = statistics.mean(q_only_ms) / 1e3
     quant_gbs = q_bytes / quant_only_s / 1e9
+    # the floor for moving the contract's bytes once in this protocol: a plain
+    # torch copy of half of them (it reads and writes each byte once)
+    q_floor = read_floor(dev, q_bytes // 2, flush_l2, args.steps, args.warmup)
     if bits == 4:
         # e4m3 dense rate: the measured bf16 burst x the nominal fp8 / bf16 ratio (4.5 / 2.25)
         peak8 = 2.0 * pk["bf16_tflops"]
@@ -726,7 +731,12 @@ def gpu_main(args, world, rank, local):
                                   if bits == 4 else
                                   "int8 codes + scales only; in the step the kernel also writes the fp16 operand copy"),
                          "in_step_us": quant_s * 1e6, "in_step_bytes": q_bytes_f16,
-                         "in_step_gbs": q_bytes_f16 / quant_s / 1e9},
+                         "in_step_gbs": q_bytes_f16 / quant_s / 1e9,
+                         "copy_floor_us": q_floor["copy_us"],
+                         "frac_of_copy_floor": q_floor["copy_us"] / (quant_only_s * 1e6),
+                         "copy_floor_note": "a torch copy reading and writing the contract's algorithmic bytes "
+                                            "once, same flush and pause (event-timed launches carry a fixed "
+                                            "cost of a few microseconds on this GPU)"},
         "rotate_quant_hmatmul": None if hm_ms is None else {
             "kernel": "hmatmul_kernel", "us": statistics.mean(hm_ms) * 1e3,
             "gbs": q_bytes / (statistics.mean(hm_ms) / 1e3) / 1e9,

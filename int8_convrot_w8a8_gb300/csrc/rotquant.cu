@@ -717,8 +717,13 @@ static __device__ unsigned int g_rq_sched[kRqSchedSlots][2];
 // split over several calls, as in a row-parallel linear).
 constexpr int kRqFull = 0, kRqAbsmax = 1, kRqGivenMax = 2;
 
-// WQ / WH: the int8 codes / the fp16 copy are written.
-template <int G, int STAGES, bool WQ, bool WH, int MODE>
+// QM = 127: WQ / WH write the int8 codes / their fp16 copy. QM = 7 (4-bit
+// codes in [-7, 7]): WQ writes the packed nibbles (element 2j in the low
+// nibble of byte j), WH their e4m3 copy.
+// NB: staging buffers for the outputs. With two, a tile's bulk store is
+// issued after the next tile's row-max barrier, so a tile costs one CTA-wide
+// barrier instead of two.
+template <int G, int STAGES, bool WQ, bool WH, int MODE, int QM, int NB>
 __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     const __grid_constant__ CUtensorMap xmap, long long M, int K, int R, int nsb, int8_t* __restrict__ Q,
     float* __restrict__ S, __half* __restrict__ Q16, float* __restrict__ amax, float s_div, int stage_bytes,
@@ -733,14 +738,19 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_base = smem_u32(smem);
-  // output staging: the tile's fp16 copy [R, K] and int8 codes [R, K] (each
-  // present when asked for; both start on a 512-byte boundary), written out
-  // by one bulk copy per tile
+  // output staging: the tile's tensor-core copy [R, K] (fp16, or e4m3 for
+  // 4-bit codes) and its codes [R, K] (int8, or nibbles [R, K / 2]); each
+  // present when asked for, each starting on a 128-byte boundary, each
+  // written out by one bulk copy per tile
+  constexpr uint32_t kHB2 = QM == 127 ? 4 : 2;  // bytes per element of the copy, x2
+  constexpr uint32_t kQB2 = QM == 127 ? 2 : 1;  // bytes per element of the codes, x2
   const uint32_t tile_elems = static_cast<uint32_t>(R) * static_cast<uint32_t>(K);
+  const uint32_t h_bytes = WH ? kHB2 * tile_elems / 2 : 0u, q_bytes = WQ ? kQB2 * tile_elems / 2 : 0u;
+  const uint32_t buf_bytes = (h_bytes + q_bytes + 1023u) & ~1023u;  // one staging buffer, 1 KB aligned
   const uint32_t out_h = stage_base + STAGES * stage_bytes;
-  const uint32_t out_q = out_h + (WH ? 2u * tile_elems : 0u);
-  unsigned int* rowmax_buf = reinterpret_cast<unsigned int*>(
-      smem + STAGES * stage_bytes + (WQ ? tile_elems : 0u) + (WH ? 2u * tile_elems : 0u));  // [3][R]
+  const uint32_t out_q = out_h + h_bytes;
+  unsigned int* rowmax_buf =
+      reinterpret_cast<unsigned int*>(smem + STAGES * stage_bytes + NB * buf_bytes);  // [3][R]
   uint64_t* full = reinterpret_cast<uint64_t*>(rowmax_buf + ((3 * R + 1) & ~1));            // [STAGES]
   long long* stage_tile = reinterpret_cast<long long*>(full + STAGES);                      // [STAGES]
 
@@ -750,6 +760,54 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   const int sb_per_row = K >> 8;
   const uint32_t tile_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(K) * 2u;
 
+  // Tiles: the first STAGES rounds go out round-robin (tile blockIdx.x +
+  // k * gridDim.x for the k-th stage filled), the rest by claims on the
+  // counter, numbered from STAGES * gridDim.x. Only tid 0 claims, one claim
+  // ahead (the atomic's round trip overlaps a whole tile). Tiles come out in
+  // increasing order for each CTA, so once one lies past the end every later
+  // one does too, and a CTA leaves with no copy in flight.
+  unsigned int* claims = &g_rq_sched[slot][0];
+  const long long dyn_base = static_cast<long long>(STAGES) * gridDim.x;
+  unsigned int pending = 0;  // tid 0: the claim for the next refill
+  bool exhausted = false;    // tid 0: a claim came back past the end
+  auto fill = [&](int s, long long c) {  // tid 0: start stage s on tile c (or mark it empty)
+    if (c < ntiles) {
+      stage_tile[s] = c;
+      mbar_expect_tx(&full[s], tile_bytes);
+      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
+        tma_load_3d(stage_base + s * stage_bytes + l0 * 128, &xmap, 0, l0, static_cast<int>(c * R), &full[s]);
+    } else {
+      exhausted = true;
+      stage_tile[s] = -1;
+      mbar_arrive(&full[s]);
+    }
+  };
+  // (tid 0) bulk-stores tile tl's codes from staging buffer b
+  auto store_tile = [&](long long tl, int b) {
+    const long long rows = M - tl * R < R ? M - tl * R : R;
+    const long long e0 = tl * R * static_cast<long long>(K);
+    const uint32_t n = static_cast<uint32_t>(rows * K);
+    const uint32_t off = static_cast<uint32_t>(b) * buf_bytes;
+    if constexpr (WQ)
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       reinterpret_cast<unsigned char*>(Q) + e0 * kQB2 / 2),
+                   "r"(out_q + off), "r"(kQB2 * n / 2)
+                   : "memory");
+    if constexpr (WH)
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       reinterpret_cast<unsigned char*>(Q16) + e0 * kHB2 / 2),
+                   "r"(out_h + off), "r"(kHB2 * n / 2)
+                   : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  };
+  // the first tile's copy starts before anything else, alone: the first
+  // tiles of all CTAs then reach the SMs ahead of the deeper stages
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fill(0, blockIdx.x);
+  }
+
   // ---- result side: this thread's superblock and positions
   const int g = lane >> 2, t = lane & 3;
   const int sb = warp * 8 + g;
@@ -757,10 +815,10 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   const int my_row = sb_valid ? sb / sb_per_row : -1;            // row within the tile
   // staging address of positions 4t .. 4t + 3 of chunk g of this superblock
   // (the superblocks of a tile are consecutive in the dense output); chunk
-  // s ^ g is then at that address XOR 16 s (32 s for fp16), since the chunk
+  // s ^ g is then at that address XOR (chunk bytes) * s, since the chunk
   // offset bits of the superblock's base are zero
-  const uint32_t my_q = (out_q + static_cast<uint32_t>(sb) * 256u + 4u * t) | (16u * g);
-  const uint32_t my_h = (out_h + static_cast<uint32_t>(sb) * 512u + 8u * t) | (32u * g);
+  const uint32_t my_q = (out_q + static_cast<uint32_t>(sb) * 128u * kQB2 + 2u * kQB2 * t) | (8u * kQB2 * g);
+  const uint32_t my_h = (out_h + static_cast<uint32_t>(sb) * 128u * kHB2 + 2u * kHB2 * t) | (8u * kHB2 * g);
 
   // ---- operand side: the rows this lane addresses for ldmatrix.x4
   // (matrix m = lane / 8: h = m & 1 picks row g + 8h, hf = m >> 1 the 8-value
@@ -788,39 +846,17 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     bfrag[nb][1] = bf16x2_bits(h16_entry(G, p, 2 * t + 8), h16_entry(G, p, 2 * t + 9));
   }
 
-  // Tiles: the first STAGES rounds go out round-robin (tile blockIdx.x +
-  // k * gridDim.x for the k-th stage filled), the rest by claims on the
-  // counter, numbered from STAGES * gridDim.x. Only tid 0 claims, one claim
-  // ahead (the atomic's round trip overlaps a whole tile). Tiles come out in
-  // increasing order for each CTA, so once one lies past the end every later
-  // one does too, and a CTA leaves with no copy in flight.
-  unsigned int* claims = &g_rq_sched[slot][0];
-  const long long dyn_base = static_cast<long long>(STAGES) * gridDim.x;
-  unsigned int pending = 0;  // tid 0: the claim for the next refill
-  bool exhausted = false;    // tid 0: a claim came back past the end
-  auto fill = [&](int s, long long c) {  // tid 0: start stage s on tile c (or mark it empty)
-    if (c < ntiles) {
-      stage_tile[s] = c;
-      mbar_expect_tx(&full[s], tile_bytes);
-      for (int l0 = 0; l0 < lines_per_row; l0 += box_lines)
-        tma_load_3d(stage_base + s * stage_bytes + l0 * 128, &xmap, 0, l0, static_cast<int>(c * R), &full[s]);
-    } else {
-      exhausted = true;
-      stage_tile[s] = -1;
-      mbar_arrive(&full[s]);
-    }
-  };
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the first STAGES tiles are in flight during the set-up below
-    for (int s = 0; s < STAGES; ++s) fill(s, blockIdx.x + static_cast<long long>(s) * gridDim.x);
-    if (!exhausted) pending = atomicAdd(claims, 1u);
-  }
   for (int i = tid; i < 3 * R; i += blockDim.x) rowmax_buf[i] = 0u;
   __syncthreads();
+  // the deeper stages of the first round-robin rounds, then the first claim
+  if (tid == 0) {
+    for (int s = 1; s < STAGES; ++s) fill(s, blockIdx.x + static_cast<long long>(s) * gridDim.x);
+    if (!exhausted) pending = atomicAdd(claims, 1u);
+  }
 
   const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+  long long prev_tile = -1;  // NB = 2: the tile whose codes wait in the other staging buffer
+  int prev_it = 0;           //        and the iteration that wrote them
   for (int it = 0;; ++it) {
     const int st = it % STAGES;
     unsigned int* rowmax = rowmax_buf + (it % 3) * R;
@@ -906,7 +942,7 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
       const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
       if (sb_valid && lane == __ffs(grp) - 1) atomicMax(&rowmax[my_row], mx);
     }
-    // the previous tile's bulk store has finished reading the staging buffers
+    // the bulk store that last read this tile's staging buffer is done with it
     if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     __syncthreads();
     // every warp has read stage st (and its tile index): refill it
@@ -917,7 +953,10 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
         fill(st, dyn_base + pending);
         if (!exhausted) pending = atomicAdd(claims, 1u);
       }
+      // NB = 2: the previous tile's codes are complete (the barrier above)
+      if (NB == 2 && prev_tile >= 0) store_tile(prev_tile, (it - 1) & 1);
     }
+    const uint32_t bsel = NB == 2 ? static_cast<uint32_t>(it & 1) * buf_bytes : 0u;
 
     // ---- quantize into the staging buffers (4-byte code words, 8-byte fp16
     // pieces; both conflict-free), then one bulk copy per output
@@ -929,22 +968,37 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
       } else {
         amax_u = __uint_as_float(rowmax[my_row]);
       }
-      const float inv = amax_u > 0.0f ? 127.0f / amax_u : 0.0f;
+      const float inv = amax_u > 0.0f ? static_cast<float>(QM) / amax_u : 0.0f;
       const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
         const float2 t0 = f2_fma(v[s][0], inv2, mg2);  // positions 4t, 4t + 1
         const float2 t1 = f2_fma(v[s][1], inv2, mg2);  // positions 4t + 2, 4t + 3
+        if constexpr (QM == 7) {
+          if constexpr (WQ) {  // four two's-complement nibbles, the first in the low bits
+            const uint32_t n = (__float_as_uint(t0.x) & 0xFu) | ((__float_as_uint(t0.y) & 0xFu) << 4) |
+                               ((__float_as_uint(t1.x) & 0xFu) << 8) | ((__float_as_uint(t1.y) & 0xFu) << 12);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"((my_q ^ (8u * s)) + bsel), "h"(static_cast<unsigned short>(n))
+                         : "memory");
+          }
+          if constexpr (WH) {
+            const float2 c0 = f2_sub(t0, mg2), c1 = f2_sub(t1, mg2);
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"((my_h ^ (16u * s)) + bsel),
+                         "r"(e4m3x2(c0.x, c0.y) | (e4m3x2(c1.x, c1.y) << 16))
+                         : "memory");
+          }
+          continue;
+        }
         if constexpr (WQ) {
           const uint32_t b01 = __byte_perm(__float_as_uint(t0.x), __float_as_uint(t0.y), 0x0040);
           const uint32_t b23 = __byte_perm(__float_as_uint(t1.x), __float_as_uint(t1.y), 0x0040);
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"(my_q ^ (16u * s)), "r"(__byte_perm(b01, b23, 0x5410))
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"((my_q ^ (16u * s)) + bsel), "r"(__byte_perm(b01, b23, 0x5410))
                        : "memory");
         }
         if constexpr (WH) {
           const float2 c0 = f2_sub(t0, mg2), c1 = f2_sub(t1, mg2);
           const __half2 h0 = __floats2half2_rn(c0.x, c0.y), h1 = __floats2half2_rn(c1.x, c1.y);
-          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(my_h ^ (32u * s)),
+          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"((my_h ^ (32u * s)) + bsel),
                        "r"(*reinterpret_cast<const uint32_t*>(&h0)), "r"(*reinterpret_cast<const uint32_t*>(&h1))
                        : "memory");
         }
@@ -956,23 +1010,20 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
       continue;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // staging writes -> the bulk copy
-    __syncthreads();
-    if (tid == 0) {
-      const long long rows = M - tile * R < R ? M - tile * R : R;
-      const long long e0 = tile * R * static_cast<long long>(K);
-      const uint32_t n = static_cast<uint32_t>(rows * K);
-      if constexpr (WQ)
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Q + e0), "r"(out_q), "r"(n)
-                     : "memory");
-      if constexpr (WH)
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(Q16 + e0), "r"(out_h),
-                     "r"(2u * n)
-                     : "memory");
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    if constexpr (NB == 1) {
+      __syncthreads();
+      if (tid == 0) store_tile(tile, 0);
     }
     for (int i = tid; i < R; i += blockDim.x)
       if (tile * R + i < M)
         S[tile * R + i] = (MODE == kRqGivenMax ? amax[tile * R + i] / kNorm : __uint_as_float(rowmax[i])) / s_div;
+    prev_tile = tile;
+    prev_it = it;
+  }
+  if constexpr (NB == 2 && MODE != kRqAbsmax) {
+    // the last tile's codes: every warp has written and fenced them
+    __syncthreads();
+    if (tid == 0 && prev_tile >= 0) store_tile(prev_tile, prev_it & 1);
   }
   if (tid == 0) {
     // the last bulk stores complete before the CTA (and its shared memory) ends
@@ -1116,14 +1167,15 @@ static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
   return true;
 }
 
-template <int G, int STAGES, bool WQ, bool WH, int MODE>
+template <int G, int STAGES, bool WQ, bool WH, int MODE, int QM, int NB>
 static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int R, int nsb, int box_lines, int8_t* Q,
                                 float* S, __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   const int threads = 32 * ((nsb + 7) / 8);
   const int stage_bytes = (R * K * 2 + 1023) / 1024 * 1024;
-  const int out_bytes = (WQ ? R * K : 0) + (WH ? 2 * R * K : 0);
-  const int smem = 1024 + STAGES * stage_bytes + out_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 16;
-  auto kern = rq_mma_kernel<G, STAGES, WQ, WH, MODE>;
+  const int out_bytes = QM == 127 ? (WQ ? R * K : 0) + (WH ? 2 * R * K : 0) : (WQ ? R * K / 2 : 0) + (WH ? R * K : 0);
+  const int buf_bytes = (out_bytes + 1023) / 1024 * 1024;
+  const int smem = 1024 + STAGES * stage_bytes + NB * buf_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 16;
+  auto kern = rq_mma_kernel<G, STAGES, WQ, WH, MODE, QM, NB>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -1137,7 +1189,7 @@ static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int 
   static std::atomic<unsigned int> launches{0};
   const int slot = static_cast<int>(launches.fetch_add(1u, std::memory_order_relaxed) % kRqSchedSlots);
   kern<<<static_cast<unsigned>(grid), threads, smem, st>>>(map, M, K, R, nsb, Q, S, Q16, amax,
-                                                           scale_divisor(CONVROT_T_REGULAR_H4, G, 127), stage_bytes,
+                                                           scale_divisor(CONVROT_T_REGULAR_H4, G, QM), stage_bytes,
                                                            box_lines, slot, kDefaultSpinLimit);
   *launched = true;
   return cudaGetLastError();
@@ -1161,7 +1213,7 @@ static bool make_x_map(const __nv_bfloat16* X, long long M, int K, long long ldx
 // The tensor-core kernel: regular Hadamard, int8 codes (and fp16 copy), K a
 // multiple of 256 (1024 for G = 1024). *launched stays false for shapes it
 // does not take.
-template <int G, int MODE>
+template <int G, int MODE, int QM>
 static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
                               __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   *launched = false;
@@ -1175,11 +1227,14 @@ static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long l
   CUtensorMap map;
   if (!make_x_map(X, M, K, ldx, R, box_lines, &map)) return cudaSuccess;
   // stages: up to three tiles in flight behind the one being worked on,
-  // within about 72 KB of staging per CTA
+  // within about 72 KB of input staging per CTA; two output staging buffers
+  // when the codes alone are written (the fp16 copy's would cost a CTA per SM)
   const bool three = R * K * 2 <= 24 * 1024;
-#define CONVROT_RQ_MMA(WQ, WH)                                                                                  \
-  return three ? launch_mma_s<G, 3, WQ, WH, MODE>(map, M, K, R, nsb, box_lines, Q, S, Q16, amax, st, launched) \
-               : launch_mma_s<G, 2, WQ, WH, MODE>(map, M, K, R, nsb, box_lines, Q, S, Q16, amax, st, launched)
+#define CONVROT_RQ_MMA(WQ, WH)                                                                                       \
+  return three ? launch_mma_s<G, 3, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1>(map, M, K, R, nsb, box_lines, Q, S, Q16,   \
+                                                                           amax, st, launched)                      \
+               : launch_mma_s<G, 2, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1>(map, M, K, R, nsb, box_lines, Q, S, Q16,   \
+                                                                           amax, st, launched)
   if constexpr (MODE == kRqAbsmax) {
     CONVROT_RQ_MMA(false, false);
   } else {
@@ -1190,16 +1245,16 @@ static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long l
 #undef CONVROT_RQ_MMA
 }
 
-template <int MODE>
+template <int MODE, int QM = 127>
 static cudaError_t launch_mma_any(const __nv_bfloat16* X, long long M, int K, long long ldx, int G, int8_t* Q,
                                   float* S, __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   *launched = false;
   switch (G) {
-    case 4: return launch_mma<4, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
-    case 16: return launch_mma<16, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
-    case 64: return launch_mma<64, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
-    case 256: return launch_mma<256, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
-    case 1024: return launch_mma<1024, MODE>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 4: return launch_mma<4, MODE, QM>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 16: return launch_mma<16, MODE, QM>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 64: return launch_mma<64, MODE, QM>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 256: return launch_mma<256, MODE, QM>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
+    case 1024: return launch_mma<1024, MODE, QM>(X, M, K, ldx, Q, S, Q16, amax, st, launched);
     default: return cudaSuccess;
   }
 }
@@ -1269,9 +1324,10 @@ cudaError_t rotquant_launch(const void* X, int in_dtype, long long M, int K, lon
                          (Q16 == nullptr || reinterpret_cast<uintptr_t>(Q16) % 32 == 0);
   const bool fast_ok = in_dtype == CONVROT_DTYPE_BF16 && aligned32 && K % 16 == 0;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(X);
-  if (fast_ok && qm == 127 && transform == CONVROT_T_REGULAR_H4 && (kernel == kRqAuto || kernel == kRqMma)) {
+  if (fast_ok && transform == CONVROT_T_REGULAR_H4 && (kernel == kRqAuto || kernel == kRqMma)) {
     bool launched = false;
-    cudaError_t e = launch_mma_any<kRqFull>(xb, M, K, ldx, G, Q, S, q16, nullptr, st, &launched);
+    cudaError_t e = qm == 7 ? launch_mma_any<kRqFull, 7>(xb, M, K, ldx, G, Q, S, q16, nullptr, st, &launched)
+                            : launch_mma_any<kRqFull, 127>(xb, M, K, ldx, G, Q, S, q16, nullptr, st, &launched);
     if (e != cudaSuccess) return e;
     if (launched) {
       *path = 2;

@@ -57,7 +57,17 @@ def test_quantize_act4_matches_oracle_on_both_kernels(cr, M, K, G, transform):
     check_scales(to_np(fast.scale), s, f"w4 {transform} G{G}")
     assert np.abs(q_fast).max() <= 7
     assert np.array_equal(f_fast, q_fast.astype(np.int64))
-    assert torch.equal(fast.q4, gen.q4) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f8, gen.q_f8)
+    q_gen, f_gen = _codes4(gen)
+    check_codes(q_gen, Q, v, f"w4 generic {transform} G{G}")
+    assert np.array_equal(f_gen, q_gen.astype(np.int64))
+    if transform == "h4" and K % max(256, G) == 0:
+        # the tensor-core kernel: its 16-point stage sums in the tensor core's
+        # order, so a code may differ by one from the generic kernel's where
+        # the value lies within a few fp32 ulps of a rounding boundary
+        d = np.abs(q_fast.astype(np.int64) - q_gen)
+        assert d.max() <= 1 and (d > 0).sum() <= max(1, int(1e-4 * d.size))
+    else:
+        assert torch.equal(fast.q4, gen.q4) and torch.equal(fast.scale, gen.scale) and torch.equal(fast.q_f8, gen.q_f8)
 
 
 def test_prepare_weights4_matches_oracle(cr):
