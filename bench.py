@@ -64,15 +64,15 @@ PRE_STEP_SLEEP_CYCLES = 300_000
 # capture time: once the code has changed the figure no longer applies and
 # the line reports null.
 NCU_TRAFFIC = {
-    ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
-        "bytes": 245_465_600 + 44_179_712,
+    ("gemm_tc_kernel", "qkv_32700x3072x(3x3072)_G256"): {
+        "bytes": 713_397_248 + 580_912_640,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "7ca86947208241132365343ee29c1b082cfc07d12b165f765ac1fd988c01121d",
+        "sha256": "1c738c7f3fbe0c2433a726f36243b7ef20830bea7f6e2f58aa230976108e1218",
     },
-    ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256_W4A4"): {
-        "bytes": 64_004_864 + 24_824_064,
+    ("gemm_tc_kernel", "dit_linear_4096x6144x6144_G256"): {
+        "bytes": 247_918_848 + 44_043_520,
         "source": "int8_convrot_w8a8_gb300/csrc/gemm_tc.cu",
-        "sha256": "7ca86947208241132365343ee29c1b082cfc07d12b165f765ac1fd988c01121d",
+        "sha256": "1c738c7f3fbe0c2433a726f36243b7ef20830bea7f6e2f58aa230976108e1218",
     },
 }
 
