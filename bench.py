@@ -533,9 +533,13 @@ def gpu_main(args, world, rank, local):
     assert cr.convrot_get_device_status() == 0
     if args.profile:
         # a short, fixed launch list for ncu: one more step, then one int8-only
-        # rotate+quantize and (where supported) one matmul-form rotate+quantize
+        # rotate+quantize, the same on the register butterfly kernel where the
+        # library runs the tensor-core one, and (where supported) one
+        # matmul-form rotate+quantize
         step()
         quant(X, False)
+        if bits == 8 and rq_kernel_name(wl) == "rq_mma_kernel":
+            cr.convrot_quantize_act_kernel(X, wl.group, wl.transform, sg, kernel="butterfly", with_f16=False)
         if bits == 8 and wl.transform == "h4" and wl.group in (16, 64, 256) and K % max(wl.group, 64) == 0 \
                 and K // max(wl.group, 64) <= 128:
             cr.convrot_quantize_act_hmatmul(X, wl.group, with_f16=False)
