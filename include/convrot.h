@@ -132,7 +132,9 @@ convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N
  * device, zero when the library is loaded; each completed launch puts its
  * slot back to zero; convrot_get_device_status() clears them all after a
  * timeout). Launches take the slots in turn, so at most 256 rotate+quantize
- * launches may be in flight on one device at the same time.
+ * launches may be in flight on one device at the same time. A launch recorded
+ * into a CUDA graph keeps the slot it was given: replays of one graph must
+ * not overlap each other in time.
  * M == 0 is a no-op. */
 convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t ldx,
                                     int32_t group, int32_t transform, const int8_t* signs,
