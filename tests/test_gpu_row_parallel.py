@@ -30,6 +30,7 @@ def _slice_weight(cr, w, cols):
                                            (77, 4096, 136, 1024, 2), (40, 3072, 264, 64, 3)])
 def test_row_parallel_steps_match_the_whole_row(cr, M, K, N, G, ranks):
     wl = WL.make_case(M, K, [N], group=G, seed=M + K + ranks, name="row_parallel")
+    wl.X[3] = 0.0      # a zero row: every rank's maximum is 0, so scale 0 and codes 0
     X = wl.X.cuda()
     w = cr.convrot_prepare_weights(wl.weights[0].cuda(), G, "h4")  # offline, on the whole K
     b = wl.biases[0].cuda()
@@ -51,6 +52,7 @@ def test_row_parallel_steps_match_the_whole_row(cr, M, K, N, G, ranks):
     assert torch.equal(torch.cat([a.q_f16 for a in acts], dim=1), full.q_f16)
     for a in acts:
         assert torch.equal(a.scale, full.scale)
+        assert float(a.scale[3]) == 0.0 and not bool(a.q[3].any())
     assert torch.equal(A, A_full)
     assert torch.equal(Y, Y_full)
     # and against the oracle
