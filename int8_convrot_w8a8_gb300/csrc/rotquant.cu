@@ -1139,11 +1139,9 @@ static cudaError_t launch_lane_x(const __nv_bfloat16* X, long long M, int K, lon
 }
 
 // Tiles of the tensor-core kernel: R rows whose superblocks fill whole warps
-// (or nearly), at least kMmaMinWarps warps where the shape allows, at most
-// kMmaMaxWarps warps and 48 KB per tile. Larger CTAs pay the two barriers of
-// a tile over more work (GB300: 6 warps of 24 KB tiles beat 2-3 warps of 8-12
-// KB tiles by 5-10 % on the DiT, qkv and group-sweep activations).
-static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
+// (or nearly), at least min_warps warps where the shape allows, at most
+// kMmaMaxWarps warps and 48 KB per tile.
+static bool choose_rows_mma(int K, int min_warps, int* R_out, int* nsb_out) {
   const int sbpr = K / 256;
   int bestR = -1;
   double best = -1.0;
@@ -1152,7 +1150,7 @@ static bool choose_rows_mma(int K, int* R_out, int* nsb_out) {
     const int warps = (nsb + 7) / 8;
     if (warps > kMmaMaxWarps || static_cast<long long>(R) * K * 2 > 48 * 1024) break;
     const double eff = static_cast<double>(nsb) / (8.0 * warps);
-    if (warps >= kMmaMinWarps && eff >= 0.999) {
+    if (warps >= min_warps && eff >= 0.999) {
       bestR = R;
       break;
     }
@@ -1218,18 +1216,27 @@ static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long l
                               __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   *launched = false;
   if (K % 256 != 0 || (G == 1024 && K % 1024 != 0) || M > 0x7fffffffLL) return cudaSuccess;
+  // Tile shape by what the launch writes (GB300, one GPU, the DiT, qkv and
+  // group-sweep activations). With the fp16 copy (or the e4m3 one) the
+  // staging is large: 6-warp tiles of about 24 KB with 3 stages, 2 CTAs per
+  // SM. With the codes alone (two small staging buffers) or nothing but the
+  // row maxima: 3-warp tiles of about 12 KB with 2 stages, 4-5 CTAs per SM,
+  // which took the qkv activation from 47.4 to 45.4 us.
+  const bool light = MODE == kRqAbsmax || (Q && !Q16);
   int R = 0, nsb = 0;
-  if (!choose_rows_mma(K, &R, &nsb)) return cudaSuccess;
+  if (!choose_rows_mma(K, light ? 3 : kMmaMinWarps, &R, &nsb)) return cudaSuccess;
   const int lines = K / 64;
   const int parts = (lines + 255) / 256;
   const int box_lines = lines / parts;
   if (parts > 1 && (R != 1 || lines % parts != 0 || box_lines % 8 != 0)) return cudaSuccess;
   CUtensorMap map;
   if (!make_x_map(X, M, K, ldx, R, box_lines, &map)) return cudaSuccess;
-  // stages: up to three tiles in flight behind the one being worked on,
-  // within about 72 KB of input staging per CTA; two output staging buffers
-  // when the codes alone are written (the fp16 copy's would cost a CTA per SM)
-  const bool three = R * K * 2 <= 24 * 1024;
+  // stages: three (two tiles in flight behind the one being worked on) for
+  // the large tiles, within about 72 KB of input staging per CTA; two for the
+  // light launches, whose CTAs are smaller and more per SM. Two output
+  // staging buffers when the codes alone are written (the fp16 copy's would
+  // cost a CTA per SM).
+  const bool three = !light && R * K * 2 <= 24 * 1024;
 #define CONVROT_RQ_MMA(WQ, WH)                                                                                       \
   return three ? launch_mma_s<G, 3, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1>(map, M, K, R, nsb, box_lines, Q, S, Q16,   \
                                                                            amax, st, launched)                      \
