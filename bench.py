@@ -41,6 +41,7 @@ import subprocess
 import sys
 import threading
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -868,6 +869,7 @@ def block_main(args, world, rank, local):
         K = x.shape[1]
         ops = 2.0 * M * K * sum(ww.N for ww in w)
         per.append({"layer": name, "K": K, "N": [ww.N for ww in w], "call_us": call_s * 1e6,
+                    "rotate_quant_kernel": rq_kernel_name(types.SimpleNamespace(K=K, transform=T, group=G)),
                     "gemm_us": gemm_s * 1e6, "gemm_tflops": ops / gemm_s / 1e12,
                     "rotate_quant_us": quant_s * 1e6,
                     "rotate_quant_gbs": (5.0 * M * K + 4 * M) / quant_s / 1e9, "ops": ops})
@@ -913,7 +915,8 @@ def block_main(args, world, rank, local):
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / pk["bf16_tflops"],
                      "traffic": None,
                      "peak_note": f"{pk['source']} bf16 dense burst; the four GEMMs' flops over their summed times"},
-        "rotate_quant": {"kernel": "rq_lane_kernel", "us": q_s * 1e6, "gbs": q_bytes / q_s / 1e9,
+        "rotate_quant": {"kernel": "+".join(sorted({p_["rotate_quant_kernel"] for p_ in per})),
+                         "us": q_s * 1e6, "gbs": q_bytes / q_s / 1e9,
                          "peak_gbs": pk["hbm_gbs"], "frac": q_bytes / q_s / 1e9 / pk["hbm_gbs"],
                          "algorithmic_bytes": q_bytes,
                          "note": "the four rotate+quantize launches with their fp16 operand copies (5 bytes per element)"},
