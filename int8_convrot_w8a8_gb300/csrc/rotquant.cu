@@ -816,9 +816,28 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   // staging address of positions 4t .. 4t + 3 of chunk g of this superblock
   // (the superblocks of a tile are consecutive in the dense output); chunk
   // s ^ g is then at that address XOR (chunk bytes) * s, since the chunk
-  // offset bits of the superblock's base are zero
-  const uint32_t my_q = (out_q + static_cast<uint32_t>(sb) * 128u * kQB2 + 2u * kQB2 * t) | (8u * kQB2 * g);
-  const uint32_t my_h = (out_h + static_cast<uint32_t>(sb) * 128u * kHB2 + 2u * kHB2 * t) | (8u * kHB2 * g);
+  // offset bits of the superblock's base are zero.
+  // G = 1024: after the digit-4 exchange below, slot s of the lane with
+  // j = g & 3 holds chunk ((s & 12) ^ 4 (g >> 2)) | j of superblock
+  // 4 (g >> 2) + (j ^ (s & 3)) of the warp's group; its offset from the
+  // tile's staging base is my_q XOR a constant of s (the group's base is a
+  // multiple of the group's bytes, so the fields do not carry).
+  const int g2 = g >> 2, jq = g & 3;
+  const uint32_t my_q =
+      G == 1024 ? 128u * kQB2 * static_cast<uint32_t>(warp * 8 + 4 * g2 + jq) + 8u * kQB2 * (4 * g2 + jq) + 2u * kQB2 * t
+                : (out_q + static_cast<uint32_t>(sb) * 128u * kQB2 + 2u * kQB2 * t) | (8u * kQB2 * g);
+  const uint32_t my_h =
+      G == 1024 ? 128u * kHB2 * static_cast<uint32_t>(warp * 8 + 4 * g2 + jq) + 8u * kHB2 * (4 * g2 + jq) + 2u * kHB2 * t
+                : (out_h + static_cast<uint32_t>(sb) * 128u * kHB2 + 2u * kHB2 * t) | (8u * kHB2 * g);
+  // staging address of slot s (buffer offset bsel added by the caller)
+  auto q_at = [&](int s) -> uint32_t {
+    if constexpr (G == 1024) return out_q + (my_q ^ (128u * kQB2 * (s & 3) + 8u * kQB2 * (s & 12)));
+    return my_q ^ (8u * kQB2 * s);
+  };
+  auto h_at = [&](int s) -> uint32_t {
+    if constexpr (G == 1024) return out_h + (my_h ^ (128u * kHB2 * (s & 3) + 8u * kHB2 * (s & 12)));
+    return my_h ^ (8u * kHB2 * s);
+  };
 
   // ---- operand side: the rows this lane addresses for ldmatrix.x4
   // (matrix m = lane / 8: h = m & 1 picks row g + 8h, hf = m >> 1 the 8-value
@@ -897,37 +916,27 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
 #pragma unroll
         for (int b = 0; b < 4; ++b) h4_stage(v[b][q], v[b + 4][q], v[b + 8][q], v[b + 12][q]);
     }
-    // ---- digit 4 (G = 1024): the four superblocks of a group sit in groups
-    // g ^ {0, 1, 2, 3} (lanes ^ 4, ^ 8); partner g ^ c keeps my chunk in its
-    // slot s ^ c. u = x + x[a^1], w = x - x[a^1], y = u + w[a^2].
+    // ---- digit 4 (G = 1024): the four superblocks of a group sit in the
+    // lanes with g ^ {0, 1, 2, 3} (lane ^ 4c). A 4-lane transpose first: slot
+    // s with s & 3 = c comes from lane ^ 4c, so afterwards slot 4h + c holds
+    // superblock j ^ c (j = g & 3) of the one chunk ((4h) ^ 4 (g >> 2)) | j.
+    // The radix-4 stage depends only on the XOR of its two digits, so it runs
+    // on those four slots as they are, and each result stays in its slot.
     if constexpr (G == 1024) {
-      float2 w[16][2];
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
+      for (int c = 1; c < 4; ++c)
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float2 p;
-          p.x = __shfl_xor_sync(0xffffffffu, v[s ^ 1][q].x, 4);
-          p.y = __shfl_xor_sync(0xffffffffu, v[s ^ 1][q].y, 4);
-          w[s][q] = p;
-        }
+        for (int h = 0; h < 4; ++h)
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
+          for (int q = 0; q < 2; ++q) {
+            float2& x = v[4 * h + c][q];
+            x.x = __shfl_xor_sync(0xffffffffu, x.x, 4 * c);
+            x.y = __shfl_xor_sync(0xffffffffu, x.y, 4 * c);
+          }
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float2 p = w[s][q];
-          w[s][q] = f2_sub(v[s][q], p);
-          v[s][q] = f2_add(v[s][q], p);
-        }
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float2 p;
-          p.x = __shfl_xor_sync(0xffffffffu, w[s ^ 2][q].x, 8);
-          p.y = __shfl_xor_sync(0xffffffffu, w[s ^ 2][q].y, 8);
-          v[s][q] = f2_add(v[s][q], p);
-        }
+        for (int h = 0; h < 4; ++h) h4_stage(v[4 * h][q], v[4 * h + 1][q], v[4 * h + 2][q], v[4 * h + 3][q]);
     }
 
     // ---- row absmax (taken here, or read below in the given-max mode)
@@ -978,12 +987,12 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
           if constexpr (WQ) {  // four two's-complement nibbles, the first in the low bits
             const uint32_t n = (__float_as_uint(t0.x) & 0xFu) | ((__float_as_uint(t0.y) & 0xFu) << 4) |
                                ((__float_as_uint(t1.x) & 0xFu) << 8) | ((__float_as_uint(t1.y) & 0xFu) << 12);
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"((my_q ^ (8u * s)) + bsel), "h"(static_cast<unsigned short>(n))
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(q_at(s) + bsel), "h"(static_cast<unsigned short>(n))
                          : "memory");
           }
           if constexpr (WH) {
             const float2 c0 = f2_sub(t0, mg2), c1 = f2_sub(t1, mg2);
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"((my_h ^ (16u * s)) + bsel),
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(h_at(s) + bsel),
                          "r"(e4m3x2(c0.x, c0.y) | (e4m3x2(c1.x, c1.y) << 16))
                          : "memory");
           }
@@ -992,13 +1001,13 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
         if constexpr (WQ) {
           const uint32_t b01 = __byte_perm(__float_as_uint(t0.x), __float_as_uint(t0.y), 0x0040);
           const uint32_t b23 = __byte_perm(__float_as_uint(t1.x), __float_as_uint(t1.y), 0x0040);
-          asm volatile("st.shared.b32 [%0], %1;" ::"r"((my_q ^ (16u * s)) + bsel), "r"(__byte_perm(b01, b23, 0x5410))
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(q_at(s) + bsel), "r"(__byte_perm(b01, b23, 0x5410))
                        : "memory");
         }
         if constexpr (WH) {
           const float2 c0 = f2_sub(t0, mg2), c1 = f2_sub(t1, mg2);
           const __half2 h0 = __floats2half2_rn(c0.x, c0.y), h1 = __floats2half2_rn(c1.x, c1.y);
-          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"((my_h ^ (32u * s)) + bsel),
+          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(h_at(s) + bsel),
                        "r"(*reinterpret_cast<const uint32_t*>(&h0)), "r"(*reinterpret_cast<const uint32_t*>(&h1))
                        : "memory");
         }

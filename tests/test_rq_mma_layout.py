@@ -1,8 +1,9 @@
 """The data layout of the tensor-core rotate+quantize kernel, replayed on the
 CPU (no GPU): the TMA stage's 128B swizzle, every lane's ldmatrix row
 addresses, the m16n8k16 fragment layouts, the permuted 16-point matrix, the
-digits above the chunk on XOR-permuted register slots (and the cross-lane
-digit of G = 1024), and the staging offsets of the codes. The replayed
+digits above the chunk on XOR-permuted register slots (and, for G = 1024,
+the 4-lane transpose before the superblock digit), and the staging offsets
+of the codes. The replayed
 rotation must equal the oracle's (unnormalized by sqrt(G)); every output
 position must be written exactly once; the eight rows of every ldmatrix
 phase and the 32 lanes of every int8 staging store must fall in distinct
@@ -93,30 +94,39 @@ def replay(X, G):
                         for i in range(4):
                             v[lane, b + 4 * i, q] = y[i]
         if G == 1024:
-            t1 = np.array([[v[lane ^ 4, s ^ 1] for s in range(16)] for lane in range(32)])
-            u1, w1 = v + t1, v - t1
-            t2 = np.array([[w1[lane ^ 8, s ^ 2] for s in range(16)] for lane in range(32)])
-            v = u1 + t2
-        # int8 staging stores: lane (g, t) writes 4 codes of chunk s ^ g at
-        # (256 sb + 4 t) | 16 g, XOR 16 s
-        for s in range(16):
-            banks = set()
+            # the 4-lane transpose (slot s with s & 3 = c from lane ^ 4c), then
+            # the radix-4 stage on slots 4h .. 4h + 3
+            v = np.array([[v[lane ^ (4 * (s & 3)), s] for s in range(16)] for lane in range(32)])
             for lane in range(32):
-                g, t = lane >> 2, lane & 3
-                sb = w * 8 + g
-                addr = ((256 * sb + 4 * t) | (16 * g)) ^ (16 * s)
-                banks.add((addr // 4) % 32)
+                for q in range(2):
+                    for h in range(4):
+                        y = h4_stage(*[v[lane, 4 * h + i, q] for i in range(4)])
+                        for i in range(4):
+                            v[lane, 4 * h + i, q] = y[i]
+
+        def placed(lane, s):
+            """(int8 staging offset, superblock, chunk) of slot s of the lane."""
+            g, t = lane >> 2, lane & 3
+            if G == 1024:
+                g2, j = g >> 2, g & 3
+                rel = 256 * (w * 8 + 4 * g2 + j) + 16 * (4 * g2 + j) + 4 * t
+                addr = rel ^ (256 * (s & 3) + 16 * (s & 12))
+                return addr, w * 8 + 4 * g2 + (j ^ (s & 3)), ((s & 12) ^ (4 * g2)) | j
+            return ((256 * (w * 8 + g) + 4 * t) | (16 * g)) ^ (16 * s), w * 8 + g, s ^ g
+
+        # int8 staging stores: lane (g, t) writes the 4 codes of slot s
+        for s in range(16):
+            banks = {(placed(lane, s)[0] // 4) % 32 for lane in range(32)}
             bad_stores += full_warp and len(banks) != 32
         for lane in range(32):
             g, t = lane >> 2, lane & 3
-            sb = w * 8 + g
-            if sb >= nsb:
+            if w * 8 + g >= nsb:
                 continue
-            row, col0 = sb // sbpr, (sb % sbpr) * 256 + 4 * t
             for s in range(16):
-                addr = ((256 * sb + 4 * t) | (16 * g)) ^ (16 * s)
-                assert addr == 256 * sb + 16 * (s ^ g) + 4 * t  # the dense output offset
-                e = col0 + 16 * (s ^ g)
+                addr, sb, chunk = placed(lane, s)
+                assert sb < nsb
+                assert addr == 256 * sb + 16 * chunk + 4 * t  # the dense output offset
+                row, e = sb // sbpr, (sb % sbpr) * 256 + 16 * chunk + 4 * t
                 out[row, e:e + 2] = v[lane, s, 0]
                 out[row, e + 2:e + 4] = v[lane, s, 1]
                 written[row, e:e + 4] += 1
@@ -124,7 +134,8 @@ def replay(X, G):
 
 
 @pytest.mark.parametrize("K,G,R", [(3072, 256, 4), (6144, 256, 2), (4096, 1024, 1), (4096, 16, 3),
-                                   (4096, 64, 1), (1024, 4, 12), (5376, 256, 3), (5376, 64, 3), (1024, 1024, 4)])
+                                   (4096, 64, 1), (1024, 4, 12), (5376, 256, 3), (5376, 64, 3), (1024, 1024, 4),
+                                   (3072, 1024, 1), (5120, 1024, 1)])
 def test_replayed_layout_is_the_rotation(K, G, R):
     rng = np.random.default_rng(K + G + R)
     X = rng.standard_normal((R, K)).round(3)  # exactly representable sums in fp64
