@@ -131,6 +131,11 @@ def rq_kernel_name(wl) -> str:
     if (boxes and wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)
             and wl.K % max(256, wl.group) == 0):
         return "rq_mma_kernel"
+    # K a multiple of 64 but not of 256: tiles of 2 or 4 rows, groups within a line
+    r0 = 2 if lines % 2 == 0 else 4
+    if (wl.transform == "h4" and wl.group in (4, 16, 64) and wl.K % 64 == 0 and wl.K >= 256
+            and parts == 1 and r0 * wl.K * 2 <= 48 * 1024):
+        return "rq_mma_kernel"
     lane = (boxes and K_LANE_MAX >= wl.K and
             ((wl.transform == "h4" and wl.group in (4, 16, 64, 256, 1024)) or
              (wl.transform == "rht" and 2 <= wl.group <= 256) or wl.transform == "none"))

@@ -124,9 +124,11 @@ convrot_status convrot_prepare_weights(const void* W, int32_t w_dtype, int64_t N
  *   Qx_f16  device fp16 [M, K] (out) or NULL.
  * X must be 16-byte aligned with ldx a multiple of 8. The fast kernels run
  * when X is 16-byte aligned and Qx, Qx_f16 32-byte aligned: for the regular
- * Hadamard with K a multiple of 256 (1024 for G = 1024) the tensor-core
- * kernel (see convrot_quantize_act_kernel), else the register butterfly,
- * else the generic kernel.
+ * Hadamard with K a multiple of 256 (1024 for G = 1024), or with G <= 64 and
+ * K a multiple of 64 from 256 to 12288 (6144 when K / 64 is odd), the
+ * tensor-core kernel (see
+ * convrot_quantize_act_kernel), else the register butterfly, else the
+ * generic kernel.
  * The tensor-core kernel hands its tiles out through a small counter array
  * of the library (one pair of counters per launch slot, 256 slots per
  * device, zero when the library is loaded; each completed launch puts its
@@ -153,7 +155,10 @@ convrot_status convrot_quantize_act(const void* X, int64_t M, int64_t K, int64_t
  *                           the tensor cores (mma.sync bf16 -> fp32 from the
  *                           staged tile) and the higher digits on fp32
  *                           registers: G in {4, 16, 64, 256, 1024}, K a
- *                           multiple of 256 (1024 for G = 1024). The tensor
+ *                           multiple of 256 (1024 for G = 1024); for G <= 64
+ *                           also K a multiple of 64 from 256 up (tiles of 2
+ *                           or 4 rows of at most 48 KB, so up to 12288 when
+ *                           K / 64 is even, 6144 when odd). The tensor
  *                           core sums its 16 exact products in fp32 in its own
  *                           order, so codes can differ from the butterfly's
  *                           by one where the value lies within a few fp32

@@ -723,12 +723,15 @@ constexpr int kRqFull = 0, kRqAbsmax = 1, kRqGivenMax = 2;
 // NB: staging buffers for the outputs. With two, a tile's bulk store is
 // issued after the next tile's row-max barrier, so a tile costs one CTA-wide
 // barrier instead of two.
-template <int G, int STAGES, bool WQ, bool WH, int MODE, int QM, int NB>
+template <int G, int STAGES, bool WQ, bool WH, int MODE, int QM, int NB, bool RAG>
 __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     const __grid_constant__ CUtensorMap xmap, long long M, int K, int R, int nsb, int8_t* __restrict__ Q,
     float* __restrict__ S, __half* __restrict__ Q16, float* __restrict__ amax, float s_div, int stage_bytes,
     int box_lines, int slot, long long spin_limit) {
   static_assert(MODE != kRqAbsmax || (!WQ && !WH), "the row-max mode writes no codes");
+  // RAG: K a multiple of 64 but not of 256, so a superblock (4 lines) may
+  // end in the next row of the tile; its groups (G <= 64) stay within a line
+  static_assert(!RAG || (G <= 64 && MODE == kRqFull), "superblocks across rows: G <= 64, codes and scales");
   // the normalization 2^-n of R_G is a power of two: scaling a maximum by it
   // (or back) is exact
   constexpr float kNorm = 1.0f / static_cast<float>(1 << ilog4_c(G));
@@ -812,7 +815,21 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
   const int g = lane >> 2, t = lane & 3;
   const int sb = warp * 8 + g;
   const bool sb_valid = sb < nsb;
-  const int my_row = sb_valid ? sb / sb_per_row : -1;            // row within the tile
+  // row within the tile (of the superblock's first line)
+  const int my_row = sb_valid ? (RAG ? 4 * sb / lines_per_row : sb / sb_per_row) : -1;
+  // RAG: the row of the superblock's last line, and bit h set where slots
+  // 4h .. 4h + 3 (line h ^ (g >> 2) of the superblock) lie in that row but
+  // not in my_row
+  int my_row2 = my_row;
+  unsigned in2 = 0u;
+  if constexpr (RAG) {
+    if (sb_valid) {
+      my_row2 = (4 * sb + 3) / lines_per_row;
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        if ((4 * sb + (h ^ (g >> 2))) / lines_per_row != my_row) in2 |= 1u << h;
+    }
+  }
   // staging address of positions 4t .. 4t + 3 of chunk g of this superblock
   // (the superblocks of a tile are consecutive in the dense output); chunk
   // s ^ g is then at that address XOR (chunk bytes) * s, since the chunk
@@ -940,7 +957,28 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
     }
 
     // ---- row absmax (taken here, or read below in the given-max mode)
-    if constexpr (MODE != kRqGivenMax) {
+    if constexpr (RAG) {
+      // the maxima of the two rows, each over the lines that lie in it
+      float m = 0.0f, m2 = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float mh = 0.0f;
+#pragma unroll
+        for (int s = 4 * h; s < 4 * h + 4; ++s) {
+          mh = fmax3(mh, fabsf(v[s][0].x), fabsf(v[s][0].y));
+          mh = fmax3(mh, fabsf(v[s][1].x), fabsf(v[s][1].y));
+        }
+        const bool second = (in2 >> h) & 1u;
+        m = fmaxf(m, second ? 0.0f : mh);
+        m2 = fmaxf(m2, second ? mh : 0.0f);
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, my_row);
+      const unsigned mx = __reduce_max_sync(grp, __float_as_uint(m));
+      if (sb_valid && lane == __ffs(grp) - 1) atomicMax(&rowmax[my_row], mx);
+      const unsigned grp2 = __match_any_sync(0xffffffffu, my_row2);
+      const unsigned mx2 = __reduce_max_sync(grp2, __float_as_uint(m2));
+      if (sb_valid && lane == __ffs(grp2) - 1) atomicMax(&rowmax[my_row2], mx2);
+    } else if constexpr (MODE != kRqGivenMax) {
       float m = 0.0f;
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
@@ -978,9 +1016,15 @@ __global__ void __launch_bounds__(32 * kMmaMaxWarps) rq_mma_kernel(
         amax_u = __uint_as_float(rowmax[my_row]);
       }
       const float inv = amax_u > 0.0f ? static_cast<float>(QM) / amax_u : 0.0f;
-      const float2 inv2 = make_float2(inv, inv);
+      float inv_b = inv;  // RAG: the multiplier of the superblock's second row
+      if constexpr (RAG) {
+        const float amax_b = __uint_as_float(rowmax[my_row2]);
+        inv_b = amax_b > 0.0f ? static_cast<float>(QM) / amax_b : 0.0f;
+      }
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
+        const float inv_s = RAG && ((in2 >> (s >> 2)) & 1u) ? inv_b : inv;
+        const float2 inv2 = make_float2(inv_s, inv_s);
         const float2 t0 = f2_fma(v[s][0], inv2, mg2);  // positions 4t, 4t + 1
         const float2 t1 = f2_fma(v[s][1], inv2, mg2);  // positions 4t + 2, 4t + 3
         if constexpr (QM == 7) {
@@ -1151,11 +1195,14 @@ static cudaError_t launch_lane_x(const __nv_bfloat16* X, long long M, int K, lon
 // (or nearly), at least min_warps warps where the shape allows, at most
 // kMmaMaxWarps warps and 48 KB per tile.
 static bool choose_rows_mma(int K, int min_warps, int* R_out, int* nsb_out) {
-  const int sbpr = K / 256;
+  // R is a multiple of r0, so that a tile is a whole number of superblocks
+  // (4 lines of 64): 1 when K is a multiple of 256, else 2 or 4
+  const int lines = K / 64;
+  const int r0 = lines % 4 == 0 ? 1 : lines % 2 == 0 ? 2 : 4;
   int bestR = -1;
   double best = -1.0;
-  for (int R = 1; R <= 64; ++R) {
-    const int nsb = R * sbpr;
+  for (int R = r0; R <= 64; R += r0) {
+    const int nsb = R * lines / 4;
     const int warps = (nsb + 7) / 8;
     if (warps > kMmaMaxWarps || static_cast<long long>(R) * K * 2 > 48 * 1024) break;
     const double eff = static_cast<double>(nsb) / (8.0 * warps);
@@ -1170,11 +1217,11 @@ static bool choose_rows_mma(int K, int min_warps, int* R_out, int* nsb_out) {
   }
   if (bestR < 0) return false;
   *R_out = bestR;
-  *nsb_out = bestR * sbpr;
+  *nsb_out = bestR * lines / 4;
   return true;
 }
 
-template <int G, int STAGES, bool WQ, bool WH, int MODE, int QM, int NB>
+template <int G, int STAGES, bool WQ, bool WH, int MODE, int QM, int NB, bool RAG>
 static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int R, int nsb, int box_lines, int8_t* Q,
                                 float* S, __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   const int threads = 32 * ((nsb + 7) / 8);
@@ -1182,7 +1229,7 @@ static cudaError_t launch_mma_s(const CUtensorMap& map, long long M, int K, int 
   const int out_bytes = QM == 127 ? (WQ ? R * K : 0) + (WH ? 2 * R * K : 0) : (WQ ? R * K / 2 : 0) + (WH ? R * K : 0);
   const int buf_bytes = (out_bytes + 1023) / 1024 * 1024;
   const int smem = 1024 + STAGES * stage_bytes + NB * buf_bytes + ((3 * R + 1) & ~1) * 4 + STAGES * 16;
-  auto kern = rq_mma_kernel<G, STAGES, WQ, WH, MODE, QM, NB>;
+  auto kern = rq_mma_kernel<G, STAGES, WQ, WH, MODE, QM, NB, RAG>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -1218,13 +1265,16 @@ static bool make_x_map(const __nv_bfloat16* X, long long M, int K, long long ldx
 }
 
 // The tensor-core kernel: regular Hadamard, int8 codes (and fp16 copy), K a
-// multiple of 256 (1024 for G = 1024). *launched stays false for shapes it
-// does not take.
+// multiple of 256 (1024 for G = 1024); for G <= 64 with codes and scales,
+// also K a multiple of 64 from 256 up (a superblock then spans at most two
+// rows of a tile). *launched stays false for shapes it does not take.
 template <int G, int MODE, int QM>
 static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long long ldx, int8_t* Q, float* S,
                               __half* Q16, float* amax, cudaStream_t st, bool* launched) {
   *launched = false;
-  if (K % 256 != 0 || (G == 1024 && K % 1024 != 0) || M > 0x7fffffffLL) return cudaSuccess;
+  if ((G == 1024 && K % 1024 != 0) || M > 0x7fffffffLL) return cudaSuccess;
+  const bool rag = K % 256 != 0;
+  if (rag && !(G <= 64 && MODE == kRqFull && K % 64 == 0 && K >= 256)) return cudaSuccess;
   // Tile shape by what the launch writes (GB300, one GPU, the DiT, qkv and
   // group-sweep activations). With the fp16 copy (or the e4m3 one) the
   // staging is large: 6-warp tiles of about 24 KB with 3 stages, 2 CTAs per
@@ -1246,19 +1296,27 @@ static cudaError_t launch_mma(const __nv_bfloat16* X, long long M, int K, long l
   // staging buffers when the codes alone are written (the fp16 copy's would
   // cost a CTA per SM).
   const bool three = !light && R * K * 2 <= 24 * 1024;
-#define CONVROT_RQ_MMA(WQ, WH)                                                                                       \
-  return three ? launch_mma_s<G, 3, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1>(map, M, K, R, nsb, box_lines, Q, S, Q16,   \
-                                                                           amax, st, launched)                      \
-               : launch_mma_s<G, 2, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1>(map, M, K, R, nsb, box_lines, Q, S, Q16,   \
-                                                                           amax, st, launched)
+#define CONVROT_RQ_MMA_R(WQ, WH, RG)                                                                               \
+  return three ? launch_mma_s<G, 3, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1, RG>(map, M, K, R, nsb, box_lines, Q, S,   \
+                                                                               Q16, amax, st, launched)             \
+               : launch_mma_s<G, 2, WQ, WH, MODE, QM, (WQ && !WH) ? 2 : 1, RG>(map, M, K, R, nsb, box_lines, Q, S,   \
+                                                                               Q16, amax, st, launched)
+#define CONVROT_RQ_MMA(WQ, WH)                      \
+  {                                                 \
+    if constexpr (G <= 64 && MODE == kRqFull) {     \
+      if (rag) CONVROT_RQ_MMA_R(WQ, WH, true);      \
+    }                                               \
+    CONVROT_RQ_MMA_R(WQ, WH, false);                \
+  }
   if constexpr (MODE == kRqAbsmax) {
-    CONVROT_RQ_MMA(false, false);
+    CONVROT_RQ_MMA(false, false)
   } else {
-    if (Q && Q16) CONVROT_RQ_MMA(true, true);
-    if (Q16) CONVROT_RQ_MMA(false, true);
-    CONVROT_RQ_MMA(true, false);
+    if (Q && Q16) CONVROT_RQ_MMA(true, true)
+    if (Q16) CONVROT_RQ_MMA(false, true)
+    CONVROT_RQ_MMA(true, false)
   }
 #undef CONVROT_RQ_MMA
+#undef CONVROT_RQ_MMA_R
 }
 
 template <int MODE, int QM = 127>

@@ -77,3 +77,19 @@ def check_y_e2e(y_gpu, y_or, label=""):
     err = np.abs(y_gpu - y_or).max()
     assert err <= Y_E2E_RTOL * np.abs(y_or).max(), f"{label}: Y error {err:.3g}"
     return err / np.abs(y_or).max()
+
+
+def tensor_core_takes(K, G, transform="h4"):
+    """Whether the library's tensor-core rotate+quantize kernel takes rows of
+    K with this group (it then runs where the caller does not ask for a
+    kernel): the regular Hadamard, K a multiple of 256 (1024 for G = 1024),
+    or for G <= 64 a multiple of 64 from 256 up whose tiles of 2 or 4 rows
+    (a whole number of 4-line superblocks) fit the 48 KB stage."""
+    if transform != "h4" or G not in (4, 16, 64, 256, 1024) or K % 64 != 0:
+        return False
+    lines = K // 64
+    if K % max(256, G) == 0:
+        return lines <= 256 or (lines % ((lines + 255) // 256) == 0 and (lines // ((lines + 255) // 256)) % 8 == 0)
+    r0 = 2 if lines % 2 == 0 else 4
+    return G <= 64 and K >= 256 and lines <= 256 and r0 * K * 2 <= 48 * 1024
+

@@ -84,7 +84,10 @@ def test_misaligned_outputs_take_the_generic_kernel(cr):
 
 @pytest.mark.parametrize("M,K,G", [(37, 6144, 256), (130, 3072, 256), (33, 4096, 16), (33, 4096, 64),
                                    (33, 4096, 1024), (7, 1024, 4), (37, 5376, 256), (37, 5376, 64),
-                                   (3, 21504, 256), (2, 24576, 1024), (1, 256, 16), (300, 1024, 1024)])
+                                   (3, 21504, 256), (2, 24576, 1024), (1, 256, 16), (300, 1024, 1024),
+                                   # K not a multiple of 256: superblocks across rows
+                                   (45, 2688, 64), (41, 2688, 16), (13, 2688, 4), (9, 320, 64), (33, 1088, 64),
+                                   (7, 1088, 16), (300, 2688, 64), (1, 2688, 64), (5, 4032, 64)])
 def test_tensor_core_kernel_matches_oracle(cr, M, K, G):
     """The 16-point stage on the tensor cores (mma.sync bf16 -> fp32 from the
     staged tile), the higher digits on fp32 registers: codes and scales
@@ -134,9 +137,13 @@ def test_tensor_core_kernel_concurrent_launches(cr):
 
 
 def test_tensor_core_kernel_refuses_other_shapes(cr):
-    X = torch.zeros((4, 2688), dtype=torch.bfloat16, device="cuda")   # K not a multiple of 256
-    with pytest.raises(cr.ConvRotError, match="does not take"):
-        cr.convrot_quantize_act_kernel(X, 64, "h4", kernel="tensor_core")
+    for K in (192, 2720):   # fewer than 256 columns; not a multiple of 64
+        X = torch.zeros((4, K), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(cr.ConvRotError, match="does not take"):
+            cr.convrot_quantize_act_kernel(X, 16, "h4", kernel="tensor_core")
+    X = torch.zeros((4, 2688), dtype=torch.bfloat16, device="cuda")   # G = 256 does not divide K
+    with pytest.raises(cr.ConvRotError):
+        cr.convrot_quantize_act_kernel(X, 256, "h4", kernel="tensor_core")
     Y = torch.zeros((4, 1536), dtype=torch.bfloat16, device="cuda")   # G = 1024 needs K % 1024 == 0
     with pytest.raises(cr.ConvRotError):
         cr.convrot_quantize_act_kernel(Y, 1024, "h4", kernel="tensor_core")

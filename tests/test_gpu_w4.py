@@ -8,7 +8,7 @@ import torch
 
 import oracle as O
 import workloads as WL
-from parity import check_codes, check_scales, check_y_e2e, check_y_same_codes, to_np
+from parity import check_codes, check_scales, check_y_e2e, check_y_same_codes, tensor_core_takes, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def _oracle4(X_bf16, G, transform, signs=None):
 @pytest.mark.parametrize("M,K,G,transform", [
     (37, 6144, 256, "h4"), (33, 4096, 16, "h4"), (33, 4096, 64, "h4"), (33, 4096, 1024, "h4"),
     (16, 1152, 128, "rht"), (21, 2048, 128, "rht"), (21, 2048, 256, "rht"), (9, 1152, 0, "none"), (1, 128, 4, "h4"),
-    (300, 3072, 256, "h4"),
+    (300, 3072, 256, "h4"), (45, 2688, 64, "h4"), (13, 2688, 16, "h4"),
 ])
 def test_quantize_act4_matches_oracle_on_both_kernels(cr, M, K, G, transform):
     wl = WL.make_case(M, K, [], dist="t3", outlier_frac=0.002, outlier_scale=40.0, group=max(G, 2),
@@ -60,7 +60,7 @@ def test_quantize_act4_matches_oracle_on_both_kernels(cr, M, K, G, transform):
     q_gen, f_gen = _codes4(gen)
     check_codes(q_gen, Q, v, f"w4 generic {transform} G{G}")
     assert np.array_equal(f_gen, q_gen.astype(np.int64))
-    if transform == "h4" and K % max(256, G) == 0:
+    if tensor_core_takes(K, G, transform):
         # the tensor-core kernel: its 16-point stage sums in the tensor core's
         # order, so a code may differ by one from the generic kernel's where
         # the value lies within a few fp32 ulps of a rounding boundary

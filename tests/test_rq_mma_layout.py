@@ -3,7 +3,9 @@ CPU (no GPU): the TMA stage's 128B swizzle, every lane's ldmatrix row
 addresses, the m16n8k16 fragment layouts, the permuted 16-point matrix, the
 digits above the chunk on XOR-permuted register slots (and, for G = 1024,
 the 4-lane transpose before the superblock digit), and the staging offsets
-of the codes. The replayed
+of the codes, including K not a multiple of 256 (G <= 64), where a
+superblock may end in the next row of the tile and the kernel takes each
+line's scale from the row it lies in. The replayed
 rotation must equal the oracle's (unnormalized by sqrt(G)); every output
 position must be written exactly once; the eight rows of every ldmatrix
 phase and the 32 lanes of every int8 staging store must fall in distinct
@@ -31,8 +33,9 @@ def h4_stage(x0, x1, x2, x3):
 def replay(X, G):
     """The kernel's arithmetic on one tile of R = X.shape[0] rows, in fp64."""
     R, K = X.shape
-    sbpr, lines = K // 256, K // 64
-    nsb = R * sbpr
+    lines = K // 64
+    assert R * lines % 4 == 0  # a tile is a whole number of superblocks
+    nsb = R * lines // 4
     warps = (nsb + 7) // 8
     # the stage as TMA writes it: logical 16-byte chunk c of line L at physical chunk c ^ (L & 7)
     stage = np.zeros((R * lines, 8, 8))
@@ -120,13 +123,20 @@ def replay(X, G):
             bad_stores += full_warp and len(banks) != 32
         for lane in range(32):
             g, t = lane >> 2, lane & 3
-            if w * 8 + g >= nsb:
+            sb0 = w * 8 + g
+            if sb0 >= nsb:
                 continue
+            # the kernel's rows: the superblock's first and last line, and
+            # bit h where slots 4h .. 4h + 3 (line h ^ (g >> 2)) lie in the second
+            row1, row2 = 4 * sb0 // lines, (4 * sb0 + 3) // lines
+            in2 = sum(1 << h for h in range(4) if (4 * sb0 + (h ^ (g >> 2))) // lines != row1)
             for s in range(16):
                 addr, sb, chunk = placed(lane, s)
                 assert sb < nsb
                 assert addr == 256 * sb + 16 * chunk + 4 * t  # the dense output offset
-                row, e = sb // sbpr, (sb % sbpr) * 256 + 16 * chunk + 4 * t
+                row, e = divmod(addr, K)
+                if G <= 64:
+                    assert row == (row2 if (in2 >> (s >> 2)) & 1 else row1)
                 out[row, e:e + 2] = v[lane, s, 0]
                 out[row, e + 2:e + 4] = v[lane, s, 1]
                 written[row, e:e + 4] += 1
@@ -135,7 +145,10 @@ def replay(X, G):
 
 @pytest.mark.parametrize("K,G,R", [(3072, 256, 4), (6144, 256, 2), (4096, 1024, 1), (4096, 16, 3),
                                    (4096, 64, 1), (1024, 4, 12), (5376, 256, 3), (5376, 64, 3), (1024, 1024, 4),
-                                   (3072, 1024, 1), (5120, 1024, 1)])
+                                   (3072, 1024, 1), (5120, 1024, 1),
+                                   # K not a multiple of 256: superblocks across rows (G <= 64)
+                                   (2688, 64, 6), (2688, 16, 2), (2688, 4, 4), (320, 64, 4), (1088, 64, 4),
+                                   (2688, 64, 8)])
 def test_replayed_layout_is_the_rotation(K, G, R):
     rng = np.random.default_rng(K + G + R)
     X = rng.standard_normal((R, K)).round(3)  # exactly representable sums in fp64
