@@ -153,6 +153,26 @@ def test_tensor_core_kernel_refuses_other_shapes(cr):
         cr.convrot_quantize_act_kernel(Z, 128, "rht", g, kernel="tensor_core")
 
 
+def test_tensor_core_kernel_takes_exactly_the_documented_shapes(cr):
+    """The routing rule of the header (and of the parity helper): asked for
+    by name, the tensor-core kernel runs on exactly the widths and groups the
+    rule names and refuses the rest without launching."""
+    from parity import tensor_core_takes
+    for K in (192, 256, 320, 1088, 2688, 4032, 5376, 6144, 6208, 12288, 12416, 21504, 24576):
+        X = torch.zeros((3, K), dtype=torch.bfloat16, device="cuda")
+        for G in (4, 16, 64, 256, 1024):
+            if K % G:
+                continue
+            if tensor_core_takes(K, G):
+                a = cr.convrot_quantize_act_kernel(X, G, "h4", kernel="tensor_core")
+                assert int(a.q.abs().max()) == 0 and float(a.scale.abs().max()) == 0.0
+            else:
+                with pytest.raises(cr.ConvRotError, match="does not take"):
+                    cr.convrot_quantize_act_kernel(X, G, "h4", kernel="tensor_core")
+    torch.cuda.synchronize()
+    assert cr.convrot_get_device_status() == 0
+
+
 def test_without_f16_copy(cr):
     wl = WL.make_case(20, 3072, [], seed=12)
     a = _run_act(cr, wl.X, 256, "h4", with_f16=False)

@@ -85,3 +85,23 @@ def test_dit_block_layers():
     assert tuple(blk.X.shape) == (8, 256) and tuple(blk.A.shape) == (8, 256)
     assert tuple(blk.fc1.shape) == (1024, 256) and tuple(blk.fc2.shape) == (256, 1024)
     assert blk.group == 256 and blk.transform == "h4" and blk.seed == 6
+
+
+def test_bench_names_the_kernel_the_routing_rule_picks():
+    """bench.py labels its rotate+quantize lines with the kernel the library
+    routes the shape to; that label follows the same rule as the parity
+    tests' helper (the GPU test of the rule itself is in test_gpu_quant)."""
+    import types
+    import bench
+    from parity import tensor_core_takes
+    for K in (192, 256, 320, 1088, 1152, 2688, 3072, 4032, 5376, 6144, 6208, 12288, 12416, 21504, 24576):
+        for G in (4, 16, 64, 256, 1024):
+            if K % G:
+                continue
+            wl = types.SimpleNamespace(K=K, group=G, transform="h4")
+            assert (bench.rq_kernel_name(wl) == "rq_mma_kernel") == tensor_core_takes(K, G), (K, G)
+    # the bench workloads' shapes: DiT, qkv, the group sweep, K = 2688
+    for K, G in ((6144, 256), (3072, 256), (4096, 16), (4096, 1024), (2688, 64)):
+        assert bench.rq_kernel_name(types.SimpleNamespace(K=K, group=G, transform="h4")) == "rq_mma_kernel"
+    ffn = types.SimpleNamespace(K=1152, group=128, transform="rht")  # the small-M FFN pair
+    assert bench.rq_kernel_name(ffn) == "rq_lane_kernel"
