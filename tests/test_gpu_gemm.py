@@ -77,6 +77,32 @@ def test_gemm_s32_adversarial_magnitudes(cr, path, K):
     assert np.abs(ref).max() == 16129 * K
 
 
+@pytest.mark.parametrize("M,K,path", [(300, 32768, "tc"), (300, 32768, "mma"), (40, 32768, "tc"), (8, 32768, "tc"),
+                                      (40, 8192, "tc")])
+def test_gemm_s32_at_the_largest_k(cr, M, K, path):
+    """K up to the largest the library accepts (CONVROT_MAX_K = 32768): all-127
+    rows give |A| = 16129 K = 5.3e8, exact in int32 on every route (the
+    large-M tensor-core GEMM with 32 exact fp32 chunks per tile, the small-M
+    weight stream, the small-M tensor-core kernel at K = 8192, and the int8
+    warp MMA), with random rows between them."""
+    N = 136
+    rng = np.random.default_rng(M + K)
+    Qx = np.full((M, K), 127, dtype=np.int8)
+    Qx[1::2] = -127
+    Qx[2::5, ::3] = 1
+    Qx[3::7] = rng.integers(-127, 128, size=Qx[3::7].shape, dtype=np.int8)
+    Qw = np.full((N, K), 127, dtype=np.int8)
+    Qw[3::4] = -127
+    Qw[5::7, 1::2] = -1
+    Qw[6::9] = rng.integers(-127, 128, size=Qw[6::9].shape, dtype=np.int8)
+    a = packed_from_codes(cr, Qx, np.ones(M), 0, "none", path == "tc", "act")
+    w = packed_from_codes(cr, Qw, np.ones(N), 0, "none", path == "tc", "w")
+    A = to_np(cr.convrot_gemm_s32(a, w, int8_mma=path == "mma")).astype(np.int64)
+    ref = O.int_gemm(Qx, Qw)
+    assert np.abs(ref).max() == 16129 * K
+    assert np.array_equal(A, ref)
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", ["tiny", "dit", "ffn_rht", "g64_2688"])
 def test_linear_on_oracle_codes(cr, path, case):

@@ -173,6 +173,18 @@ def test_tensor_core_kernel_takes_exactly_the_documented_shapes(cr):
     assert cr.convrot_get_device_status() == 0
 
 
+@pytest.mark.parametrize("G", [256, 1024])
+def test_quantize_act_at_the_largest_k(cr, G):
+    """Rows of K = 32768 (CONVROT_MAX_K), wider than any tile of the fast
+    kernels: codes and scales against the oracle."""
+    wl = WL.make_case(3, 32768, [], dist="t3", outlier_frac=0.001, outlier_scale=50.0, group=G, seed=G + 1)
+    a = _run_act(cr, wl.X, G, "h4")
+    Q, s, v = _oracle_act(wl.X, G, "h4")
+    check_codes(to_np(a.q), Q, v, f"K32768 G{G}")
+    check_scales(to_np(a.scale), s, f"K32768 G{G}")
+    assert torch.equal(a.q_f16.float(), a.q.float())
+
+
 def test_without_f16_copy(cr):
     wl = WL.make_case(20, 3072, [], seed=12)
     a = _run_act(cr, wl.X, 256, "h4", with_f16=False)
