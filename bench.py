@@ -935,13 +935,132 @@ def block_main(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+ROWPAR = {"qkv32700_rowpar2": lambda: (WL.qkv32700(), 2)}
+
+
+def rowpar_main(args, world, rank, local):
+    """One rank of a row-parallel (K-sharded) linear group (sglang digest,
+    "风险与影响": each rank holds whole groups of every row): the qkv linears
+    with their 3072 input features split over two ranks. Each rank runs the
+    row maxima of its slice, the quantization of its slice against the
+    all-reduced maxima, its partial int32 accumulators (one launch for the
+    three weights), and after the all-reduced sum the dequant. This GPU runs
+    rank 0's launches, each timed alone and all four back to back; the two
+    all-reduces are exchanges between GPUs and are not part of the time."""
+    import int8_convrot_w8a8_gb300 as cr
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    wl, ranks = ROWPAR[args.workload]()
+    M, K, G, T = wl.M, wl.K, wl.group, wl.transform
+    Kr = K // ranks
+    Xf = wl.X.to(dev)
+    slices = [Xf[:, r * Kr:(r + 1) * Kr] for r in range(ranks)]  # views, row pitch K
+    X = slices[rank % ranks]
+    ws = [cr.convrot_prepare_weights(W.to(dev), G, T) for W in wl.weights]  # offline, whole K
+    cols = slice((rank % ranks) * Kr, (rank % ranks + 1) * Kr)
+    qw = torch.cat([w.q[:, cols] for w in ws]).contiguous()
+    w_cat = cr.PackedWeight(qw, torch.cat([w.scale for w in ws]), qw.to(torch.float16), G, ws[0].transform)
+    b_cat = torch.cat([b.to(dev) for b in wl.biases])
+    N = w_cat.N
+    # the two exchanges, done once outside the timed launches
+    amax_all = torch.stack([cr.convrot_rotate_absmax(x, G, T) for x in slices]).amax(dim=0)
+    amax = torch.empty(M, dtype=torch.float32, device=dev)
+    act = cr.convrot_quantize_act_given_max(X, amax_all, G, T)
+    A = torch.empty((M, N), dtype=torch.int32, device=dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush_l2 = l2_flusher(dev)
+
+    def s_absmax():
+        cr.convrot_rotate_absmax(X, G, T, out=amax)
+
+    def s_quant():
+        cr.convrot_quantize_act_given_max(X, amax_all, G, T, out=act)
+
+    def s_gemm():
+        cr.convrot_gemm_s32(act, w_cat, out=A)
+
+    def s_dequant():
+        cr.convrot_dequant(A, act.scale, w_cat.scale, b_cat, out=Y)
+
+    def s_all():
+        s_absmax()
+        s_quant()
+        s_gemm()
+        s_dequant()
+
+    def timed(fn):
+        marks = []
+        for i in range(args.warmup + args.steps):
+            flush_l2()
+            torch.cuda._sleep(PRE_STEP_SLEEP_CYCLES)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                marks.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in marks) / 1e3
+
+    barrier(world)
+    with ClockSampler(local) as clocks:
+        step_s = timed(s_all)
+    total_s = max_over_ranks(step_s * args.steps, world)
+    parts = {name: timed(fn) for name, fn in
+             (("rotate_absmax", s_absmax), ("quantize_given_max", s_quant), ("gemm_s32", s_gemm),
+              ("dequant", s_dequant))}
+    torch.cuda.synchronize()
+    if cr.convrot_get_device_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    if rank != 0:
+        return
+    pk = peaks()
+    ops = 2.0 * M * N * Kr
+    bytes_ = {"rotate_absmax": 2.0 * M * Kr + 4 * M,
+              "quantize_given_max": 2.0 * M * Kr + 4 * M + 1.0 * M * Kr + 4 * M,
+              "dequant": 4.0 * M * N + 2.0 * M * N + 4 * M + 8 * N}
+    steps = {}
+    for name, t in parts.items():
+        d = {"us": t * 1e6}
+        if name in bytes_:
+            d.update({"algorithmic_bytes": bytes_[name], "gbs": bytes_[name] / t / 1e9,
+                      "frac_of_hbm": bytes_[name] / t / 1e9 / pk["hbm_gbs"]})
+            if name == "quantize_given_max":
+                d["note"] = "int8 codes + scales; the launch also writes the fp16 operand copy the GEMM reads"
+        else:
+            d.update({"tflops": ops / t / 1e12, "frac_of_bf16": ops / t / 1e12 / pk["bf16_tflops"]})
+        steps[name] = d
+    g = parts["gemm_s32"]
+    line = {
+        "metric": METRIC, "value": ops * args.steps / total_s / 1e12, "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": wl.name + f"_rowparallel{ranks}_rank0", "M": M, "K": K, "K_per_rank": Kr, "N": N,
+                   "group": G, "transform": T, "seed": wl.seed, "ranks": ranks,
+                   "l2": "flushed between steps outside the events: 256 MiB write, then 256 MiB read",
+                   "exchanges": "the all-reduce (max) of the row maxima and the all-reduce (sum) of the int32 "
+                                "partial accumulators run between GPUs and are not in the time (one GPU)",
+                   "value": "this rank's 2*M*N*K_per_rank int ops over its four launches back to back"},
+        "roofline": {"kernel": "gemm_tc_kernel", "bound": "tensor", "achieved": ops / g / 1e12,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": ops / g / 1e12 / pk["bf16_tflops"],
+                     "traffic": None, "peak_note": f"{pk['source']} bf16 dense burst (raw int32 output)"},
+        "steps_alone": steps,
+        "gpu_launches": 4 * args.steps,
+        "e2e": None,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="qkv32700", choices=sorted(WORKLOADS) + sorted(BLOCKS))
+    ap.add_argument("--workload", default="qkv32700", choices=sorted(WORKLOADS) + sorted(BLOCKS) + sorted(ROWPAR))
     ap.add_argument("--secondary", default="dit6144", choices=["none"] + sorted(WORKLOADS),
                     help="a second 8-bit workload whose step, GEMM and rotate+quantize times go in the same line")
     ap.add_argument("--no-int8-probe", action="store_true",
@@ -957,11 +1076,13 @@ def main():
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
-            if args.workload in BLOCKS:
+            if args.workload in BLOCKS or args.workload in ROWPAR:
                 ap.error("the reference arm times single-linear workloads")
             reference_main(args, world, rank)
         elif args.workload in BLOCKS:
             block_main(args, world, rank, local)
+        elif args.workload in ROWPAR:
+            rowpar_main(args, world, rank, local)
         else:
             gpu_main(args, world, rank, local)
     finally:

@@ -119,7 +119,7 @@ struct Cfg {
 struct TcParams {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b[kMaxLinears];
-  CUtensorMap tmap_y[kMaxLinears];  // bf16 Y [M, n] for the tiled stores (when y_tma)
+  CUtensorMap tmap_y[kMaxLinears];  // Y [M, n] (bf16, or int32 when RAW) for the tiled stores (when y_tma)
   GemmOutputs outs;
   const float* sx;
   long long M;
@@ -546,7 +546,35 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
         if (lane == 0) atomicExch(p.ws_cnt + slab, 0);
       }
-      if (!RAW && p.y_tma) {
+      if (RAW && p.y_tma) {
+        // raw accumulators: the warp's 32 rows x HALF columns leave in 32 x 8
+        // int32 pieces (32 bytes a row, the bf16 pieces' layout), through the
+        // same two buffers; rows past M and columns past n are clipped
+        const int row0 = m_blk * BM + q * 32;
+        const bool rows_in = row0 < p.M;
+#pragma unroll
+        for (int j = 0; j < C::HALF; j += 8) {
+          if (!rows_in || nb + j >= o.n) continue;  // warp-uniform
+          const uint32_t pb = wout + static_cast<uint32_t>((ob % OUT_BUFS) * OUT_PIECE_BYTES);
+          if (ob >= OUT_BUFS) {
+            if (lane == 0) bulk_wait_read<OUT_BUFS - 1>();
+            __syncwarp();
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + out_row + out_sw), "r"(acc[j]),
+                       "r"(acc[j + 1]), "r"(acc[j + 2]), "r"(acc[j + 3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + out_row + (16u ^ out_sw)), "r"(acc[j + 4]),
+                       "r"(acc[j + 5]), "r"(acc[j + 6]), "r"(acc[j + 7])
+                       : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmap_y[li], pb, nb + j, row0);
+            bulk_commit();
+          }
+          ++ob;
+        }
+      } else if (!RAW && p.y_tma) {
         // The warp's 32 rows x HALF columns leave in 32 x 16 pieces through
         // two buffers; lane 0 issues the stores and, before a buffer is
         // rewritten, waits until the copy issued from it two uses ago has
@@ -775,22 +803,25 @@ cudaError_t launch_bn(EncodeTiledFn enc, const void* Qx16, const float* sx, long
     // in a pair each CTA loads its BN / 2 rows of the B tile
     if (!make_map(enc, &p.tmap_b[i], outs.o[i].qw16, outs.o[i].n, K, BN / CL, F8)) return cudaErrorInvalidValue;
   }
-  // Y through tiled stores when every output allows it: bf16, 16-byte aligned
-  // base and row pitch, at least one full piece wide
-  p.y_tma = RAW ? 0 : 1;
+  // Y through tiled stores when every output allows it: 16-byte aligned base
+  // and row pitch, at least one full piece wide. A piece is 32 rows of 32
+  // bytes: 16 bf16 columns, or 8 int32 columns of raw accumulators.
+  constexpr int y_bytes = RAW ? 4 : 2;
+  constexpr int piece_cols = 32 / y_bytes;
+  p.y_tma = 1;
   for (int i = 0; i < outs.count && p.y_tma; ++i) {
     const GemmOut& o = outs.o[i];
-    if (reinterpret_cast<uintptr_t>(o.y) % 16 != 0 || (o.ldy * 2) % 16 != 0 || o.n < OUT_COLS || M < 32) {
+    if (reinterpret_cast<uintptr_t>(o.y) % 16 != 0 || (o.ldy * y_bytes) % 16 != 0 || o.n < piece_cols || M < 32) {
       p.y_tma = 0;
       break;
     }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.n), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ldy) * 2};
-    cuuint32_t box[2] = {OUT_COLS, 32};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ldy) * y_bytes};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(piece_cols), 32};
     cuuint32_t estr[2] = {1, 1};
-    if (enc(&p.tmap_y[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.y, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (enc(&p.tmap_y[i], RAW ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.y, dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       p.y_tma = 0;
   }
   p.outs = outs;
