@@ -555,8 +555,8 @@ def test_planted_dropped_term_in_gemm_is_caught():
 
 # ------------------------------------------------------------ 4-bit codes --
 # "feat: load ConvRot int4 and per-channel int8 safetensors", "Solution":
+# int4 values occupy [-7, 7], adjacent pairs packed in a byte (nibble order
 # and two's-complement nibbles are a reading of that section, pinned here).
-# and two's-complement nibbles are this build's reading, pinned here).
 
 def pin_int4_bytes(pack):
     # codes (1, -1) -> low nibble 0x1, high nibble 0xF; (7, -7) -> 0x7, 0x9;
