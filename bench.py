@@ -1004,6 +1004,12 @@ def rowpar_main(args, world, rank, local):
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in marks) / 1e3
 
+    if args.profile:
+        # a short, fixed launch list for ncu: the four launches, twice
+        for _ in range(2):
+            s_all()
+        torch.cuda.synchronize()
+        return
     barrier(world)
     with ClockSampler(local) as clocks:
         step_s = timed(s_all)
