@@ -46,6 +46,10 @@ CASES = [
     (16, 1280, [512], WL.TRANSFORM_RHT, 256),
     (16, 1664, [256], WL.TRANSFORM_H4, 64),
     (48, 1152, [256, 136], WL.TRANSFORM_RHT, 128),
+    # large M with K not a multiple of 256: the tensor-core rotate+quantize's
+    # tiles of whole superblocks across rows, writing only the fp16 copy
+    (300, 2688, [256, 136], WL.TRANSFORM_H4, 64),
+    (130, 1088, [200], WL.TRANSFORM_H4, 16),
     (300, 512, [512, 272], WL.TRANSFORM_H4, 64),
     (1000, 1024, [768], WL.TRANSFORM_NONE, 256),
     (4096, 2048, [2048, 1024, 512], WL.TRANSFORM_H4, 256),
